@@ -1,0 +1,208 @@
+"""Ring and double-binary-tree topology, written from the pages' description.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).  Pure-Python integers.
+
+Sources:
+* [Course13] "NCCL 专家课程 13：Tree、双树、层次化连接与真实交叉区间",
+  sections "先固定方向" (up = parent, down[] = children), "数据结构不是纯二叉树"
+  (ncclTree {depth, up, down[3]}), "节点内先形成链" (ncclTopoPreset: the
+  intra-node chain and the head ranks), "节点间连接" (connectTrees: Dtree over
+  the node index, heads joined, the depth formula), "Btree 的 bit 构造"
+  (ncclGetBtree), "双树：偶数 mirror，奇数 shift" (ncclGetDtree).
+* [Interview] "all-reduce 每张卡要发多少数据? ring 和 tree 有什么区别?",
+  section "先弄清楚:每个概念是什么" (ring: every rank sends to its right-hand
+  neighbour; two complementary trees each carry half of the data).
+
+Readings where the pages are silent:
+* setTreeUp / setTreeDown bodies are not shown.  setTreeUp assigns ``up``
+  (nothing when the node-level parent is -1); setTreeDown appends the child to
+  the first -1 slot of ``down[]`` (nothing when the child is -1) and fails past
+  three slots.  Supported by the log "Tree 0 : -1 -> 0 -> 1/-1/-1" (a root's
+  only child sits in slot 0) and by leaf detection through ``down[0] == -1``.
+* With no topology search, the intra-node order ``treeIntra`` is the identity:
+  local rank l of node k is global rank k*L + l, and the head of node k (pattern
+  TREE: parent, child0 and child1 heads are all treeIntra[0]) is k*L.
+* The ring has no physical search either: every channel uses the identity ring.
+* Channel -> tree: the channel metadata is duplicated so that one copy joins
+  tree 0 and the other tree 1, each carrying half the data.  Channels
+  [0, ceil(nCh/2)) use tree 0, the rest tree 1; one channel uses tree 0 only.
+"""
+
+from dataclasses import dataclass, field
+from typing import List
+
+
+# ------------------------------------------------------------------- ring
+def build_ring(R, n_channels):
+    """Identity ring for every channel: next = r+1, prev = r-1 (mod R).
+    Returns (next, prev), each a list of n_channels lists of R ints."""
+    if R < 1 or n_channels < 1:
+        raise ValueError("R and n_channels must be >= 1")
+    nxt = [[(r + 1) % R for r in range(R)] for _ in range(n_channels)]
+    prv = [[(r - 1 + R) % R for r in range(R)] for _ in range(n_channels)]
+    return nxt, prv
+
+
+# ------------------------------------------------------------------ trees
+def btree(n, r):
+    """Node r of the bit-trick binary tree over n nodes.
+
+    The lowest set bit b of r (scanning b = 1, 2, 4, ... while b < n) fixes
+    r's level.  Node 0 is the root; its single child is the largest power of
+    two below n.  Any other node's parent clears b and sets the next bit up,
+    falling back to only clearing b when that leaves the range.  Its children
+    sit b/2 below and b/2 above; the upper child is pulled closer by halving
+    the offset until it lands inside the range, and disappears at offset 0.
+    parentChildType is 0 when r lies below its parent, else 1 (-1 for the
+    root, whose type the page's routine leaves unset).
+
+    Returns (up, d0, d1, parentChildType)."""
+    if not (0 <= r < n):
+        raise ValueError("rank %d outside [0, %d)" % (r, n))
+    b = 1
+    while b < n and not (b & r):
+        b <<= 1
+    if r == 0:
+        return (-1, -1, (b >> 1) if n > 1 else -1, -1)
+    up = (r ^ b) | (b << 1)
+    if up >= n:
+        up = r ^ b
+    ptype = 0 if r < up else 1
+    low = b >> 1
+    d0 = r - low if low else -1
+    d1 = r + low if low else -1
+    # The page's loop recomputes the candidate before halving the offset, so
+    # its first pass repeats the same value; follow it as written.
+    while d1 >= n:
+        d1 = r + low if low else -1
+        low >>= 1
+    return (up, d0, d1, ptype)
+
+
+def dtree(n, r):
+    """The two node-level trees of node r: tree 0 is btree(n, r); tree 1 is
+    btree of a relabelled node mapped back -- mirror r -> n-1-r for even n,
+    shift r -> r-1 (mod n) for odd n, with the outputs mapped back by the
+    inverse relabelling (-1 stays -1, slot order kept).
+
+    Returns ((u0, d0_0, d0_1, t0), (u1, d1_0, d1_1, t1))."""
+    t0 = btree(n, r)
+    if n % 2 == 1:
+        u, a, b, t = btree(n, (r - 1 + n) % n)
+        back = lambda x: -1 if x == -1 else (x + 1) % n  # noqa: E731
+    else:
+        u, a, b, t = btree(n, n - 1 - r)
+        back = lambda x: -1 if x == -1 else n - 1 - x  # noqa: E731
+    return t0, (back(u), back(a), back(b), t)
+
+
+def log2i(n):
+    """floor(log2 n) for n >= 1."""
+    k = 0
+    while n > 1:
+        n >>= 1
+        k += 1
+    return k
+
+
+@dataclass
+class Tree:
+    """One rank's view of one tree, the ncclTree record."""
+    depth: int
+    up: int
+    down: List[int] = field(default_factory=lambda: [-1, -1, -1])
+
+
+def _set_up(t, parent):
+    if parent != -1:
+        t.up = parent
+
+
+def _set_down(t, child):
+    if child == -1:
+        return
+    for s in range(3):
+        if t.down[s] == -1:
+            t.down[s] = child
+            return
+    raise RuntimeError("more than three children")
+
+
+def channel_tree_index(channel, n_channels):
+    """0 for the first half of the channels (rounded up), 1 for the rest."""
+    return 0 if channel < (n_channels + 1) // 2 else 1
+
+
+def build_dtree(n_nodes, local_ranks, n_channels):
+    """Per channel and rank, the hierarchical double-binary-tree record.
+
+    Step 1 (preset): each node's ranks form a chain in local order, up = the
+    previous local rank, down[0] = the next one.  Step 2 (connect): the
+    node-level double tree over node indices (not rank indices) is attached
+    to the heads: the head of node k gets up = head of its parent node and
+    appends the heads of its child nodes d0 then d1 to down[].  Every rank's
+    depth is L - 1 + floor(log2 nNodes), the page's approximation.
+
+    Returns trees[channel][rank] -> Tree."""
+    if n_nodes < 1 or local_ranks < 1 or n_channels < 1:
+        raise ValueError("sizes must be >= 1")
+    L = local_ranks
+    R = n_nodes * L
+    depth = L - 1 + log2i(n_nodes)
+    node_trees = [dtree(n_nodes, k) for k in range(n_nodes)]
+    out = []
+    for c in range(n_channels):
+        t_idx = channel_tree_index(c, n_channels)
+        per_rank = []
+        for rank in range(R):
+            k, l = divmod(rank, L)
+            t = Tree(depth=depth,
+                     up=-1 if l == 0 else rank - 1,
+                     down=[-1 if l == L - 1 else rank + 1, -1, -1])
+            if l == 0:
+                u, d0, d1, _ = node_trees[k][t_idx]
+                _set_up(t, -1 if u == -1 else u * L)
+                _set_down(t, -1 if d0 == -1 else d0 * L)
+                _set_down(t, -1 if d1 == -1 else d1 * L)
+            per_rank.append(t)
+        out.append(per_rank)
+    return out
+
+
+# ------------------------------------------------------- tree inspection
+def root_of(trees_one_channel):
+    roots = [r for r, t in enumerate(trees_one_channel) if t.up == -1]
+    return roots
+
+
+def exact_depth(trees_one_channel):
+    """Edges from the root to the deepest leaf (walks every rank to the root)."""
+    worst = 0
+    for r in range(len(trees_one_channel)):
+        d, v, seen = 0, r, set()
+        while trees_one_channel[v].up != -1:
+            if v in seen:
+                raise RuntimeError("cycle")
+            seen.add(v)
+            v = trees_one_channel[v].up
+            d += 1
+        worst = max(worst, d)
+    return worst
+
+
+def internal_nodes(trees_one_channel):
+    """Non-leaf ranks, the root included."""
+    return {r for r, t in enumerate(trees_one_channel) if any(c != -1 for c in t.down)}
+
+
+def format_tree_log(trees_one_channel, channel, style="arrow"):
+    """The two log line styles the pages quote: "Tree c : up -> rank ->
+    d0/d1/d2" and "Trees [c] d0/d1/d2->rank->up", one line per rank."""
+    lines = []
+    for r, t in enumerate(trees_one_channel):
+        kids = "/".join(str(x) for x in t.down)
+        if style == "arrow":
+            lines.append("Tree %d : %d -> %d -> %s" % (channel, t.up, r, kids))
+        else:
+            lines.append("Trees [%d] %s->%d->%d" % (channel, kids, r, t.up))
+    return lines
