@@ -1,0 +1,178 @@
+"""Python binding of libvr.so (include/vr.h): argument marshalling only.
+
+Every function keeps the C name and argument order.  Buffer arguments take
+sequences of device pointers (ints) or of torch tensors (their data_ptr() is
+passed); streams take a cudaStream_t as an int, a torch.cuda.Stream, or None
+for the legacy default stream.  A non-zero result code raises VrError.
+
+The compute path is the CUDA library only: importing this package fails
+loudly when libvr.so has not been built for this machine (build it with
+``python -m double_binary_tree_gb300.build`` or ``__graft_entry__.build()``).
+"""
+
+import ctypes
+import os
+
+from .build import LIB, is_fresh
+
+VR_SUCCESS, VR_ERR_INVALID_ARGUMENT, VR_ERR_UNSUPPORTED = 0, 1, 2
+VR_ERR_CUDA, VR_ERR_TIMEOUT, VR_ERR_INTERNAL = 3, 4, 5
+VR_FLOAT32, VR_FLOAT16, VR_BFLOAT16 = 0, 1, 2
+VR_SUM, VR_MAX = 0, 1
+VR_ALGO_RING, VR_ALGO_TREE = 0, 1
+VR_MAX_RANKS = 64
+VR_MAX_CHANNELS = 64
+ELEM_SIZE = {VR_FLOAT32: 4, VR_FLOAT16: 2, VR_BFLOAT16: 2}
+
+
+class VrError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__("%s: %s (%d)" % (where, _lib.vr_get_error_string(code).decode(), code))
+
+
+class vr_tree_t(ctypes.Structure):
+    _fields_ = [("depth", ctypes.c_int), ("up", ctypes.c_int), ("down", ctypes.c_int * 3)]
+
+
+def _load():
+    if not os.path.exists(LIB):
+        raise ImportError("libvr.so is not built: run python -m double_binary_tree_gb300.build")
+    if not is_fresh():
+        raise ImportError("libvr.so is older than its sources or built for another machine: "
+                          "run python -m double_binary_tree_gb300.build")
+    lib = ctypes.CDLL(LIB)
+    P, I, S, VP = ctypes.POINTER, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+    PP = P(VP)
+    sig = {
+        "vr_build_ring": (I, [I, I, P(I), P(I)]),
+        "vr_build_dtree": (I, [I, I, I, P(vr_tree_t)]),
+        "vr_partition": (I, [S, I, I, I, P(S), P(S)]),
+        "vr_ring_block": (I, [S, I, I, I, S, S, P(I), P(I)]),
+        "vr_allreduce": (I, [PP, PP, I, S, I, I, I, I, S, VP]),
+        "vr_allreduce_ex": (I, [PP, PP, I, S, I, I, I, I, S, I, VP]),
+        "vr_reduce_scatter": (I, [PP, PP, I, S, I, I, I, I, S, VP]),
+        "vr_allgather": (I, [PP, PP, I, S, I, I, I, S, VP]),
+        "vr_stream_status": (I, [VP]),
+        "vr_launch_count": (ctypes.c_ulonglong, []),
+        "vr_get_error_string": (ctypes.c_char_p, [I]),
+        "vr_finalize": (None, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib, sig
+
+
+_lib, _SIGNATURES = _load()
+EXPORTED = tuple(_SIGNATURES)
+
+
+def _check(code, where):
+    if code != VR_SUCCESS:
+        raise VrError(code, where)
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _ptrs(bufs):
+    if bufs is None:
+        return None
+    return (ctypes.c_void_p * len(bufs))(*[_ptr(b) for b in bufs])
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+# ------------------------------------------------------------- topology
+def vr_build_ring(R, nChannels):
+    """Returns (next, prev) as lists of nChannels*R ints."""
+    n = (ctypes.c_int * (R * nChannels))() if R > 0 and nChannels > 0 else None
+    p = (ctypes.c_int * (R * nChannels))() if R > 0 and nChannels > 0 else None
+    _check(_lib.vr_build_ring(R, nChannels, n, p), "vr_build_ring")
+    return list(n), list(p)
+
+
+def vr_build_dtree(nNodes, localRanks, nChannels):
+    """Returns nChannels*nNodes*localRanks vr_tree_t records, [c*R + r]."""
+    R = nNodes * localRanks
+    size = max(R * nChannels, 1)
+    out = (vr_tree_t * size)()
+    _check(_lib.vr_build_dtree(nNodes, localRanks, nChannels, out), "vr_build_dtree")
+    return list(out)[:R * nChannels]
+
+
+def vr_partition(count, dtype, nChannels, channel):
+    """Returns (offset, channelCount)."""
+    off, n = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(_lib.vr_partition(count, dtype, nChannels, channel, ctypes.byref(off), ctypes.byref(n)),
+           "vr_partition")
+    return off.value, n.value
+
+
+def vr_ring_block(count, dtype, R, nChannels, chunkBytes, elem):
+    """Returns (channel, block) of element `elem`."""
+    c, b = ctypes.c_int(), ctypes.c_int()
+    _check(_lib.vr_ring_block(count, dtype, R, nChannels, chunkBytes, elem, ctypes.byref(c),
+                              ctypes.byref(b)), "vr_ring_block")
+    return c.value, b.value
+
+
+# ---------------------------------------------------------- collectives
+def vr_allreduce(sendbufs, recvbufs, R, count, dtype, op, algo, nChannels, chunkBytes,
+                 stream=None):
+    _check(_lib.vr_allreduce(_ptrs(sendbufs), _ptrs(recvbufs), R, count, dtype, op, algo,
+                             nChannels, chunkBytes, _stream(stream)), "vr_allreduce")
+
+
+def vr_allreduce_ex(sendbufs, recvbufs, R, count, dtype, op, algo, nChannels, chunkBytes,
+                    localRanks, stream=None):
+    _check(_lib.vr_allreduce_ex(_ptrs(sendbufs), _ptrs(recvbufs), R, count, dtype, op, algo,
+                                nChannels, chunkBytes, localRanks, _stream(stream)),
+           "vr_allreduce_ex")
+
+
+def vr_reduce_scatter(sendbufs, recvbufs, R, recvcount, dtype, op, algo, nChannels, chunkBytes,
+                      stream=None):
+    _check(_lib.vr_reduce_scatter(_ptrs(sendbufs), _ptrs(recvbufs), R, recvcount, dtype, op,
+                                  algo, nChannels, chunkBytes, _stream(stream)),
+           "vr_reduce_scatter")
+
+
+def vr_allgather(sendbufs, recvbufs, R, sendcount, dtype, algo, nChannels, chunkBytes,
+                 stream=None):
+    _check(_lib.vr_allgather(_ptrs(sendbufs), _ptrs(recvbufs), R, sendcount, dtype, algo,
+                             nChannels, chunkBytes, _stream(stream)), "vr_allgather")
+
+
+def vr_stream_status(stream=None):
+    """Synchronises the stream and returns the device status code (0 = ok)."""
+    return _lib.vr_stream_status(_stream(stream))
+
+
+def vr_launch_count():
+    return _lib.vr_launch_count()
+
+
+def vr_get_error_string(code):
+    return _lib.vr_get_error_string(code).decode()
+
+
+def vr_finalize():
+    _lib.vr_finalize()
+
+
+def library_path():
+    return LIB

@@ -1,0 +1,361 @@
+// The C ABI of include/vr.h: argument checks, host planning and one kernel
+// launch per collective call.
+#include <algorithm>
+#include <array>
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "host.h"
+
+namespace vr {
+namespace {
+
+constexpr int kBlockThreads = 256;  // must equal kBlock of kernels.cuh
+
+std::atomic<unsigned long long> g_launches{0};
+std::mutex g_mu;
+
+struct DeviceInfo {
+  int sms = 0;
+  unsigned* status = nullptr;
+};
+std::map<int, DeviceInfo> g_devices;                             // by device ordinal
+std::map<std::pair<const void*, int>, int> g_occupancy;          // (kernel, device)
+std::map<std::pair<int, int>, std::array<FoldProg, 2>> g_progs;  // (nNodes, localRanks)
+
+size_t elem_size(int dtype) {
+  switch (dtype) {
+    case VR_FLOAT32: return 4;
+    case VR_FLOAT16:
+    case VR_BFLOAT16: return 2;
+    default: return 0;
+  }
+}
+
+vr_result_t device_info(DeviceInfo* out, int* device) {
+  if (cudaGetDevice(device) != cudaSuccess) return VR_ERR_CUDA;
+  std::lock_guard<std::mutex> g(g_mu);
+  auto it = g_devices.find(*device);
+  if (it == g_devices.end()) {
+    DeviceInfo d;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, *device) != cudaSuccess)
+      return VR_ERR_CUDA;
+    if (status_word_address(&d.status) != cudaSuccess) return VR_ERR_CUDA;
+    it = g_devices.emplace(*device, d).first;
+  }
+  *out = it->second;
+  return VR_SUCCESS;
+}
+
+int blocks_per_sm(const void* fn, int device) {
+  std::lock_guard<std::mutex> g(g_mu);
+  auto key = std::make_pair(fn, device);
+  auto it = g_occupancy.find(key);
+  if (it != g_occupancy.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kBlockThreads, 0) != cudaSuccess || n < 1)
+    n = 1;
+  g_occupancy[key] = n;
+  return n;
+}
+
+vr_result_t tree_programs(int nNodes, int L, std::array<FoldProg, 2>* out) {
+  std::lock_guard<std::mutex> g(g_mu);
+  auto key = std::make_pair(nNodes, L);
+  auto it = g_progs.find(key);
+  if (it == g_progs.end()) {
+    const int R = nNodes * L;
+    vr_tree_t trees[2 * kMaxRanks];
+    vr_result_t e = build_dtree(nNodes, L, 2, trees);  // channel 0: tree 0, channel 1: tree 1
+    if (e != VR_SUCCESS) return e;
+    std::array<FoldProg, 2> p;
+    for (int t = 0; t < 2; ++t) {
+      e = compile_fold(trees + t * R, R, &p[t]);
+      if (e != VR_SUCCESS) return e;
+    }
+    it = g_progs.emplace(key, p).first;
+  }
+  *out = it->second;
+  return VR_SUCCESS;
+}
+
+bool overlap(uintptr_t a, size_t an, uintptr_t b, size_t bn) {
+  return an && bn && a < b + bn && b < a + an;
+}
+
+// Buffer rules shared by the collectives.  recv[r] may not touch another
+// rank's send or recv buffer; against its own send buffer it is either
+// disjoint or in the collective's in-place position: recv == send + recvAt
+// (AllReduce: 0, ReduceScatter: r * recvBytes) or send == recv + sendAt
+// (AllGather: r * sendBytes).
+enum Kind { kAR, kRS, kAG };
+vr_result_t check_buffers(const void* const* send, void* const* recv, int R, size_t sendBytes,
+                          size_t recvBytes, Kind kind) {
+  if (!send || !recv) return VR_ERR_INVALID_ARGUMENT;
+  for (int r = 0; r < R; ++r)
+    if ((sendBytes && !send[r]) || (recvBytes && !recv[r])) return VR_ERR_INVALID_ARGUMENT;
+  for (int r = 0; r < R; ++r) {
+    const uintptr_t s = (uintptr_t)send[r], d = (uintptr_t)recv[r];
+    bool inPlace = false;
+    if (kind == kAR) inPlace = d == s;
+    if (kind == kRS) inPlace = d == s + (uintptr_t)r * recvBytes;
+    if (kind == kAG) inPlace = s == d + (uintptr_t)r * sendBytes;
+    if (!inPlace && overlap(s, sendBytes, d, recvBytes)) return VR_ERR_INVALID_ARGUMENT;
+    for (int q = 0; q < R; ++q) {
+      if (q == r) continue;
+      if (overlap(d, recvBytes, (uintptr_t)recv[q], recvBytes)) return VR_ERR_INVALID_ARGUMENT;
+      if (overlap(d, recvBytes, (uintptr_t)send[q], sendBytes)) return VR_ERR_INVALID_ARGUMENT;
+    }
+  }
+  return VR_SUCCESS;
+}
+
+// Optional (VR_VALIDATE_POINTERS=1): every buffer must be reachable from the
+// current device.  Off by default: it costs a driver query per buffer.
+vr_result_t check_reachable(const void* const* ptrs, int R, int device) {
+  static const bool on = [] {
+    const char* v = std::getenv("VR_VALIDATE_POINTERS");
+    return v && v[0] == '1';
+  }();
+  if (!on) return VR_SUCCESS;
+  for (int r = 0; r < R; ++r) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, ptrs[r]) != cudaSuccess) {
+      cudaGetLastError();
+      return VR_ERR_INVALID_ARGUMENT;
+    }
+    if (at.type == cudaMemoryTypeUnregistered) return VR_ERR_INVALID_ARGUMENT;
+    if (at.type == cudaMemoryTypeDevice && at.device != device) return VR_ERR_INVALID_ARGUMENT;
+    if (at.type == cudaMemoryTypeHost && at.devicePointer == nullptr) return VR_ERR_INVALID_ARGUMENT;
+  }
+  return VR_SUCCESS;
+}
+
+bool aligned16(const void* const* p, int R, size_t extraStride) {
+  for (int r = 0; r < R; ++r)
+    if (((uintptr_t)p[r] | extraStride) & 15) return false;
+  return true;
+}
+
+const void* pick_kernel(int dtype, int mode, int op, bool vec, int stack = 0) {
+  switch (dtype) {
+    case VR_FLOAT32: return kernel_ptr_f32(mode, op, vec, stack);
+    case VR_FLOAT16: return kernel_ptr_f16(mode, op, vec, stack);
+    case VR_BFLOAT16: return kernel_ptr_bf16(mode, op, vec, stack);
+    default: return nullptr;
+  }
+}
+
+vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream) {
+  if (!fn) return VR_ERR_INTERNAL;
+  DeviceInfo di;
+  int device = 0;
+  vr_result_t e = device_info(&di, &device);
+  if (e != VR_SUCCESS) return e;
+  if ((e = check_reachable(a.src, a.R, device)) != VR_SUCCESS) return e;
+  if ((e = check_reachable(const_cast<const void* const*>(a.dst), a.R, device)) != VR_SUCCESS)
+    return e;
+  a.status = di.status;
+  const long long resident = (long long)di.sms * blocks_per_sm(fn, device);
+  const long long wanted = (units + kBlockThreads - 1) / kBlockThreads;
+  const int grid = (int)std::max(1LL, std::min(resident, wanted));
+  void* args[] = {&a};
+  if (cudaLaunchKernel(fn, dim3(grid), dim3(kBlockThreads), args, 0, (cudaStream_t)stream) !=
+      cudaSuccess)
+    return VR_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return VR_SUCCESS;
+}
+
+bool valid_common(int R, int dtype, int nChannels, size_t chunkBytes) {
+  return R >= 1 && R <= kMaxRanks && elem_size(dtype) && nChannels >= 1 &&
+         nChannels <= kMaxChannels && chunkBytes > 0 && chunkBytes % kGrainBytes == 0;
+}
+
+void fill_partition(KArgs& a, size_t count, size_t E, int nCh, size_t chunkBytes) {
+  a.count = (long long)count;
+  const long long U = kGrainBytes / (long long)E;
+  a.grains = ((long long)count + U - 1) / U;
+  a.gq = a.grains / nCh;
+  a.gm = a.grains % nCh;
+  a.chunk = (long long)(chunkBytes / E);
+  a.nCh = nCh;
+}
+
+}  // namespace
+}  // namespace vr
+
+using namespace vr;
+
+extern "C" {
+
+vr_result_t vr_build_ring(int R, int nChannels, int* next, int* prev) {
+  if (R < 1 || R > kMaxRanks || nChannels < 1 || nChannels > kMaxChannels || !next || !prev)
+    return VR_ERR_INVALID_ARGUMENT;
+  for (int c = 0; c < nChannels; ++c)
+    for (int r = 0; r < R; ++r) {
+      next[c * R + r] = (r + 1) % R;
+      prev[c * R + r] = (r + R - 1) % R;
+    }
+  return VR_SUCCESS;
+}
+
+vr_result_t vr_build_dtree(int nNodes, int localRanks, int nChannels, vr_tree_t* trees) {
+  if (nNodes < 1 || localRanks < 1 || nNodes > kMaxRanks || localRanks > kMaxRanks ||
+      nNodes * localRanks > kMaxRanks || nChannels < 1 || nChannels > kMaxChannels || !trees)
+    return VR_ERR_INVALID_ARGUMENT;
+  return build_dtree(nNodes, localRanks, nChannels, trees);
+}
+
+vr_result_t vr_partition(size_t count, vr_dtype_t dtype, int nChannels, int channel,
+                         size_t* offset, size_t* channelCount) {
+  const size_t E = elem_size(dtype);
+  if (!E || nChannels < 1 || nChannels > kMaxChannels || channel < 0 || channel >= nChannels ||
+      !offset || !channelCount)
+    return VR_ERR_INVALID_ARGUMENT;
+  const size_t U = kGrainBytes / E;
+  const size_t grains = (count + U - 1) / U;
+  const size_t q = grains / nChannels, m = grains % nChannels;
+  const size_t gs = channel * q + std::min<size_t>(channel, m);
+  const size_t gl = q + ((size_t)channel < m ? 1 : 0);
+  const size_t s = std::min(count, gs * U), e = std::min(count, (gs + gl) * U);
+  *offset = s;
+  *channelCount = e - s;
+  return VR_SUCCESS;
+}
+
+vr_result_t vr_ring_block(size_t count, vr_dtype_t dtype, int R, int nChannels,
+                          size_t chunkBytes, size_t elem, int* channel, int* block) {
+  if (!valid_common(R, dtype, nChannels, chunkBytes) || elem >= count || !channel || !block)
+    return VR_ERR_INVALID_ARGUMENT;
+  const size_t E = elem_size(dtype), C = chunkBytes / E;
+  for (int c = 0; c < nChannels; ++c) {
+    size_t s, n;
+    vr_partition(count, dtype, nChannels, c, &s, &n);
+    if (elem < s || elem >= s + n) continue;
+    const size_t LC = (size_t)R * C, off = elem - s;
+    const size_t ls = off / LC * LC, L = std::min(LC, n - ls), w = off - ls;
+    const size_t q = L / R, m = L % R;
+    *channel = c;
+    *block = (int)(w < m * (q + 1) ? w / (q + 1) : m + (w - m * (q + 1)) / q);
+    return VR_SUCCESS;
+  }
+  return VR_ERR_INTERNAL;
+}
+
+vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, int R,
+                            size_t count, vr_dtype_t dtype, vr_op_t op, vr_algo_t algo,
+                            int nChannels, size_t chunkBytes, int localRanks, void* stream) {
+  if (!valid_common(R, dtype, nChannels, chunkBytes) || (op != VR_SUM && op != VR_MAX) ||
+      (algo != VR_ALGO_RING && algo != VR_ALGO_TREE) || localRanks < 1 || R % localRanks)
+    return VR_ERR_INVALID_ARGUMENT;
+  const size_t E = elem_size(dtype);
+  vr_result_t e = check_buffers(sendbufs, recvbufs, R, count * E, count * E, kAR);
+  if (e != VR_SUCCESS || count == 0) return e;
+  KArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.R = R;
+  for (int r = 0; r < R; ++r) { a.src[r] = sendbufs[r]; a.dst[r] = recvbufs[r]; }
+  fill_partition(a, count, E, nChannels, chunkBytes);
+  int mode = kRingAllReduce, stack = 0;
+  if (algo == VR_ALGO_TREE) {
+    mode = kTreeAllReduce;
+    std::array<FoldProg, 2> p;
+    if ((e = tree_programs(R / localRanks, localRanks, &p)) != VR_SUCCESS) return e;
+    a.prog[0] = p[0];
+    a.prog[1] = p[1];
+    a.treeSplit = (nChannels + 1) / 2;
+    stack = std::max(p[0].depth, p[1].depth);
+  }
+  const bool vec = aligned16(sendbufs, R, 0) && aligned16(recvbufs, R, 0);
+  const long long NV = vec ? kGrainBytes / (long long)E : 1;
+  return launch(pick_kernel(dtype, mode, op, vec, stack), a, ((long long)count + NV - 1) / NV,
+                stream);
+}
+
+vr_result_t vr_allreduce(const void* const* sendbufs, void* const* recvbufs, int R, size_t count,
+                         vr_dtype_t dtype, vr_op_t op, vr_algo_t algo, int nChannels,
+                         size_t chunkBytes, void* stream) {
+  return vr_allreduce_ex(sendbufs, recvbufs, R, count, dtype, op, algo, nChannels, chunkBytes, 1,
+                         stream);
+}
+
+vr_result_t vr_reduce_scatter(const void* const* sendbufs, void* const* recvbufs, int R,
+                              size_t recvcount, vr_dtype_t dtype, vr_op_t op, vr_algo_t algo,
+                              int nChannels, size_t chunkBytes, void* stream) {
+  if (!valid_common(R, dtype, nChannels, chunkBytes) || (op != VR_SUM && op != VR_MAX) ||
+      (algo != VR_ALGO_RING && algo != VR_ALGO_TREE))
+    return VR_ERR_INVALID_ARGUMENT;
+  if (algo == VR_ALGO_TREE) return VR_ERR_UNSUPPORTED;
+  const size_t E = elem_size(dtype);
+  vr_result_t e = check_buffers(sendbufs, recvbufs, R, (size_t)R * recvcount * E, recvcount * E, kRS);
+  if (e != VR_SUCCESS || recvcount == 0) return e;
+  KArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.R = R;
+  for (int r = 0; r < R; ++r) { a.src[r] = sendbufs[r]; a.dst[r] = recvbufs[r]; }
+  a.count = (long long)recvcount;
+  a.nCh = nChannels;
+  a.chunk = (long long)(chunkBytes / E);
+  const bool vec = aligned16(sendbufs, R, recvcount * E) && aligned16(recvbufs, R, 0);
+  const long long NV = vec ? kGrainBytes / (long long)E : 1;
+  const long long units = (long long)R * (((long long)recvcount + NV - 1) / NV);
+  return launch(pick_kernel(dtype, kReduceScatter, op, vec), a, units, stream);
+}
+
+vr_result_t vr_allgather(const void* const* sendbufs, void* const* recvbufs, int R,
+                         size_t sendcount, vr_dtype_t dtype, vr_algo_t algo, int nChannels,
+                         size_t chunkBytes, void* stream) {
+  if (!valid_common(R, dtype, nChannels, chunkBytes) ||
+      (algo != VR_ALGO_RING && algo != VR_ALGO_TREE))
+    return VR_ERR_INVALID_ARGUMENT;
+  if (algo == VR_ALGO_TREE) return VR_ERR_UNSUPPORTED;
+  const size_t bytes = sendcount * elem_size(dtype);
+  vr_result_t e = check_buffers(sendbufs, recvbufs, R, bytes, (size_t)R * bytes, kAG);
+  if (e != VR_SUCCESS || sendcount == 0) return e;
+  KArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.R = R;
+  for (int r = 0; r < R; ++r) { a.src[r] = sendbufs[r]; a.dst[r] = recvbufs[r]; }
+  a.count = (long long)bytes;
+  a.nCh = nChannels;
+  const bool vec = aligned16(sendbufs, R, bytes) && aligned16(recvbufs, R, 0);
+  const long long NB = vec ? kGrainBytes : 1;
+  const long long units = (long long)R * (((long long)bytes + NB - 1) / NB);
+  return launch(kernel_ptr_allgather(vec), a, units, stream);
+}
+
+vr_result_t vr_stream_status(void* stream) {
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return VR_ERR_CUDA;
+  unsigned v = 0;
+  if (read_and_clear_status(&v) != cudaSuccess) return VR_ERR_CUDA;
+  return (vr_result_t)v;
+}
+
+unsigned long long vr_launch_count(void) { return g_launches.load(); }
+
+const char* vr_get_error_string(vr_result_t result) {
+  switch (result) {
+    case VR_SUCCESS: return "success";
+    case VR_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case VR_ERR_UNSUPPORTED: return "unsupported combination";
+    case VR_ERR_CUDA: return "CUDA runtime error";
+    case VR_ERR_TIMEOUT: return "device-side wait timed out";
+    case VR_ERR_INTERNAL: return "internal error";
+    default: return "unknown result";
+  }
+}
+
+void vr_finalize(void) {
+  std::lock_guard<std::mutex> g(g_mu);
+  g_progs.clear();
+  g_occupancy.clear();
+  g_devices.clear();
+}
+
+}  // extern "C"

@@ -1,0 +1,49 @@
+// Internal types shared by the host planner and the kernels.
+#pragma once
+
+#include <stdint.h>
+
+#include "../../include/vr.h"
+
+namespace vr {
+
+constexpr int kMaxRanks = VR_MAX_RANKS;
+constexpr int kMaxChannels = VR_MAX_CHANNELS;
+constexpr int kGrainBytes = 16;      // channel ranges are cut in 16-byte grains
+constexpr int kMaxStack = 8;         // partial sums a tree fold keeps live at once
+
+// A tree's reduction order as a stream of rank loads.  Slot i loads rank
+// rank[i]; before it, ctl[i] & 15 "pop-add" steps fold the top partial into
+// the one below it; then the loaded value is pushed as a new partial
+// (ctl[i] & 16) or folded into the top partial.  `tail` pop-adds close the
+// stream, leaving the root's value as the only partial.
+struct alignas(4) FoldProg {
+  uint8_t rank[kMaxRanks];
+  uint8_t ctl[kMaxRanks];
+  uint8_t n;      // == R
+  uint8_t tail;
+  uint8_t depth;  // deepest partial stack the stream needs
+  uint8_t pad;
+};
+
+enum Mode : int { kRingAllReduce = 0, kTreeAllReduce = 1, kReduceScatter = 2, kAllGather = 3 };
+
+// Everything a collective kernel needs, passed by value as the kernel
+// parameter (about 1.2 KB).
+struct KArgs {
+  const void* src[kMaxRanks];
+  void* dst[kMaxRanks];
+  long long count;      // AllReduce: elements per rank; ReduceScatter: recvcount;
+                        // AllGather: sendcount in bytes
+  long long grains;     // AllReduce: 16-byte grains of the message
+  long long gq, gm;     // grains / nChannels, grains % nChannels
+  long long chunk;      // C, elements per rank per ring loop block
+  int R;
+  int nCh;
+  int treeSplit;        // channels [0, treeSplit) follow prog[0], the rest prog[1]
+  int pad;
+  unsigned* status;     // this device's status word
+  FoldProg prog[2];
+};
+
+}  // namespace vr

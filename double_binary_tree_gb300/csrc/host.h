@@ -1,0 +1,29 @@
+// Host-side planning functions and kernel launchers (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.h"
+
+namespace vr {
+
+void btree(int n, int r, int* up, int* d0, int* d1, int* childType);
+void dtree(int n, int r, int t[2][4]);
+int channel_tree(int c, int nCh);
+vr_result_t build_dtree(int nNodes, int L, int nCh, vr_tree_t* out);
+vr_result_t compile_fold(const vr_tree_t* tree, int R, FoldProg* prog);
+
+// Kernel entry points, one getter per element type: `mode` is a Mode,
+// `vec` selects the 16-byte vector path (all buffers and block offsets
+// 16-byte aligned), else the element path; `stack` is the deepest partial
+// stack of the tree programs (selects the 4- or 8-slot tree kernel).
+const void* kernel_ptr_f32(int mode, int op, bool vec, int stack);
+const void* kernel_ptr_f16(int mode, int op, bool vec, int stack);
+const void* kernel_ptr_bf16(int mode, int op, bool vec, int stack);
+const void* kernel_ptr_allgather(bool vec);
+
+// The current device's status word: its address, and read-and-clear.
+cudaError_t status_word_address(unsigned** p);
+cudaError_t read_and_clear_status(unsigned* value);
+
+}  // namespace vr

@@ -1,0 +1,171 @@
+// Ring and double-binary-tree topology of the emulated ranks, and the fold
+// programs the tree kernel executes.
+//
+// Sources (web pages):
+//   [Course13] "NCCL 专家课程 13：Tree、双树、层次化连接与真实交叉区间" (blog.cptz.space),
+//     sections "数据结构不是纯二叉树" (ncclTree record), "节点内先形成链"
+//     (ncclTopoPreset: intra-node chain, head ranks, channel duplication),
+//     "节点间连接" (connectTrees: the double tree is built over node indices
+//     and attached to the heads; depth approximation), "Btree 的 bit 构造"
+//     (ncclGetBtree), "双树：偶数 mirror，奇数 shift" (ncclGetDtree),
+//     "先固定方向" (reduce: receive from down[], reduce the local input, send up).
+//   [Interview] "all-reduce 每张卡要发多少数据? ring 和 tree 有什么区别?",
+//     section "先弄清楚:每个概念是什么" (ring neighbours; two trees, half the
+//     data each).
+#include <cstring>
+
+#include "common.h"
+#include "host.h"
+
+namespace vr {
+
+// Bit-trick binary tree over n nodes, node r.  The lowest set bit b of r
+// (searched among 1, 2, 4, ... below n) is r's level.  Node 0 is the root
+// with the single child "largest power of two below n".  Another node's
+// parent clears b and sets 2b, or only clears b when 2b would leave the
+// range; its children are r -/+ b/2, the upper one moved down by halving the
+// offset until it exists (and dropped once the offset reaches zero).
+void btree(int n, int r, int* up, int* d0, int* d1, int* childType) {
+  int b = 1;
+  while (b < n && (b & r) == 0) b <<= 1;
+  if (r == 0) {
+    *up = -1;
+    *d0 = -1;
+    *d1 = n > 1 ? (b >> 1) : -1;
+    *childType = -1;
+    return;
+  }
+  int p = (r ^ b) | (b << 1);
+  if (p >= n) p = r ^ b;
+  *up = p;
+  *childType = r < p ? 0 : 1;
+  int half = b >> 1;
+  *d0 = half ? r - half : -1;
+  int hi = half ? r + half : -1;
+  while (hi >= n) {            // the page's loop: re-evaluate, then halve
+    hi = half ? r + half : -1;
+    half >>= 1;
+  }
+  *d1 = hi;
+}
+
+// Node r's place in both trees: tree 0 is btree; tree 1 runs btree on a
+// relabelled node (mirror n-1-r for even n, shift r-1 mod n for odd n) and
+// maps parent and children back with the inverse relabelling.
+void dtree(int n, int r, int t[2][4]) {
+  btree(n, r, &t[0][0], &t[0][1], &t[0][2], &t[0][3]);
+  int u, a, b, ct;
+  if (n & 1) {
+    btree(n, (r - 1 + n) % n, &u, &a, &b, &ct);
+    auto back = [n](int x) { return x < 0 ? -1 : (x + 1) % n; };
+    t[1][0] = back(u); t[1][1] = back(a); t[1][2] = back(b);
+  } else {
+    btree(n, n - 1 - r, &u, &a, &b, &ct);
+    auto back = [n](int x) { return x < 0 ? -1 : n - 1 - x; };
+    t[1][0] = back(u); t[1][1] = back(a); t[1][2] = back(b);
+  }
+  t[1][3] = ct;
+}
+
+static int floor_log2(int n) {
+  int k = 0;
+  while (n > 1) { n >>= 1; ++k; }
+  return k;
+}
+
+int channel_tree(int c, int nCh) { return c < (nCh + 1) / 2 ? 0 : 1; }
+
+// Append `child` to the first free down[] slot; -1 adds nothing.
+static bool add_child(vr_tree_t* t, int child) {
+  if (child < 0) return true;
+  for (int s = 0; s < 3; ++s)
+    if (t->down[s] < 0) { t->down[s] = child; return true; }
+  return false;
+}
+
+vr_result_t build_dtree(int nNodes, int L, int nCh, vr_tree_t* out) {
+  const int R = nNodes * L;
+  const int depth = L - 1 + floor_log2(nNodes);
+  int nodeTree[kMaxRanks][2][4];
+  for (int k = 0; k < nNodes; ++k) dtree(nNodes, k, nodeTree[k]);
+  for (int c = 0; c < nCh; ++c) {
+    const int t = channel_tree(c, nCh);
+    for (int k = 0; k < nNodes; ++k) {
+      for (int l = 0; l < L; ++l) {
+        const int rank = k * L + l;
+        vr_tree_t* x = &out[(size_t)c * R + rank];
+        // intra-node chain in local order
+        x->depth = depth;
+        x->up = l == 0 ? -1 : rank - 1;
+        x->down[0] = l == L - 1 ? -1 : rank + 1;
+        x->down[1] = x->down[2] = -1;
+        if (l != 0) continue;
+        // the node's head joins the node-level tree t
+        const int pu = nodeTree[k][t][0], c0 = nodeTree[k][t][1], c1 = nodeTree[k][t][2];
+        if (pu >= 0) x->up = pu * L;
+        if (!add_child(x, c0 < 0 ? -1 : c0 * L)) return VR_ERR_INTERNAL;
+        if (!add_child(x, c1 < 0 ? -1 : c1 * L)) return VR_ERR_INTERNAL;
+      }
+    }
+  }
+  return VR_SUCCESS;
+}
+
+// ------------------------------------------------------------ fold program
+// A rank's partial is its local input folded with each child's partial in
+// down[] order.  Emitted as: the first child's partial (recursively), then
+// the local input folded into it (the two-operand fold commutes bit-for-bit),
+// then each further child's partial pushed and popped into it.  A chain thus
+// needs a single live partial.
+namespace {
+struct Emitter {
+  const vr_tree_t* tr;
+  FoldProg* p;
+  int slot = 0, pendingPops = 0, sp = 0, maxSp = 0;
+  bool ok = true;
+
+  void load(int rank, bool push) {
+    if (slot >= kMaxRanks || pendingPops > 15) { ok = false; return; }
+    p->rank[slot] = (uint8_t)rank;
+    p->ctl[slot] = (uint8_t)(pendingPops | (push ? 16 : 0));
+    sp -= pendingPops;
+    pendingPops = 0;
+    if (push) { ++sp; if (sp > maxSp) maxSp = sp; }
+    ++slot;
+  }
+  void emit(int v, int guard) {
+    if (guard > kMaxRanks) { ok = false; return; }
+    const int* d = tr[v].down;
+    if (d[0] < 0) { load(v, true); return; }
+    emit(d[0], guard + 1);
+    load(v, false);
+    for (int s = 1; s < 3; ++s) {
+      if (d[s] < 0) continue;
+      emit(d[s], guard + 1);
+      ++pendingPops;
+    }
+  }
+};
+}  // namespace
+
+vr_result_t compile_fold(const vr_tree_t* tr, int R, FoldProg* p) {
+  std::memset(p, 0, sizeof(*p));
+  int root = -1;
+  for (int r = 0; r < R; ++r)
+    if (tr[r].up < 0) { if (root >= 0) return VR_ERR_INTERNAL; root = r; }
+  if (root < 0) return VR_ERR_INTERNAL;
+  Emitter e{tr, p};
+  e.emit(root, 0);
+  if (!e.ok || e.slot != R || e.pendingPops > 15) return VR_ERR_INTERNAL;
+  p->n = (uint8_t)R;
+  p->tail = (uint8_t)e.pendingPops;
+  p->depth = (uint8_t)e.maxSp;
+  if (e.sp - e.pendingPops != 1 || e.maxSp > kMaxStack) return VR_ERR_INTERNAL;
+  // every rank loaded exactly once
+  uint64_t seen = 0;
+  for (int i = 0; i < R; ++i) seen |= 1ull << p->rank[i];
+  if (seen != (R == 64 ? ~0ull : ((1ull << R) - 1))) return VR_ERR_INTERNAL;
+  return VR_SUCCESS;
+}
+
+}  // namespace vr

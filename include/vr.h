@@ -1,0 +1,197 @@
+/*
+ * vr.h -- emulated Ring / Double-Binary-Tree AllReduce on one GPU.
+ *
+ * R "virtual ranks" are R device buffers in one GPU's memory.  The library
+ * computes what an AllReduce (ReduceScatter, AllGather) over R ranks
+ * computes, following the ring and double-binary-tree schedules, and writes
+ * every rank's result buffer.  Each collective call is one kernel launch on
+ * the caller's stream; nothing crosses a GPU or process boundary.
+ *
+ * Sources (web pages), cited below as [tag] "section":
+ *   [Course13]  "NCCL 专家课程 13：Tree、双树、层次化连接与真实交叉区间" (blog.cptz.space)
+ *   [Internals] "NCCL 内部机制：一次 AllReduce 如何变成拓扑图、Channel 与 GPU Kernel"
+ *               (charlestar.github.io)
+ *   [CodeNotes] "NCCL代码分析" (jianzi123.github.io)
+ *   [Interview] "all-reduce 每张卡要发多少数据? ring 和 tree 有什么区别?"
+ *               (charliedreemur.github.io)
+ *
+ * Conventions shared by every call
+ *   - All functions are thread-safe.  They return VR_SUCCESS or an error code;
+ *     argument errors are detected on the host before anything is enqueued.
+ *   - Buffers are owned by the caller.  The pointer arrays are read during the
+ *     call only (their contents are passed to the kernel by value), so the
+ *     caller may reuse or free the arrays as soon as the call returns.
+ *   - Collective calls are asynchronous on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream): returning means enqueued, not completed
+ *     ([Internals] "API 返回只意味着提交边界，不意味着数据已经可读").  Read the
+ *     result only after synchronising the stream or through a stream-ordered
+ *     dependency.
+ *   - The library allocates no device memory.  The only library-owned device
+ *     state is one status word per device (a __device__ variable).
+ *   - Reductions accumulate in fp32 for every dtype and narrow to the element
+ *     type once, round-to-nearest-even.  Sum is IEEE fp32 addition in the
+ *     schedule's order; Max returns the larger value, with +0 above -0.
+ *   - Results are deterministic: the same call on the same inputs gives the
+ *     same bits, and every rank's output is bit-identical.
+ */
+#ifndef VR_H
+#define VR_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  VR_SUCCESS = 0,
+  VR_ERR_INVALID_ARGUMENT = 1, /* bad size, pointer, overlap or enum value */
+  VR_ERR_UNSUPPORTED = 2,      /* valid arguments, combination not offered  */
+  VR_ERR_CUDA = 3,             /* a CUDA runtime call failed                */
+  VR_ERR_TIMEOUT = 4,          /* a bounded device-side wait ran out        */
+  VR_ERR_INTERNAL = 5          /* a library invariant failed                */
+} vr_result_t;
+
+typedef enum { VR_FLOAT32 = 0, VR_FLOAT16 = 1, VR_BFLOAT16 = 2 } vr_dtype_t;
+typedef enum { VR_SUM = 0, VR_MAX = 1 } vr_op_t;
+typedef enum { VR_ALGO_RING = 0, VR_ALGO_TREE = 1 } vr_algo_t;
+
+#define VR_MAX_RANKS 64
+#define VR_MAX_CHANNELS 64
+
+/* One rank's view of one tree: the ncclTree record of [Course13]
+ * "数据结构不是纯二叉树".  up = parent rank (-1 at the root); down[] = child
+ * ranks, present children first, empty slots -1; depth = the approximation
+ * localRanks - 1 + floor(log2(nNodes)) of [Course13] "节点间连接". */
+typedef struct {
+  int depth;
+  int up;
+  int down[3];
+} vr_tree_t;
+
+/* ------------------------------------------------------------ topology */
+
+/* Identity ring of every channel ([Interview] "先弄清楚": each rank sends to
+ * its right-hand neighbour).  next[c*R + r] = (r+1) mod R and
+ * prev[c*R + r] = (r-1) mod R for c < nChannels.  `next` and `prev` are
+ * caller-owned host arrays of nChannels*R ints.
+ * Errors: VR_ERR_INVALID_ARGUMENT for R outside [1, VR_MAX_RANKS], nChannels
+ * outside [1, VR_MAX_CHANNELS] or a NULL array. */
+vr_result_t vr_build_ring(int R, int nChannels, int* next, int* prev);
+
+/* Hierarchical double binary tree over R = nNodes*localRanks ranks
+ * ([Course13] "节点内先形成链", "节点间连接", "Btree 的 bit 构造",
+ * "双树：偶数 mirror，奇数 shift").  Within a node the ranks k*L .. k*L+L-1
+ * form a chain (up = previous, down[0] = next).  Over node indices, tree 0 is
+ * the bit-trick binary tree and tree 1 its mirror (even nNodes) or its
+ * one-step shift (odd nNodes); the head k*L of node k takes up = head of its
+ * parent node and appends the heads of its child nodes to down[].
+ * Channels [0, ceil(nChannels/2)) carry tree 0, the others tree 1.
+ * `trees` is a caller-owned host array of nChannels*R records,
+ * trees[c*R + r].  localRanks = 1 gives the flat double binary tree.
+ * Errors: VR_ERR_INVALID_ARGUMENT for R outside [1, VR_MAX_RANKS], nNodes or
+ * localRanks < 1, nChannels outside [1, VR_MAX_CHANNELS], NULL `trees`. */
+vr_result_t vr_build_dtree(int nNodes, int localRanks, int nChannels, vr_tree_t* trees);
+
+/* Channel c's element range of a message of `count` elements ([Course13]
+ * "前置知识": channels take different ranges of one message).  The message
+ * is cut into 16-byte grains, split over channels so that the first
+ * (grains mod nChannels) channels get one more grain, and clipped at count.
+ * Writes *offset and *channelCount (elements).
+ * Errors: VR_ERR_INVALID_ARGUMENT for a bad dtype, nChannels outside
+ * [1, VR_MAX_CHANNELS], channel outside [0, nChannels) or NULL outputs. */
+vr_result_t vr_partition(size_t count, vr_dtype_t dtype, int nChannels, int channel,
+                         size_t* offset, size_t* channelCount);
+
+/* Ring block of element `elem` in the ring AllReduce partition, which fixes
+ * the order in which the element is reduced ([Interview] "手撕代码": the
+ * block leaves rank j first and each later rank adds its copy).  A channel is
+ * walked in loops of R*C elements (C = chunkBytes / element size), the last
+ * loop shorter; each loop is cut into R blocks, the first (loop mod R) one
+ * element longer.  Writes *channel and *block (the block number j).
+ * Errors: VR_ERR_INVALID_ARGUMENT for elem >= count or the argument errors
+ * of vr_allreduce. */
+vr_result_t vr_ring_block(size_t count, vr_dtype_t dtype, int R, int nChannels,
+                          size_t chunkBytes, size_t elem, int* channel, int* block);
+
+/* --------------------------------------------------------- collectives */
+
+/* AllReduce: every recvbufs[r] (count elements) receives the reduction over
+ * r' < R of sendbufs[r'] ([Internals] "从 API 调用到可调度任务": two buffers,
+ * count, dtype, op, communicator and stream).
+ *   RING ([Interview] "手撕代码", [Internals] "Ring：带宽友好"): an element in
+ *        block j of its ring loop is reduced over ranks j, j+1, ..., j+R-1
+ *        (mod R), left to right -- reduce-scatter followed by all-gather.
+ *   TREE ([Course13] "先固定方向", "runTreeSplit 如何流水", "每种 rank 的操作"):
+ *        on the channel's tree every rank folds its local input with its
+ *        children's partials in down[] order and passes the result up; the
+ *        root's value is broadcast down to all ranks.  localRanks = 1 here.
+ * nChannels in [1, VR_MAX_CHANNELS] splits the message (vr_partition);
+ * chunkBytes (a positive multiple of 16) is the per-rank chunk C of a ring
+ * loop and the chunk of a tree channel.
+ * In place: sendbufs[r] == recvbufs[r] is allowed.
+ * Buffers: any alignment; 16-byte aligned buffers take the vector path.
+ * Errors (nothing enqueued): VR_ERR_INVALID_ARGUMENT for R outside
+ * [1, VR_MAX_RANKS], NULL arrays, a NULL buffer with count > 0, a bad enum,
+ * bad nChannels or chunkBytes, or a recv buffer that overlaps another rank's
+ * send or recv buffer or partly overlaps its own send buffer.
+ * count == 0 enqueues nothing.  R == 1 copies (or leaves in place). */
+vr_result_t vr_allreduce(const void* const* sendbufs, void* const* recvbufs, int R,
+                         size_t count, vr_dtype_t dtype, vr_op_t op, vr_algo_t algo,
+                         int nChannels, size_t chunkBytes, void* stream);
+
+/* vr_allreduce with a hierarchical rank layout: R = nNodes * localRanks,
+ * node k holding ranks k*localRanks .. (k+1)*localRanks - 1.  TREE uses the
+ * trees of vr_build_dtree(R / localRanks, localRanks, nChannels); RING is the
+ * same as vr_allreduce.  Extra error: localRanks < 1 or not dividing R. */
+vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, int R,
+                            size_t count, vr_dtype_t dtype, vr_op_t op, vr_algo_t algo,
+                            int nChannels, size_t chunkBytes, int localRanks, void* stream);
+
+/* ReduceScatter ([Interview] "先弄清楚": each rank keeps the reduced 1/n
+ * segment it is responsible for): sendbufs[r] holds R*recvcount elements;
+ * recvbufs[b] (recvcount elements) receives block b = elements
+ * [b*recvcount, (b+1)*recvcount) reduced over all ranks, in ring order
+ * b+1, b+2, ..., b (mod R).  Only VR_ALGO_RING: tree implements AllReduce
+ * only ([CodeNotes] "通讯时如何选择Channel"), so VR_ALGO_TREE returns
+ * VR_ERR_UNSUPPORTED.  In place: recvbufs[r] == sendbufs[r] + r*recvcount
+ * (in elements).  Other errors as vr_allreduce. */
+vr_result_t vr_reduce_scatter(const void* const* sendbufs, void* const* recvbufs, int R,
+                              size_t recvcount, vr_dtype_t dtype, vr_op_t op,
+                              vr_algo_t algo, int nChannels, size_t chunkBytes,
+                              void* stream);
+
+/* AllGather ([Interview] "先弄清楚": the segments are concatenated back):
+ * recvbufs[q] (R*sendcount elements) receives sendbufs[r] (sendcount
+ * elements) at elements [r*sendcount, (r+1)*sendcount) for every r -- an exact
+ * copy.  Only VR_ALGO_RING (VR_ALGO_TREE: VR_ERR_UNSUPPORTED).  In place:
+ * sendbufs[r] == recvbufs[r] + r*sendcount.  Other errors as vr_allreduce. */
+vr_result_t vr_allgather(const void* const* sendbufs, void* const* recvbufs, int R,
+                         size_t sendcount, vr_dtype_t dtype, vr_algo_t algo,
+                         int nChannels, size_t chunkBytes, void* stream);
+
+/* ------------------------------------------------------------- status */
+
+/* Synchronises `stream`, then returns and clears the current device's status
+ * word: VR_SUCCESS, or the first device-side error any kernel of this library
+ * recorded since the last call (VR_ERR_TIMEOUT for a bounded wait that ran
+ * out, VR_ERR_INTERNAL for a broken invariant), or VR_ERR_CUDA when the
+ * synchronisation itself fails.  The word is per device, not per stream. */
+vr_result_t vr_stream_status(void* stream);
+
+/* Number of kernels this library has launched in this process (all devices,
+ * all threads). */
+unsigned long long vr_launch_count(void);
+
+/* Static English text for a result code ("unknown result" for others). */
+const char* vr_get_error_string(vr_result_t result);
+
+/* Releases host-side caches (tree programs, device properties).  Optional;
+ * the library stays usable afterwards. */
+void vr_finalize(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VR_H */

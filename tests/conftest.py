@@ -24,3 +24,12 @@ def read_golden(name):
 @pytest.fixture(scope="session")
 def golden():
     return read_golden
+
+
+def _ensure_library():
+    """Build libvr.so for this machine before any test imports the binding."""
+    from double_binary_tree_gb300 import build as _b
+    _b.build()
+
+
+_ensure_library()

