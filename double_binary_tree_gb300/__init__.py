@@ -5,9 +5,10 @@ sequences of device pointers (ints) or of torch tensors (their data_ptr() is
 passed); streams take a cudaStream_t as an int, a torch.cuda.Stream, or None
 for the legacy default stream.  A non-zero result code raises VrError.
 
-The compute path is the CUDA library only: importing this package fails
-loudly when libvr.so has not been built for this machine (build it with
-``python -m double_binary_tree_gb300.build`` or ``__graft_entry__.build()``).
+The compute path is the CUDA library only: the first call loads libvr.so
+and fails loudly (ImportError) when it has not been built for this machine
+(build it with ``python -m double_binary_tree_gb300.build`` or
+``__graft_entry__.build()``).
 """
 
 import ctypes
@@ -28,11 +29,31 @@ ELEM_SIZE = {VR_FLOAT32: 4, VR_FLOAT16: 2, VR_BFLOAT16: 2}
 class VrError(RuntimeError):
     def __init__(self, code, where):
         self.code = code
-        super().__init__("%s: %s (%d)" % (where, _lib.vr_get_error_string(code).decode(), code))
+        super().__init__("%s: %s (%d)" % (where, vr_get_error_string(code), code))
 
 
 class vr_tree_t(ctypes.Structure):
     _fields_ = [("depth", ctypes.c_int), ("up", ctypes.c_int), ("down", ctypes.c_int * 3)]
+
+
+P, I, S, VP = ctypes.POINTER, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+PP = P(VP)
+_SIGNATURES = {
+    "vr_build_ring": (I, [I, I, P(I), P(I)]),
+    "vr_build_dtree": (I, [I, I, I, P(vr_tree_t)]),
+    "vr_partition": (I, [S, I, I, I, P(S), P(S)]),
+    "vr_ring_block": (I, [S, I, I, I, S, S, P(I), P(I)]),
+    "vr_allreduce": (I, [PP, PP, I, S, I, I, I, I, S, VP]),
+    "vr_allreduce_ex": (I, [PP, PP, I, S, I, I, I, I, S, I, VP]),
+    "vr_reduce_scatter": (I, [PP, PP, I, S, I, I, I, I, S, VP]),
+    "vr_allgather": (I, [PP, PP, I, S, I, I, I, S, VP]),
+    "vr_stream_status": (I, [VP]),
+    "vr_launch_count": (ctypes.c_ulonglong, []),
+    "vr_get_error_string": (ctypes.c_char_p, [I]),
+    "vr_finalize": (None, []),
+}
+EXPORTED = tuple(_SIGNATURES)
+_lib = None
 
 
 def _load():
@@ -42,31 +63,19 @@ def _load():
         raise ImportError("libvr.so is older than its sources or built for another machine: "
                           "run python -m double_binary_tree_gb300.build")
     lib = ctypes.CDLL(LIB)
-    P, I, S, VP = ctypes.POINTER, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
-    PP = P(VP)
-    sig = {
-        "vr_build_ring": (I, [I, I, P(I), P(I)]),
-        "vr_build_dtree": (I, [I, I, I, P(vr_tree_t)]),
-        "vr_partition": (I, [S, I, I, I, P(S), P(S)]),
-        "vr_ring_block": (I, [S, I, I, I, S, S, P(I), P(I)]),
-        "vr_allreduce": (I, [PP, PP, I, S, I, I, I, I, S, VP]),
-        "vr_allreduce_ex": (I, [PP, PP, I, S, I, I, I, I, S, I, VP]),
-        "vr_reduce_scatter": (I, [PP, PP, I, S, I, I, I, I, S, VP]),
-        "vr_allgather": (I, [PP, PP, I, S, I, I, I, S, VP]),
-        "vr_stream_status": (I, [VP]),
-        "vr_launch_count": (ctypes.c_ulonglong, []),
-        "vr_get_error_string": (ctypes.c_char_p, [I]),
-        "vr_finalize": (None, []),
-    }
-    for name, (res, args) in sig.items():
+    for name, (res, args) in _SIGNATURES.items():
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    return lib, sig
+    return lib
 
 
-_lib, _SIGNATURES = _load()
-EXPORTED = tuple(_SIGNATURES)
+def _L():
+    """The loaded library (loaded on first use)."""
+    global _lib
+    if _lib is None:
+        _lib = _load()
+    return _lib
 
 
 def _check(code, where):
@@ -101,7 +110,7 @@ def vr_build_ring(R, nChannels):
     """Returns (next, prev) as lists of nChannels*R ints."""
     n = (ctypes.c_int * (R * nChannels))() if R > 0 and nChannels > 0 else None
     p = (ctypes.c_int * (R * nChannels))() if R > 0 and nChannels > 0 else None
-    _check(_lib.vr_build_ring(R, nChannels, n, p), "vr_build_ring")
+    _check(_L().vr_build_ring(R, nChannels, n, p), "vr_build_ring")
     return list(n), list(p)
 
 
@@ -110,14 +119,14 @@ def vr_build_dtree(nNodes, localRanks, nChannels):
     R = nNodes * localRanks
     size = max(R * nChannels, 1)
     out = (vr_tree_t * size)()
-    _check(_lib.vr_build_dtree(nNodes, localRanks, nChannels, out), "vr_build_dtree")
+    _check(_L().vr_build_dtree(nNodes, localRanks, nChannels, out), "vr_build_dtree")
     return list(out)[:R * nChannels]
 
 
 def vr_partition(count, dtype, nChannels, channel):
     """Returns (offset, channelCount)."""
     off, n = ctypes.c_size_t(), ctypes.c_size_t()
-    _check(_lib.vr_partition(count, dtype, nChannels, channel, ctypes.byref(off), ctypes.byref(n)),
+    _check(_L().vr_partition(count, dtype, nChannels, channel, ctypes.byref(off), ctypes.byref(n)),
            "vr_partition")
     return off.value, n.value
 
@@ -125,7 +134,7 @@ def vr_partition(count, dtype, nChannels, channel):
 def vr_ring_block(count, dtype, R, nChannels, chunkBytes, elem):
     """Returns (channel, block) of element `elem`."""
     c, b = ctypes.c_int(), ctypes.c_int()
-    _check(_lib.vr_ring_block(count, dtype, R, nChannels, chunkBytes, elem, ctypes.byref(c),
+    _check(_L().vr_ring_block(count, dtype, R, nChannels, chunkBytes, elem, ctypes.byref(c),
                               ctypes.byref(b)), "vr_ring_block")
     return c.value, b.value
 
@@ -133,45 +142,45 @@ def vr_ring_block(count, dtype, R, nChannels, chunkBytes, elem):
 # ---------------------------------------------------------- collectives
 def vr_allreduce(sendbufs, recvbufs, R, count, dtype, op, algo, nChannels, chunkBytes,
                  stream=None):
-    _check(_lib.vr_allreduce(_ptrs(sendbufs), _ptrs(recvbufs), R, count, dtype, op, algo,
+    _check(_L().vr_allreduce(_ptrs(sendbufs), _ptrs(recvbufs), R, count, dtype, op, algo,
                              nChannels, chunkBytes, _stream(stream)), "vr_allreduce")
 
 
 def vr_allreduce_ex(sendbufs, recvbufs, R, count, dtype, op, algo, nChannels, chunkBytes,
                     localRanks, stream=None):
-    _check(_lib.vr_allreduce_ex(_ptrs(sendbufs), _ptrs(recvbufs), R, count, dtype, op, algo,
+    _check(_L().vr_allreduce_ex(_ptrs(sendbufs), _ptrs(recvbufs), R, count, dtype, op, algo,
                                 nChannels, chunkBytes, localRanks, _stream(stream)),
            "vr_allreduce_ex")
 
 
 def vr_reduce_scatter(sendbufs, recvbufs, R, recvcount, dtype, op, algo, nChannels, chunkBytes,
                       stream=None):
-    _check(_lib.vr_reduce_scatter(_ptrs(sendbufs), _ptrs(recvbufs), R, recvcount, dtype, op,
+    _check(_L().vr_reduce_scatter(_ptrs(sendbufs), _ptrs(recvbufs), R, recvcount, dtype, op,
                                   algo, nChannels, chunkBytes, _stream(stream)),
            "vr_reduce_scatter")
 
 
 def vr_allgather(sendbufs, recvbufs, R, sendcount, dtype, algo, nChannels, chunkBytes,
                  stream=None):
-    _check(_lib.vr_allgather(_ptrs(sendbufs), _ptrs(recvbufs), R, sendcount, dtype, algo,
+    _check(_L().vr_allgather(_ptrs(sendbufs), _ptrs(recvbufs), R, sendcount, dtype, algo,
                              nChannels, chunkBytes, _stream(stream)), "vr_allgather")
 
 
 def vr_stream_status(stream=None):
     """Synchronises the stream and returns the device status code (0 = ok)."""
-    return _lib.vr_stream_status(_stream(stream))
+    return _L().vr_stream_status(_stream(stream))
 
 
 def vr_launch_count():
-    return _lib.vr_launch_count()
+    return _L().vr_launch_count()
 
 
 def vr_get_error_string(code):
-    return _lib.vr_get_error_string(code).decode()
+    return _L().vr_get_error_string(code).decode()
 
 
 def vr_finalize():
-    _lib.vr_finalize()
+    _L().vr_finalize()
 
 
 def library_path():
