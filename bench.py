@@ -287,14 +287,25 @@ def e2e_arm(args, vr, torch, inputs, dev, stream, world):
 
 def time_calls(torch, stream, call, sets, iters):
     """Average device time of `call(i)` over iters calls, rotating buffer
-    sets i so that L2-sized workloads read from HBM."""
+    sets i so that L2-sized workloads read from HBM.  The calls are captured
+    once into a CUDA graph and replayed, so host-side launch cost does not
+    leave the GPU idle between short kernels."""
     for i in range(3):
-        call(i % sets)
+        call(i % sets, stream)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            cs = torch.cuda.current_stream()
+            for i in range(iters):
+                call(i % sets, cs)
+    torch.cuda.synchronize()
+    graph.replay()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for i in range(iters):
-        call(i % sets)
+    graph.replay()
     b.record(stream)
     torch.cuda.synchronize()
     return a.elapsed_time(b) / iters
@@ -325,9 +336,9 @@ def other_workloads(vr, torch, workloads, dev, stream):
         bufs = [([t.to(dev) for t in base], [torch.empty(count, dtype=base[0].dtype, device=dev)
                                              for _ in range(R)]) for _ in range(sets)]
         for nch in (2, 12):
-            def call(i, nch=nch):
+            def call(i, st, nch=nch):
                 s, d = bufs[i]
-                vr.vr_allreduce(s, d, R, count, w["dtype"], 0, 1, nch, w["chunk_bytes"], stream)
+                vr.vr_allreduce(s, d, R, count, w["dtype"], 0, 1, nch, w["chunk_bytes"], st)
             ms = time_calls(torch, stream, call, sets, 200)
             out["%s_tree_%dch" % (name, nch)] = entry(ms, nbytes, count * 2, R)
         del bufs
@@ -341,20 +352,20 @@ def other_workloads(vr, torch, workloads, dev, stream):
     nbytes = ar_bytes(R, count, 1)
     for algo, aname in ((0, "ring"), (1, "tree")):
         for op, oname in ((0, "sum"), (1, "max")):
-            def call(i, algo=algo, op=op):
-                vr.vr_allreduce_ex(src, dst, R, count, 1, op, algo, 12, 512 * 1024, L, stream)
+            def call(i, st, algo=algo, op=op):
+                vr.vr_allreduce_ex(src, dst, R, count, 1, op, algo, 12, 512 * 1024, L, st)
             ms = time_calls(torch, stream, call, 1, 20)
             out["hier_16mib_fp16_%s_%s" % (aname, oname)] = entry(ms, nbytes, count * 2, R)
     rc = count // R
     rs = [torch.empty(rc, dtype=torch.float16, device=dev) for _ in range(R)]
 
-    def call_rs(i):
-        vr.vr_reduce_scatter(src, rs, R, rc, 1, 0, 0, 12, 512 * 1024, stream)
+    def call_rs(i, st):
+        vr.vr_reduce_scatter(src, rs, R, rc, 1, 0, 0, 12, 512 * 1024, st)
     ms = time_calls(torch, stream, call_rs, 1, 20)
     out["hier_16mib_fp16_reduce_scatter"] = entry(ms, R * count * 2 + R * rc * 2)
 
-    def call_ag(i):
-        vr.vr_allgather(rs, dst, R, rc, 1, 0, 12, 512 * 1024, stream)
+    def call_ag(i, st):
+        vr.vr_allgather(rs, dst, R, rc, 1, 0, 12, 512 * 1024, st)
     ms = time_calls(torch, stream, call_ag, 1, 20)
     out["hier_16mib_fp16_allgather"] = entry(ms, R * rc * 2 + R * count * 2)
     return out
@@ -419,6 +430,46 @@ def reference_arm(args):
                     "d2h_bytes_per_step": 0}}
 
 
+PROFILE_CASES = {
+    # name: (R, local ranks, dtype, op, algo) -- counts come from --count
+    "ring_r8_fp32": (8, 1, 0, 0, 0),
+    "tree_r8_bf16": (8, 1, 2, 0, 1),
+    "tree_r64_fp16_hier": (64, 8, 1, 0, 1),
+    "tree_r64_fp16_hier_max": (64, 8, 1, 1, 1),
+    "ring_r64_fp16": (64, 1, 1, 0, 0),
+}
+
+
+def profile_case(args):
+    """One collective configuration only, W + K plain launches, nothing else
+    on the GPU: the command the ncu captures run."""
+    import torch
+    import double_binary_tree_gb300 as vr
+    R, L, dtype, op, algo = PROFILE_CASES[args.profile]
+    count = args.count
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    tdt = {0: torch.float32, 1: torch.float16, 2: torch.bfloat16}[dtype]
+    src = [torch.randn(count, generator=g, device=dev).to(tdt) for _ in range(R)]
+    dst = [torch.empty_like(s) for s in src]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup + args.steps):
+        if i == args.warmup:
+            torch.cuda.synchronize()
+            a.record(stream)
+        vr.vr_allreduce_ex(src, dst, R, count, dtype, op, algo, 12, 512 * 1024, L, stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    if vr.vr_stream_status(stream) != 0:
+        raise RuntimeError("device status error")
+    ms = a.elapsed_time(b) / max(args.steps, 1)
+    nbytes = ar_bytes(R, count, dtype)
+    print(json.dumps({"profile": args.profile, "count": count, "us": round(ms * 1e3, 2),
+                      "hbm_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}))
+
+
 def sweep(args):
     """Ring vs tree, R=4 fp32 Sum, 8 B .. 256 MiB per rank, 12 channels,
     512 KiB chunks; L2-sized messages rotate buffer sets."""
@@ -440,9 +491,9 @@ def sweep(args):
                  [torch.empty(count, device=dev) for _ in range(R)]) for _ in range(sets)]
         row = {"bytes_per_rank": size}
         for algo, name in ((0, "ring"), (1, "tree")):
-            def call(i, algo=algo):
+            def call(i, st, algo=algo):
                 s, d = bufs[i]
-                vr.vr_allreduce(s, d, R, count, 0, 0, algo, 12, 512 * 1024, stream)
+                vr.vr_allreduce(s, d, R, count, 0, 0, algo, 12, 512 * 1024, st)
             iters = 200 if size <= (1 << 24) else 20
             samples = [time_calls(torch, stream, call, sets, iters) for _ in range(5)]
             ms = statistics.median(samples)
@@ -468,6 +519,10 @@ def main():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--quick", action="store_true", help="skip the other workloads")
     p.add_argument("--sweep", action="store_true")
+    p.add_argument("--profile", choices=sorted(PROFILE_CASES),
+                   help="run one collective configuration only (for ncu)")
+    p.add_argument("--count", type=int, default=8 * 1024 * 1024,
+                   help="elements per rank for --profile")
     args = p.parse_args()
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -482,6 +537,9 @@ def main():
         return
     if args.sweep:
         sweep(args)
+        return
+    if args.profile:
+        profile_case(args)
         return
     if world > 1:
         import torch
