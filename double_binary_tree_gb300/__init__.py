@@ -49,6 +49,7 @@ _SIGNATURES = {
     "vr_allgather": (I, [PP, PP, I, S, I, I, I, S, VP]),
     "vr_stream_status": (I, [VP]),
     "vr_launch_count": (ctypes.c_ulonglong, []),
+    "vr_debug_stall_next": (I, [ctypes.c_longlong]),
     "vr_get_error_string": (ctypes.c_char_p, [I]),
     "vr_finalize": (None, []),
 }
@@ -173,6 +174,10 @@ def vr_stream_status(stream=None):
 
 def vr_launch_count():
     return _L().vr_launch_count()
+
+
+def vr_debug_stall_next(tile):
+    _check(_L().vr_debug_stall_next(tile), "vr_debug_stall_next")
 
 
 def vr_get_error_string(code):

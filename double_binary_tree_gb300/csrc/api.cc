@@ -22,11 +22,33 @@ std::mutex g_mu;
 
 struct DeviceInfo {
   int sms = 0;
+  int smemOptin = 0;  // largest dynamic shared memory a CTA may opt into
   unsigned* status = nullptr;
 };
 std::map<int, DeviceInfo> g_devices;                             // by device ordinal
 std::map<std::pair<const void*, int>, int> g_occupancy;          // (kernel, device)
 std::map<std::pair<int, int>, std::array<FoldProg, 2>> g_progs;  // (nNodes, localRanks)
+std::map<std::pair<const void*, int>, int> g_smemSet;            // (kernel, device) -> bytes
+std::atomic<long long> g_stallNext{-1};                          // test hook
+
+unsigned long long wait_timeout_ns() {
+  static const unsigned long long ns = [] {
+    const char* v = std::getenv("VR_WAIT_TIMEOUT_NS");
+    const unsigned long long x = v ? std::strtoull(v, nullptr, 10) : 0;
+    return x ? x : 1000000000ull;  // 1 s
+  }();
+  return ns;
+}
+
+// Temporary comparison switch: VR_KERNEL_PATH=register runs aligned
+// AllReduce / ReduceScatter on the register-path kernels.
+bool force_register_path() {
+  static const bool on = [] {
+    const char* v = std::getenv("VR_KERNEL_PATH");
+    return v && std::strcmp(v, "register") == 0;
+  }();
+  return on;
+}
 
 size_t elem_size(int dtype) {
   switch (dtype) {
@@ -43,7 +65,9 @@ vr_result_t device_info(DeviceInfo* out, int* device) {
   auto it = g_devices.find(*device);
   if (it == g_devices.end()) {
     DeviceInfo d;
-    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, *device) != cudaSuccess)
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, *device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smemOptin, cudaDevAttrMaxSharedMemoryPerBlockOptin, *device) !=
+            cudaSuccess)
       return VR_ERR_CUDA;
     if (status_word_address(&d.status) != cudaSuccess) return VR_ERR_CUDA;
     it = g_devices.emplace(*device, d).first;
@@ -142,6 +166,15 @@ bool aligned16(const void* const* p, int R, size_t extraStride) {
   return true;
 }
 
+const void* pick_staged(int dtype, int mode, int op, int stack = 0) {
+  switch (dtype) {
+    case VR_FLOAT32: return staged_kernel_ptr_f32(mode, op, stack);
+    case VR_FLOAT16: return staged_kernel_ptr_f16(mode, op, stack);
+    case VR_BFLOAT16: return staged_kernel_ptr_bf16(mode, op, stack);
+    default: return nullptr;
+  }
+}
+
 const void* pick_kernel(int dtype, int mode, int op, bool vec, int stack = 0) {
   switch (dtype) {
     case VR_FLOAT32: return kernel_ptr_f32(mode, op, vec, stack);
@@ -167,6 +200,53 @@ vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream) {
   void* args[] = {&a};
   if (cudaLaunchKernel(fn, dim3(grid), dim3(kBlockThreads), args, 0, (cudaStream_t)stream) !=
       cudaSuccess)
+    return VR_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return VR_SUCCESS;
+}
+
+// Staged geometry: tiles of 32 * upl 16-byte units per rank; as many stages
+// (one consumer warp each, at most 16) as fit in the opt-in shared memory.
+// a.unitsAll / a.unitsFull describe the message (AllReduce) or one block
+// (ReduceScatter); the tile count follows from the geometry.
+vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
+  if (!fn) return VR_ERR_INTERNAL;
+  DeviceInfo di;
+  int device = 0;
+  vr_result_t e = device_info(&di, &device);
+  if (e != VR_SUCCESS) return e;
+  if ((e = check_reachable(a.src, a.R, device)) != VR_SUCCESS) return e;
+  if ((e = check_reachable(const_cast<const void* const*>(a.dst), a.R, device)) != VR_SUCCESS)
+    return e;
+  a.status = di.status;
+  a.upl = a.R <= 4 ? 4 : (a.R <= 16 ? 2 : 1);
+  a.tileBytes = 512u * (unsigned)a.upl;
+  const long long TU = 32LL * a.upl;
+  a.tiles = mode == kReduceScatter ? (long long)a.R * ((a.unitsFull + TU - 1) / TU)
+                                   : (a.unitsAll + TU - 1) / TU;
+  a.stageBytes = ((unsigned)a.R * a.tileBytes + 127u) & ~127u;
+  const int fit = (di.smemOptin - kStagedHeader) / (int)a.stageBytes;
+  a.stages = std::min(kStagedMaxStages, fit);
+  if (a.stages < 2) return VR_ERR_INTERNAL;
+  if (a.stages > kStagedMaxConsumers) a.stages -= a.stages % kStagedMaxConsumers;
+  a.consumers = std::min(a.stages, kStagedMaxConsumers);
+  const size_t smem = kStagedHeader + (size_t)a.stages * a.stageBytes;
+  {
+    std::lock_guard<std::mutex> g(g_mu);
+    int& set = g_smemSet[std::make_pair(fn, device)];
+    if (set < (int)smem) {
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smemOptin) !=
+          cudaSuccess)
+        return VR_ERR_CUDA;
+      set = di.smemOptin;
+    }
+  }
+  a.timeoutNs = wait_timeout_ns();
+  a.injectStall = g_stallNext.exchange(-1);
+  const int grid = (int)std::max(1LL, std::min<long long>(di.sms, a.tiles));
+  void* args[] = {&a};
+  if (cudaLaunchKernel(fn, dim3(grid), dim3(32 * (a.consumers + 1)), args, smem,
+                       (cudaStream_t)stream) != cudaSuccess)
     return VR_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return VR_SUCCESS;
@@ -273,6 +353,12 @@ vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, 
     stack = std::max(p[0].depth, p[1].depth);
   }
   const bool vec = aligned16(sendbufs, R, 0) && aligned16(recvbufs, R, 0);
+  if (vec && !force_register_path()) {
+    const long long bytes = (long long)count * (long long)E;
+    a.unitsAll = (bytes + 15) / 16;
+    a.unitsFull = bytes / 16;
+    return launch_staged(pick_staged(dtype, mode, op, stack), a, mode, stream);
+  }
   const long long NV = vec ? kGrainBytes / (long long)E : 1;
   return launch(pick_kernel(dtype, mode, op, vec, stack), a, ((long long)count + NV - 1) / NV,
                 stream);
@@ -303,6 +389,11 @@ vr_result_t vr_reduce_scatter(const void* const* sendbufs, void* const* recvbufs
   a.nCh = nChannels;
   a.chunk = (long long)(chunkBytes / E);
   const bool vec = aligned16(sendbufs, R, recvcount * E) && aligned16(recvbufs, R, 0);
+  if (vec && !force_register_path()) {
+    a.unitsFull = (long long)(recvcount * E / 16);
+    a.unitsAll = a.unitsFull;
+    return launch_staged(pick_staged(dtype, kReduceScatter, op), a, kReduceScatter, stream);
+  }
   const long long NV = vec ? kGrainBytes / (long long)E : 1;
   const long long units = (long long)R * (((long long)recvcount + NV - 1) / NV);
   return launch(pick_kernel(dtype, kReduceScatter, op, vec), a, units, stream);
@@ -339,6 +430,12 @@ vr_result_t vr_stream_status(void* stream) {
 
 unsigned long long vr_launch_count(void) { return g_launches.load(); }
 
+vr_result_t vr_debug_stall_next(long long tile) {
+  if (tile < -1) return VR_ERR_INVALID_ARGUMENT;
+  g_stallNext.store(tile);
+  return VR_SUCCESS;
+}
+
 const char* vr_get_error_string(vr_result_t result) {
   switch (result) {
     case VR_SUCCESS: return "success";
@@ -356,6 +453,7 @@ void vr_finalize(void) {
   g_progs.clear();
   g_occupancy.clear();
   g_devices.clear();
+  g_smemSet.clear();
 }
 
 }  // extern "C"

@@ -1,0 +1,416 @@
+// The reduction of one unit over the emulated ranks, in the schedule's order.
+//
+// All R ranks' buffers sit in one GPU's memory, so every "message" of the
+// ring or tree schedule stays on chip: a thread takes the R ranks' copies of
+// one 16-byte unit (or one element), folds them in exactly the order the
+// schedule reduces them, narrows once, and the kernel stores the result to
+// every rank that receives it.
+//
+// Reduction orders (sources: [Interview] "all-reduce 每张卡要发多少数据? ring 和
+// tree 有什么区别?", section "手撕代码(NumPy 模拟 ring all-reduce)" and Figure 1;
+// [Course13] "NCCL 专家课程 13：Tree、双树、层次化连接与真实交叉区间", sections
+// "先固定方向", "runTreeSplit 如何流水", "每种 rank 的操作"):
+//   ring AllReduce  element in block j of its loop: ranks j, j+1, ..., j-1
+//   ReduceScatter   element of block b: ranks b+1, ..., b
+//   tree AllReduce  post-order over the channel's tree, local input first,
+//                   children in down[] order (the FoldProg stream)
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+#include "common.h"
+
+namespace vr {
+
+constexpr int kBatch = 8;  // rank loads issued together before they are folded
+
+// ------------------------------------------------------------ element types
+template <typename T> struct Ty;
+template <> struct Ty<float> {
+  static constexpr int U = 4;  // elements per 16 bytes
+  typedef unsigned Bits;
+  static __device__ __forceinline__ float widen(Bits b) { return __uint_as_float(b); }
+  static __device__ __forceinline__ Bits narrow(float x) { return __float_as_uint(x); }
+};
+template <> struct Ty<__half> {
+  static constexpr int U = 8;
+  typedef unsigned short Bits;
+  static __device__ __forceinline__ float widen(Bits b) { return __half2float(__ushort_as_half(b)); }
+  static __device__ __forceinline__ Bits narrow(float x) { return __half_as_ushort(__float2half_rn(x)); }
+};
+template <> struct Ty<__nv_bfloat16> {
+  static constexpr int U = 8;
+  typedef unsigned short Bits;
+  static __device__ __forceinline__ float widen(Bits b) {
+    return __bfloat162float(__ushort_as_bfloat16(b));
+  }
+  static __device__ __forceinline__ Bits narrow(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+  }
+};
+
+// ---------------------------------------------------------- memory access
+__device__ __forceinline__ uint4 ld_global_v4(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ unsigned ld_shared_u32(uint32_t a) {
+  unsigned v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ unsigned short ld_shared_u16(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// A unit is one 16-byte vector (NV = Ty<T>::U elements) or one element.
+template <typename T, int NV> struct Unit {
+  typedef typename Ty<T>::Bits Bits;
+  typedef typename std::conditional<NV == 1, Bits, uint4>::type Raw;
+
+  static __device__ __forceinline__ void store(char* p, Raw v) {
+    if constexpr (NV == 1) *reinterpret_cast<Bits*>(p) = v;
+    else st_global_v4(p, v);
+  }
+  static __device__ __forceinline__ void unpack(Raw v, float (&x)[NV]) {
+    if constexpr (NV == 1) {
+      x[0] = Ty<T>::widen(v);
+    } else if constexpr (sizeof(T) == 4) {
+      x[0] = Ty<T>::widen(v.x); x[1] = Ty<T>::widen(v.y);
+      x[2] = Ty<T>::widen(v.z); x[3] = Ty<T>::widen(v.w);
+    } else {
+      const unsigned w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[2 * i] = Ty<T>::widen((Bits)(w[i] & 0xFFFFu));
+        x[2 * i + 1] = Ty<T>::widen((Bits)(w[i] >> 16));
+      }
+    }
+  }
+  static __device__ __forceinline__ Raw pack(const float (&x)[NV]) {
+    if constexpr (NV == 1) {
+      return Ty<T>::narrow(x[0]);
+    } else if constexpr (sizeof(T) == 4) {
+      return make_uint4(Ty<T>::narrow(x[0]), Ty<T>::narrow(x[1]), Ty<T>::narrow(x[2]),
+                        Ty<T>::narrow(x[3]));
+    } else {
+      unsigned w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        w[i] = (unsigned)Ty<T>::narrow(x[2 * i]) | ((unsigned)Ty<T>::narrow(x[2 * i + 1]) << 16);
+      return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+};
+
+// Where rank r's copy of the unit being folded lives.
+struct GlobalSrc {              // ptr[r] + off, global memory
+  const char* const* ptr;
+  long long off;
+};
+struct SharedSrc {              // base + r * stride, shared memory
+  uint32_t base;
+  uint32_t stride;
+};
+
+template <typename T, int NV>
+__device__ __forceinline__ typename Unit<T, NV>::Raw load_unit(const GlobalSrc& s, int r) {
+  const char* p = s.ptr[r] + s.off;
+  if constexpr (NV == 1) return __ldg(reinterpret_cast<const typename Ty<T>::Bits*>(p));
+  else return ld_global_v4(p);
+}
+template <typename T, int NV>
+__device__ __forceinline__ typename Unit<T, NV>::Raw load_unit(const SharedSrc& s, int r) {
+  const uint32_t a = s.base + (uint32_t)r * s.stride;
+  if constexpr (NV != 1) return ld_shared_v4(a);
+  else if constexpr (sizeof(T) == 4) return ld_shared_u32(a);
+  else return ld_shared_u16(a);
+}
+
+// ----------------------------------------------------------- reduction op
+// Sum: IEEE fp32 addition of the exactly widened inputs, never contracted.
+__device__ __forceinline__ float add_rn(float a, float b) { return __fadd_rn(a, b); }
+
+// Max: the larger value in the IEEE total order of non-NaN floats (-0 below
+// +0).  Widening is exact and monotone, so the order of the widened fp32
+// values is the order of the element type's own values; Max therefore runs
+// on order-preserving integer keys of the raw bits -- sign-magnitude mapped
+// to unsigned (negative: all bits flipped, positive: sign bit flipped) --
+// and needs no float conversion.  16-bit keys are compared two per 32-bit
+// word.
+__device__ __forceinline__ unsigned key32(unsigned b) {
+  return b ^ ((unsigned)((int)b >> 31) | 0x80000000u);
+}
+__device__ __forceinline__ unsigned unkey32(unsigned k) {
+  return k ^ (~(unsigned)((int)k >> 31) | 0x80000000u);
+}
+__device__ __forceinline__ unsigned key16x2(unsigned w) {
+  const unsigned neg = ((w >> 15) & 0x00010001u) * 0xFFFFu;  // 0xFFFF in negative lanes
+  return w ^ (neg | 0x80008000u);
+}
+__device__ __forceinline__ unsigned unkey16x2(unsigned k) {
+  const unsigned pos = ((k >> 15) & 0x00010001u) * 0xFFFFu;  // 0xFFFF in lanes >= +0
+  return k ^ (~pos | 0x80008000u);
+}
+
+// The fold's working lanes for one unit: fp32 values for Sum, integer keys
+// for Max.
+template <typename T, int OP, int NV, bool IS_SUM = (OP == VR_SUM)> struct Lanes;
+
+template <typename T, int NV> struct Lanes<T, VR_SUM, NV, true> {
+  typedef float L;
+  static constexpr int N = NV;
+  typedef Unit<T, NV> Un;
+  static __device__ __forceinline__ void decode(typename Un::Raw v, L (&x)[N]) { Un::unpack(v, x); }
+  static __device__ __forceinline__ typename Un::Raw encode(const L (&x)[N]) { return Un::pack(x); }
+  static __device__ __forceinline__ L op(L a, L b) { return add_rn(a, b); }
+};
+
+template <typename T, int NV> struct Lanes<T, VR_MAX, NV, false> {
+  typedef unsigned L;
+  typedef Unit<T, NV> Un;
+  static constexpr bool kWide = sizeof(T) == 4;
+  static constexpr int N = NV == 1 ? 1 : 4;  // 32-bit words per unit
+  static __device__ __forceinline__ void decode(typename Un::Raw v, L (&x)[N]) {
+    if constexpr (NV == 1) {
+      x[0] = kWide ? key32((unsigned)v) : key16x2((unsigned)v);
+    } else {
+      const unsigned w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[i] = kWide ? key32(w[i]) : key16x2(w[i]);
+    }
+  }
+  static __device__ __forceinline__ typename Un::Raw encode(const L (&x)[N]) {
+    if constexpr (NV == 1) {
+      return (typename Un::Raw)(kWide ? unkey32(x[0]) : (unkey16x2(x[0]) & 0xFFFFu));
+    } else {
+      unsigned w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[i] = kWide ? unkey32(x[i]) : unkey16x2(x[i]);
+      return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  static __device__ __forceinline__ L op(L a, L b) {
+    if constexpr (kWide) return max(a, b);
+    else return __vmaxu2(a, b);
+  }
+};
+
+// ------------------------------------------------------------------ folds
+// Ranks j, j+1, ..., j+R-1 (mod R), left to right.
+template <typename T, int OP, int NV, class Src>
+__device__ __forceinline__ typename Unit<T, NV>::Raw ring_fold(const Src& src, int R, int j) {
+  typedef Unit<T, NV> Un;
+  typedef Lanes<T, OP, NV> Ln;
+  typename Ln::L acc[Ln::N];
+#pragma unroll
+  for (int e = 0; e < Ln::N; ++e) acc[e] = 0;
+  for (int k0 = 0; k0 < R; k0 += kBatch) {
+    typename Un::Raw v[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int k = k0 + i;
+      if (k < R) {
+        int r = j + k;
+        r -= r >= R ? R : 0;
+        v[i] = load_unit<T, NV>(src, r);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int k = k0 + i;
+      if (k < R) {
+        typename Ln::L x[Ln::N];
+        Ln::decode(v[i], x);
+#pragma unroll
+        for (int e = 0; e < Ln::N; ++e) acc[e] = k == 0 ? x[e] : Ln::op(acc[e], x[e]);
+      }
+    }
+  }
+  return Ln::encode(acc);
+}
+
+// Partials of a tree fold.  The top partial lives in fixed registers, so
+// the common step -- fold a loaded value into the top -- is straight-line
+// code; only a push (a second child's subtree begins) or a pop (it ends)
+// touches the slots below, through a switch on the depth.  The depth is the
+// same for every lane that follows the same program, so the switches are
+// uniform branches, and naming each slot statically keeps them in registers.
+template <typename Ln, int S> struct Below {
+  static_assert(S == 4 || S == 8, "4 or 8 partials");
+  static constexpr int N = Ln::N;
+  typename Ln::L b0[N], b1[N], b2[N], b3[N], b4[N], b5[N], b6[N];
+};
+#define VR_BELOW_SLOTS(X) X(0, b0) X(1, b1) X(2, b2) X(3, b3) X(4, b4) X(5, b5) X(6, b6)
+
+// below[d] = top
+template <typename Ln, int S>
+__device__ __forceinline__ void below_store(Below<Ln, S>& bl, int d, const typename Ln::L (&top)[Ln::N]) {
+  switch (d) {
+#define VR_CASE(i, m)                                                       \
+  case i:                                                                   \
+    if constexpr (i < S - 1) {                                              \
+      _Pragma("unroll") for (int e = 0; e < Ln::N; ++e) bl.m[e] = top[e];   \
+    }                                                                       \
+    break;
+    VR_BELOW_SLOTS(VR_CASE)
+#undef VR_CASE
+  }
+}
+// top = below[d] (op) top
+template <typename Ln, int S>
+__device__ __forceinline__ void below_fold(const Below<Ln, S>& bl, int d, typename Ln::L (&top)[Ln::N]) {
+  switch (d) {
+#define VR_CASE(i, m)                                                                  \
+  case i:                                                                              \
+    if constexpr (i < S - 1) {                                                         \
+      _Pragma("unroll") for (int e = 0; e < Ln::N; ++e) top[e] = Ln::op(bl.m[e], top[e]); \
+    }                                                                                  \
+    break;
+    VR_BELOW_SLOTS(VR_CASE)
+#undef VR_CASE
+  }
+}
+#undef VR_BELOW_SLOTS
+
+template <typename T, int OP, int NV, int S, class Src>
+__device__ __forceinline__ typename Unit<T, NV>::Raw tree_fold(const Src& src, const FoldProg& p,
+                                                              int R) {
+  typedef Unit<T, NV> Un;
+  typedef Lanes<T, OP, NV> Ln;
+  typename Ln::L top[Ln::N];
+#pragma unroll
+  for (int e = 0; e < Ln::N; ++e) top[e] = 0;
+  Below<Ln, S> below;
+  int sp = 0;  // live partials, the top included
+  for (int k0 = 0; k0 < R; k0 += kBatch) {
+    typename Un::Raw v[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int k = k0 + i;
+      if (k < R) v[i] = load_unit<T, NV>(src, p.rank[k]);
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int k = k0 + i;
+      if (k < R) {
+        const int c = p.ctl[k];
+        for (int q = c & 15; q > 0; --q) below_fold<Ln, S>(below, --sp - 1, top);
+        typename Ln::L x[Ln::N];
+        Ln::decode(v[i], x);
+        if (c & 16) {
+          if (sp > 0) below_store<Ln, S>(below, sp - 1, top);
+#pragma unroll
+          for (int e = 0; e < Ln::N; ++e) top[e] = x[e];
+          ++sp;
+        } else {
+#pragma unroll
+          for (int e = 0; e < Ln::N; ++e) top[e] = Ln::op(top[e], x[e]);
+        }
+      }
+    }
+  }
+  for (int q = p.tail; q > 0; --q) below_fold<Ln, S>(below, --sp - 1, top);
+  return Ln::encode(top);
+}
+
+// --------------------------------------------------------- partition math
+// Where element e sits: its channel range [lo, hi) and, for the ring, its
+// block [lo, hi) inside the loop with block number j.  Channels hold 16-byte
+// grains split with array_split semantics; ring loops hold R*C elements, the
+// last one shorter, each cut into R blocks with array_split semantics.
+struct Cursor {
+  long long lo, hi;
+  int j;  // ring block number
+  int t;  // tree index of the channel
+};
+
+template <int U>
+__device__ __forceinline__ void locate_channel(const KArgs& a, long long e, int& k,
+                                               long long& cs, long long& ce) {
+  const long long g = e / U;
+  const long long big = a.gm * (a.gq + 1);
+  long long gs;
+  if (g < big) {
+    k = (int)(g / (a.gq + 1));
+    gs = (long long)k * (a.gq + 1);
+  } else {
+    k = (int)(a.gm + (g - big) / a.gq);
+    gs = big + (long long)(k - a.gm) * a.gq;
+  }
+  const long long len = a.gq + (k < a.gm ? 1 : 0);
+  cs = gs * U;
+  ce = min(a.count, (gs + len) * U);
+}
+
+template <int U, int MODE>
+__device__ __forceinline__ void locate(const KArgs& a, long long e, Cursor& c) {
+  int k;
+  long long cs, ce;
+  locate_channel<U>(a, e, k, cs, ce);
+  if constexpr (MODE == kTreeAllReduce) {
+    c.lo = cs;
+    c.hi = ce;
+    c.t = k < a.treeSplit ? 0 : 1;
+    c.j = 0;
+  } else {
+    const long long R = a.R;
+    const long long LC = R * a.chunk;
+    const long long off = e - cs;
+    const long long ls = (off / LC) * LC;
+    const long long L = min(LC, (ce - cs) - ls);
+    const long long w = off - ls;
+    const long long q = L / R, m = L % R;
+    long long j, bs, bl;
+    if (w < m * (q + 1)) {
+      j = w / (q + 1);
+      bs = j * (q + 1);
+      bl = q + 1;
+    } else {
+      j = m + (w - m * (q + 1)) / q;
+      bs = m * (q + 1) + (j - m) * q;
+      bl = q;
+    }
+    c.lo = cs + ls + bs;
+    c.hi = c.lo + bl;
+    c.j = (int)j;
+    c.t = 0;
+  }
+}
+
+// One element of an AllReduce: its fold in the schedule of element e.
+template <typename T, int OP, int MODE, int S, class Src>
+__device__ __forceinline__ typename Ty<T>::Bits fold_element(const KArgs& a, const Src& src,
+                                                            const FoldProg* progs, long long e,
+                                                            Cursor& cur) {
+  if (e < cur.lo || e >= cur.hi) locate<Ty<T>::U, MODE>(a, e, cur);
+  if constexpr (MODE == kTreeAllReduce) return tree_fold<T, OP, 1, S>(src, progs[cur.t], a.R);
+  else return ring_fold<T, OP, 1>(src, a.R, cur.j);
+}
+
+}  // namespace vr

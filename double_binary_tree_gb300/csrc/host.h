@@ -21,6 +21,9 @@ const void* kernel_ptr_f32(int mode, int op, bool vec, int stack);
 const void* kernel_ptr_f16(int mode, int op, bool vec, int stack);
 const void* kernel_ptr_bf16(int mode, int op, bool vec, int stack);
 const void* kernel_ptr_allgather(bool vec);
+const void* staged_kernel_ptr_f32(int mode, int op, int stack);
+const void* staged_kernel_ptr_f16(int mode, int op, int stack);
+const void* staged_kernel_ptr_bf16(int mode, int op, int stack);
 
 // The current device's status word: its address, and read-and-clear.
 cudaError_t status_word_address(unsigned** p);

@@ -2,24 +2,41 @@
 // float (one translation unit per type, compiled in parallel).
 #include "host.h"
 #include "kernels.cuh"
+#include "staged.cuh"
 
 namespace vr {
 
+// Register-path kernels: `vec` = 16-byte units, else element units.
 const void* kernel_ptr_f32(int mode, int op, bool vec, int stack) {
-#define VR_PICK(OP, VEC)                                                         \
-  switch (mode) {                                                                \
+#define VR_PICK(OP, VEC)                                                                         \
+  switch (mode) {                                                                                \
     case kRingAllReduce: return (const void*)allreduce_kernel<float, OP, kRingAllReduce, VEC, 4>; \
-    case kTreeAllReduce:                                                         \
-      return stack <= 4 ? (const void*)allreduce_kernel<float, OP, kTreeAllReduce, VEC, 4>  \
-                        : (const void*)allreduce_kernel<float, OP, kTreeAllReduce, VEC, 8>;  \
-    case kReduceScatter: return (const void*)reduce_scatter_kernel<float, OP, VEC>;  \
-    default: return nullptr;                                                     \
+    case kTreeAllReduce:                                                                         \
+      return stack <= 4 ? (const void*)allreduce_kernel<float, OP, kTreeAllReduce, VEC, 4>        \
+                        : (const void*)allreduce_kernel<float, OP, kTreeAllReduce, VEC, 8>;       \
+    case kReduceScatter: return (const void*)reduce_scatter_kernel<float, OP, VEC>;               \
+    default: return nullptr;                                                                     \
   }
   if (op == VR_SUM) {
     if (vec) { VR_PICK(VR_SUM, true) } else { VR_PICK(VR_SUM, false) }
   } else {
     if (vec) { VR_PICK(VR_MAX, true) } else { VR_PICK(VR_MAX, false) }
   }
+#undef VR_PICK
+}
+
+// TMA-staged kernels (16-byte aligned buffers only).
+const void* staged_kernel_ptr_f32(int mode, int op, int stack) {
+#define VR_PICK(OP)                                                                       \
+  switch (mode) {                                                                         \
+    case kRingAllReduce: return (const void*)staged_kernel<float, OP, kRingAllReduce, 4>;  \
+    case kTreeAllReduce:                                                                  \
+      return stack <= 4 ? (const void*)staged_kernel<float, OP, kTreeAllReduce, 4>          \
+                        : (const void*)staged_kernel<float, OP, kTreeAllReduce, 8>;         \
+    case kReduceScatter: return (const void*)staged_kernel<float, OP, kReduceScatter, 4>;  \
+    default: return nullptr;                                                              \
+  }
+  if (op == VR_SUM) { VR_PICK(VR_SUM) } else { VR_PICK(VR_MAX) }
 #undef VR_PICK
 }
 

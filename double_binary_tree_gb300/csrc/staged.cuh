@@ -1,0 +1,264 @@
+// TMA-staged collective kernels (sm_103a): AllReduce (ring, tree) and
+// ReduceScatter on 16-byte aligned buffers.
+//
+// One CTA per SM.  The message is cut into tiles of 32*upl 16-byte units per
+// rank.  Warp 0 (the producer) moves each tile's R rank slices into a stage
+// of shared memory with bulk asynchronous copies (cp.async.bulk, completion
+// counted on the stage's "full" mbarrier); warp 1+s (a consumer) owns stage
+// s: it waits for the stage, folds every unit of the tile from shared memory
+// in the schedule's order (fold.cuh), stores the result to every receiving
+// rank straight from registers, and hands the stage back on its "empty"
+// mbarrier (up to 8 consumer warps, each owning every 8th stage).  With up
+// to 16 stages per SM the copies in flight no longer depend on registers,
+// which is what bounded the register-path kernels.
+//
+// Reduce-up and broadcast-down of the tree overlap the way the pages'
+// runTreeSplit overlaps them ([Course13] "runTreeSplit 如何流水": different
+// chunks are in different phases at once): while one stage is folded and
+// broadcast, the following stages' inputs are already being reduced into
+// shared memory.
+//
+// Every wait is bounded: after KArgs::timeoutNs the waiting warp records
+// VR_ERR_TIMEOUT in the status word and raises the CTA's abort flag; the
+// others leave their loops, and the producer still waits (bounded) for every
+// copy it issued before the CTA exits, so no copy lands in freed shared
+// memory.
+#pragma once
+
+#include "fold.cuh"
+
+namespace vr {
+
+constexpr int kWarpSize = 32;
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, unsigned bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait until the phase of `bar` with parity `parity` has completed.  Gives
+// up (false) after limit_ns, or as soon as *abort is raised when honor_abort.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, unsigned parity, const volatile int* abort,
+                                           bool honor_abort, unsigned long long limit_ns) {
+  if (mbar_test(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (unsigned it = 1;; ++it) {
+    if (mbar_test(bar, parity)) return true;
+    if ((it & 15) == 0) {
+      if (honor_abort && *abort) return false;
+      if (global_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void raise_error(unsigned* status, volatile int* abort, unsigned code) {
+  if (status) atomicCAS(status, 0u, code);
+  *abort = 1;
+}
+
+// Tile t of the message: the byte offset of its slice inside each source
+// rank's buffer, the bytes the producer copies, and the units it covers.
+struct TileGeom {
+  long long srcOff;   // bytes from each source buffer's start
+  unsigned bytes;     // bytes copied per rank (full 16-byte units only)
+  long long u0;       // first unit (AllReduce: of the message; ReduceScatter: of block b)
+  int units;          // units in the tile, a trailing partial unit included
+  int b;              // ReduceScatter: the block (and receiving rank)
+};
+
+template <int MODE>
+__device__ __forceinline__ TileGeom tile_geom(const KArgs& a, long long t) {
+  const int TU = kWarpSize * a.upl;
+  TileGeom g;
+  if constexpr (MODE == kReduceScatter) {
+    const long long perB = a.unitsFull;           // units of one block (all full)
+    const long long tilesB = (perB + TU - 1) / TU;
+    g.b = (int)(t / tilesB);
+    const long long tt = t - (long long)g.b * tilesB;
+    g.u0 = tt * TU;
+    g.units = (int)min((long long)TU, perB - g.u0);
+    g.bytes = (unsigned)g.units * 16u;
+    g.srcOff = (long long)g.b * perB * 16 + g.u0 * 16;
+  } else {
+    g.b = 0;
+    g.u0 = t * TU;
+    g.units = (int)min((long long)TU, a.unitsAll - g.u0);
+    const long long full = min((long long)TU, max(0LL, a.unitsFull - g.u0));
+    g.bytes = (unsigned)full * 16u;
+    g.srcOff = g.u0 * 16;
+  }
+  return g;
+}
+
+template <typename T, int OP, int MODE, int S>
+__global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
+    staged_kernel(const __grid_constant__ KArgs a) {
+  constexpr int U = Ty<T>::U;
+  constexpr long long E = sizeof(T);
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int NS = a.stages;
+  const int R = a.R;
+  const uint32_t TB = a.tileBytes;                   // bytes per rank per tile
+  const uint32_t stageBytes = a.stageBytes;          // R * TB, 128-byte multiple
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[s] = bars[s], empty[s] = bars[16 + s]
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + 16 * kStagedMaxStages);
+  const char** s_src = reinterpret_cast<const char**>(smem + 16 * kStagedMaxStages + 16);
+  char** s_dst = reinterpret_cast<char**>(smem + 16 * kStagedMaxStages + 16 + 8 * kMaxRanks);
+  FoldProg* s_prog = reinterpret_cast<FoldProg*>(s_dst + kMaxRanks);
+  static_assert(16 * kStagedMaxStages + 16 + 16 * kMaxRanks + 2 * sizeof(FoldProg) <= kStagedHeader,
+                "shared-memory header overflows");
+  const uint32_t data = smem_addr(smem + kStagedHeader);
+  const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kStagedMaxStages);
+
+  const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
+  for (int i = threadIdx.x; i < R; i += blockDim.x) {
+    s_src[i] = static_cast<const char*>(a.src[i]);
+    s_dst[i] = static_cast<char*>(a.dst[i]);
+  }
+  if constexpr (MODE == kTreeAllReduce) {
+    const unsigned* from = reinterpret_cast<const unsigned*>(a.prog);
+    unsigned* to = reinterpret_cast<unsigned*>(s_prog);
+    for (int i = threadIdx.x; i < (int)(2 * sizeof(FoldProg) / 4); i += blockDim.x) to[i] = from[i];
+  }
+  if (threadIdx.x == 0) {
+    *abort = 0;
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, 1);   // the producer's arrive (plus the copies' bytes)
+      mbar_init(empty0 + 8 * s, 1);  // the consumer's release
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+
+  const long long tb = a.tiles * blockIdx.x / gridDim.x;
+  const long long te = a.tiles * (blockIdx.x + 1) / gridDim.x;
+  const long long n = te - tb;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const long long stallAt = blockIdx.x == 0 ? a.injectStall : -1;
+    long long issued = 0;
+    for (long long i = 0; i < n; ++i) {
+      const int s = (int)(i % NS);
+      const long long k = i / NS;
+      if (k > 0) {
+        const bool ok = __any_sync(
+            ~0u, wait_phase(empty0 + 8 * s, (unsigned)((k - 1) & 1), abort, true, a.timeoutNs));
+        if (!ok) {
+          if (lane == 0 && !*abort) raise_error(a.status, abort, VR_ERR_TIMEOUT);
+          break;
+        }
+      }
+      if (__shfl_sync(~0u, *abort, 0)) break;
+      const TileGeom g = tile_geom<MODE>(a, tb + i);
+      if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * s, (unsigned)R * g.bytes);
+      __syncwarp();
+      issued = i + 1;
+      if (i == stallAt) continue;  // test hook: this fill never lands
+      if (g.bytes)
+        for (int r = lane; r < R; r += kWarpSize)
+          bulk_load(data + s * stageBytes + r * TB, s_src[r] + g.srcOff, g.bytes, full0 + 8 * s);
+    }
+    // Drain: every copy issued must have landed before the CTA may exit.
+    for (int s = 0; s < NS && s < issued; ++s) {
+      const long long last = s + ((issued - 1 - s) / NS) * NS;  // last tile index of stage s
+      if (last == stallAt) continue;
+      const bool ok = __any_sync(
+          ~0u, wait_phase(full0 + 8 * s, (unsigned)((last / NS) & 1), abort, false, a.timeoutNs));
+      if (!ok && lane == 0) raise_error(a.status, abort, VR_ERR_TIMEOUT);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
+  // Consumer c owns the stages c, c + NC, ... (NC divides NS): it takes the
+  // CTA's tiles c, c + NC, c + 2 NC, ... in order.
+  const int NC = a.consumers;
+  const int c = warp - 1;
+  if (c >= NC) return;
+  Cursor cur{0, -1, 0, 0};
+  for (long long i = c; i < n; i += NC) {
+    const int s = (int)(i % NS);
+    const bool ok =
+        __any_sync(~0u, wait_phase(full0 + 8 * s, (unsigned)((i / NS) & 1), abort, true, a.timeoutNs));
+    if (!ok) {
+      if (lane == 0 && !*abort) raise_error(a.status, abort, VR_ERR_TIMEOUT);
+      break;
+    }
+    const TileGeom g = tile_geom<MODE>(a, tb + i);
+    const uint32_t base = data + s * stageBytes;
+    for (int q = 0; q < a.upl; ++q) {
+      const int lu = lane + kWarpSize * q;
+      if (lu >= g.units) break;
+      if constexpr (MODE == kReduceScatter) {
+        const int j = g.b + 1 == R ? 0 : g.b + 1;
+        const SharedSrc src{base + 16u * lu, TB};
+        Unit<T, U>::store(s_dst[g.b] + (g.u0 + lu) * 16, ring_fold<T, OP, U>(src, R, j));
+      } else {
+        const long long u = g.u0 + lu;
+        const long long e0 = u * U;
+        if (u < a.unitsFull) {
+          if (e0 < cur.lo || e0 >= cur.hi) locate<U, MODE>(a, e0, cur);
+          if (e0 + U <= cur.hi) {
+            const SharedSrc src{base + 16u * lu, TB};
+            typename Unit<T, U>::Raw o;
+            if constexpr (MODE == kTreeAllReduce) o = tree_fold<T, OP, U, S>(src, s_prog[cur.t], R);
+            else o = ring_fold<T, OP, U>(src, R, cur.j);
+            for (int r = 0; r < R; ++r) Unit<T, U>::store(s_dst[r] + e0 * E, o);
+          } else {
+            // a unit cut by a ring block boundary: element by element
+            for (int x = 0; x < U; ++x) {
+              const SharedSrc src{base + 16u * lu + (uint32_t)(x * E), TB};
+              const typename Ty<T>::Bits o =
+                  fold_element<T, OP, MODE, S>(a, src, s_prog, e0 + x, cur);
+              for (int r = 0; r < R; ++r) Unit<T, 1>::store(s_dst[r] + (e0 + x) * E, o);
+            }
+          }
+        } else {
+          // the partial unit at the end of the message: not copied, read here
+          for (long long e = e0; e < a.count; ++e) {
+            const GlobalSrc src{s_src, e * E};
+            const typename Ty<T>::Bits o = fold_element<T, OP, MODE, S>(a, src, s_prog, e, cur);
+            for (int r = 0; r < R; ++r) Unit<T, 1>::store(s_dst[r] + e * E, o);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+  }
+}
+
+}  // namespace vr

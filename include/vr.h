@@ -183,6 +183,16 @@ vr_result_t vr_stream_status(void* stream);
  * all threads). */
 unsigned long long vr_launch_count(void);
 
+/* Test hook for the device-side failure path.  The next collective call
+ * that runs a shared-memory-staged kernel (16-byte aligned AllReduce or
+ * ReduceScatter) makes its first CTA skip the loads of its tile number
+ * `tile`, so the wait for that tile runs out after the bounded-wait limit
+ * (1 s, or VR_WAIT_TIMEOUT_NS nanoseconds from the environment at first
+ * use): that call's results are incomplete and vr_stream_status reports
+ * VR_ERR_TIMEOUT; the stream and the context stay usable.  -1 cancels a
+ * pending request.  Errors: VR_ERR_INVALID_ARGUMENT for tile < -1. */
+vr_result_t vr_debug_stall_next(long long tile);
+
 /* Static English text for a result code ("unknown result" for others). */
 const char* vr_get_error_string(vr_result_t result);
 
