@@ -431,12 +431,16 @@ def reference_arm(args):
 
 
 PROFILE_CASES = {
-    # name: (R, local ranks, dtype, op, algo) -- counts come from --count
-    "ring_r8_fp32": (8, 1, 0, 0, 0),
-    "tree_r8_bf16": (8, 1, 2, 0, 1),
-    "tree_r64_fp16_hier": (64, 8, 1, 0, 1),
-    "tree_r64_fp16_hier_max": (64, 8, 1, 1, 1),
-    "ring_r64_fp16": (64, 1, 1, 0, 0),
+    # name: (collective, R, local ranks, dtype, op, algo); counts come from
+    # --count (elements per rank for AllReduce, per block for the others)
+    "ring_r8_fp32": ("ar", 8, 1, 0, 0, 0),
+    "tree_r8_bf16": ("ar", 8, 1, 2, 0, 1),
+    "tree_r7_bf16": ("ar", 7, 1, 2, 0, 1),
+    "tree_r64_fp16_hier": ("ar", 64, 8, 1, 0, 1),
+    "tree_r64_fp16_hier_max": ("ar", 64, 8, 1, 1, 1),
+    "ring_r64_fp16": ("ar", 64, 1, 1, 0, 0),
+    "rs_r64_fp16": ("rs", 64, 1, 1, 0, 0),
+    "ag_r64_fp16": ("ag", 64, 1, 1, 0, 0),
 }
 
 
@@ -445,27 +449,39 @@ def profile_case(args):
     on the GPU: the command the ncu captures run."""
     import torch
     import double_binary_tree_gb300 as vr
-    R, L, dtype, op, algo = PROFILE_CASES[args.profile]
+    coll, R, L, dtype, op, algo = PROFILE_CASES[args.profile]
     count = args.count
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
     g = torch.Generator(device=dev)
     g.manual_seed(7)
     tdt = {0: torch.float32, 1: torch.float16, 2: torch.bfloat16}[dtype]
-    src = [torch.randn(count, generator=g, device=dev).to(tdt) for _ in range(R)]
-    dst = [torch.empty_like(s) for s in src]
+    n_in = {"ar": count, "rs": R * count, "ag": count}[coll]
+    n_out = {"ar": count, "rs": count, "ag": R * count}[coll]
+    src = [torch.randn(n_in, generator=g, device=dev).to(tdt) for _ in range(R)]
+    dst = [torch.empty(n_out, dtype=tdt, device=dev) for _ in range(R)]
+
+    def call():
+        if coll == "ar":
+            vr.vr_allreduce_ex(src, dst, R, count, dtype, op, algo, 12, 512 * 1024, L, stream)
+        elif coll == "rs":
+            vr.vr_reduce_scatter(src, dst, R, count, dtype, op, 0, 12, 512 * 1024, stream)
+        else:
+            vr.vr_allgather(src, dst, R, count, dtype, 0, 12, 512 * 1024, stream)
+
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for i in range(args.warmup + args.steps):
         if i == args.warmup:
             torch.cuda.synchronize()
             a.record(stream)
-        vr.vr_allreduce_ex(src, dst, R, count, dtype, op, algo, 12, 512 * 1024, L, stream)
+        call()
     b.record(stream)
     torch.cuda.synchronize()
     if vr.vr_stream_status(stream) != 0:
         raise RuntimeError("device status error")
     ms = a.elapsed_time(b) / max(args.steps, 1)
-    nbytes = ar_bytes(R, count, dtype)
+    E = elem_size(dtype)
+    nbytes = (n_in + n_out) * R * E
     print(json.dumps({"profile": args.profile, "count": count, "us": round(ms * 1e3, 2),
                       "hbm_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}))
 

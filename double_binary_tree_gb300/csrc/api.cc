@@ -31,6 +31,12 @@ std::map<std::pair<int, int>, std::array<FoldProg, 2>> g_progs;  // (nNodes, loc
 std::map<std::pair<const void*, int>, int> g_smemSet;            // (kernel, device) -> bytes
 std::atomic<long long> g_stallNext{-1};                          // test hook
 
+// Tuning overrides read from the environment (0 when unset).
+unsigned env_uint(const char* name, unsigned dflt) {
+  const char* v = std::getenv(name);
+  return v ? (unsigned)std::strtoul(v, nullptr, 10) : dflt;
+}
+
 unsigned long long wait_timeout_ns() {
   static const unsigned long long ns = [] {
     const char* v = std::getenv("VR_WAIT_TIMEOUT_NS");
@@ -205,8 +211,8 @@ vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream) {
   return VR_SUCCESS;
 }
 
-// Staged geometry: tiles of 32 * upl 16-byte units per rank; as many stages
-// (one consumer warp each, at most 16) as fit in the opt-in shared memory.
+// Staged geometry: tiles of tileUnits 16-byte units per rank; as many stages
+// (at most 16) as fit in the opt-in shared memory; up to 8 consumer warps.
 // a.unitsAll / a.unitsFull describe the message (AllReduce) or one block
 // (ReduceScatter); the tile count follows from the geometry.
 vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
@@ -219,17 +225,27 @@ vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
   if ((e = check_reachable(const_cast<const void* const*>(a.dst), a.R, device)) != VR_SUCCESS)
     return e;
   a.status = di.status;
-  a.upl = a.R <= 4 ? 4 : (a.R <= 16 ? 2 : 1);
-  a.tileBytes = 512u * (unsigned)a.upl;
-  const long long TU = 32LL * a.upl;
+  // Largest per-rank tile (fewer, larger bulk copies) that still leaves
+  // at least kMinStages stages in the opt-in shared memory.
+  const int room = di.smemOptin - kStagedHeader;
+  unsigned tb = env_uint("VR_STAGED_TILE_BYTES", 0);
+  int minStages = (int)env_uint("VR_STAGED_MIN_STAGES", 3);
+  if (!tb) {
+    tb = 8192;
+    while (tb > 512 && (long long)a.R * tb * minStages > room) tb >>= 1;
+  }
+  a.tileBytes = tb;
+  a.tileUnits = (int)(tb / 16);
+  const long long TU = a.tileUnits;
   a.tiles = mode == kReduceScatter ? (long long)a.R * ((a.unitsFull + TU - 1) / TU)
                                    : (a.unitsAll + TU - 1) / TU;
   a.stageBytes = ((unsigned)a.R * a.tileBytes + 127u) & ~127u;
-  const int fit = (di.smemOptin - kStagedHeader) / (int)a.stageBytes;
+  const int fit = room / (int)a.stageBytes;
   a.stages = std::min(kStagedMaxStages, fit);
+  const int cap = (int)env_uint("VR_STAGED_STAGES", 0);
+  if (cap) a.stages = std::min(a.stages, cap);
   if (a.stages < 2) return VR_ERR_INTERNAL;
-  if (a.stages > kStagedMaxConsumers) a.stages -= a.stages % kStagedMaxConsumers;
-  a.consumers = std::min(a.stages, kStagedMaxConsumers);
+  a.consumers = std::max(1, std::min(kStagedMaxConsumers, a.tileUnits / 32));
   const size_t smem = kStagedHeader + (size_t)a.stages * a.stageBytes;
   {
     std::lock_guard<std::mutex> g(g_mu);

@@ -12,7 +12,7 @@ constexpr int kMaxChannels = VR_MAX_CHANNELS;
 constexpr int kGrainBytes = 16;      // channel ranges are cut in 16-byte grains
 constexpr int kMaxStack = 8;         // partial sums a tree fold keeps live at once
 constexpr int kStagedMaxStages = 16; // shared-memory stages of a staged kernel
-constexpr int kStagedMaxConsumers = 8;  // its consumer warps (each owns every 8th stage)
+constexpr int kStagedMaxConsumers = 8;  // its consumer warps (all of them fold every stage)
 constexpr int kStagedHeader = 2048;  // its barriers, flags, pointer tables and programs
 
 // A tree's reduction order as a stream of rank loads.  Slot i loads rank
@@ -49,13 +49,13 @@ struct KArgs {
   // TMA-staged kernels (staged.cuh)
   long long unitsAll;   // 16-byte units of the message, a trailing partial one included
   long long unitsFull;  // full 16-byte units (ReduceScatter: per block)
-  long long tiles;      // tiles of 32 * upl units
+  long long tiles;      // tiles of tileUnits units
   unsigned long long timeoutNs;  // limit of every bounded wait
   long long injectStall;         // test hook: CTA 0 never loads its tile of this index (-1: off)
   int stages;           // shared-memory stages
-  int consumers;        // consumer warps (divides stages)
-  int upl;              // units per lane per tile
-  unsigned tileBytes;   // bytes per rank per tile (32 * upl * 16)
+  int consumers;        // consumer warps
+  int tileUnits;        // 16-byte units per rank per tile
+  unsigned tileBytes;   // bytes per rank per tile (16 * tileUnits)
   unsigned stageBytes;  // R * tileBytes
   FoldProg prog[2];
 };

@@ -1,16 +1,16 @@
 // TMA-staged collective kernels (sm_103a): AllReduce (ring, tree) and
 // ReduceScatter on 16-byte aligned buffers.
 //
-// One CTA per SM.  The message is cut into tiles of 32*upl 16-byte units per
-// rank.  Warp 0 (the producer) moves each tile's R rank slices into a stage
-// of shared memory with bulk asynchronous copies (cp.async.bulk, completion
-// counted on the stage's "full" mbarrier); warp 1+s (a consumer) owns stage
-// s: it waits for the stage, folds every unit of the tile from shared memory
-// in the schedule's order (fold.cuh), stores the result to every receiving
-// rank straight from registers, and hands the stage back on its "empty"
-// mbarrier (up to 8 consumer warps, each owning every 8th stage).  With up
-// to 16 stages per SM the copies in flight no longer depend on registers,
-// which is what bounded the register-path kernels.
+// One CTA per SM.  The message is cut into tiles of tileUnits 16-byte units
+// per rank.  Warp 0 (the producer) moves each tile's R rank slices into a
+// stage of shared memory with bulk asynchronous copies (cp.async.bulk, one
+// copy of tileBytes per rank, completion counted on the stage's "full"
+// mbarrier); the consumer warps wait for the stage, fold its units from
+// shared memory in the schedule's order (fold.cuh), each thread a strided
+// share of the tile, store the results to every receiving rank straight from
+// registers, and hand the stage back on its "empty" mbarrier.  The copies in
+// flight depend on the stages, not on registers, which is what bounded the
+// register-path kernels.
 //
 // Reduce-up and broadcast-down of the tree overlap the way the pages'
 // runTreeSplit overlaps them ([Course13] "runTreeSplit 如何流水": different
@@ -99,7 +99,7 @@ struct TileGeom {
 
 template <int MODE>
 __device__ __forceinline__ TileGeom tile_geom(const KArgs& a, long long t) {
-  const int TU = kWarpSize * a.upl;
+  const int TU = a.tileUnits;
   TileGeom g;
   if constexpr (MODE == kReduceScatter) {
     const long long perB = a.unitsFull;           // units of one block (all full)
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
     *abort = 0;
     for (int s = 0; s < NS; ++s) {
       mbar_init(full0 + 8 * s, 1);   // the producer's arrive (plus the copies' bytes)
-      mbar_init(empty0 + 8 * s, 1);  // the consumer's release
+      mbar_init(empty0 + 8 * s, a.consumers);  // one release per consumer warp
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -203,13 +203,14 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
   }
 
   // ------------------------------------------------------------ consumers
-  // Consumer c owns the stages c, c + NC, ... (NC divides NS): it takes the
-  // CTA's tiles c, c + NC, c + 2 NC, ... in order.
+  // Every consumer warp takes part in every tile: thread ct folds the units
+  // ct, ct + 32 * NC, ... of the tile.
   const int NC = a.consumers;
-  const int c = warp - 1;
-  if (c >= NC) return;
+  if (warp > NC) return;
+  const int ct = threadIdx.x - kWarpSize;
+  const int nct = kWarpSize * NC;
   Cursor cur{0, -1, 0, 0};
-  for (long long i = c; i < n; i += NC) {
+  for (long long i = 0; i < n; ++i) {
     const int s = (int)(i % NS);
     const bool ok =
         __any_sync(~0u, wait_phase(full0 + 8 * s, (unsigned)((i / NS) & 1), abort, true, a.timeoutNs));
@@ -219,9 +220,7 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
     }
     const TileGeom g = tile_geom<MODE>(a, tb + i);
     const uint32_t base = data + s * stageBytes;
-    for (int q = 0; q < a.upl; ++q) {
-      const int lu = lane + kWarpSize * q;
-      if (lu >= g.units) break;
+    for (int lu = ct; lu < g.units; lu += nct) {
       if constexpr (MODE == kReduceScatter) {
         const int j = g.b + 1 == R ? 0 : g.b + 1;
         const SharedSrc src{base + 16u * lu, TB};
