@@ -46,14 +46,14 @@ unsigned long long wait_timeout_ns() {
   return ns;
 }
 
-// Temporary comparison switch: VR_KERNEL_PATH=register runs aligned
-// AllReduce / ReduceScatter on the register-path kernels.
-bool force_register_path() {
-  static const bool on = [] {
-    const char* v = std::getenv("VR_KERNEL_PATH");
-    return v && std::strcmp(v, "register") == 0;
-  }();
-  return on;
+// Temporary comparison switch (read on every call): VR_KERNEL_PATH=register
+// or =staged forces aligned AllReduce / ReduceScatter onto one kernel family.
+int forced_path() {
+  const char* v = std::getenv("VR_KERNEL_PATH");
+  if (!v) return 0;
+  if (std::strcmp(v, "register") == 0) return 1;
+  if (std::strcmp(v, "staged") == 0) return 2;
+  return 0;
 }
 
 size_t elem_size(int dtype) {
@@ -211,6 +211,16 @@ vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream) {
   return VR_SUCCESS;
 }
 
+// Which kernel family serves an aligned AllReduce / ReduceScatter: the
+// staged kernels need per-rank copies of at least 2 KB with several stages
+// resident (few ranks) and enough tiles per SM to amortise their pipeline
+// fill (large messages); otherwise the register path is faster.
+bool use_staged(int R, size_t bytesPerRank) {
+  const size_t minBytes = env_uint("VR_STAGED_MIN_BYTES", 8u << 20);
+  const int maxR = (int)env_uint("VR_STAGED_MAX_RANKS", 16);
+  return R <= maxR && bytesPerRank >= minBytes;
+}
+
 // Staged geometry: tiles of tileUnits 16-byte units per rank; as many stages
 // (at most 16) as fit in the opt-in shared memory; up to 8 consumer warps.
 // a.unitsAll / a.unitsFull describe the message (AllReduce) or one block
@@ -231,7 +241,7 @@ vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
   unsigned tb = env_uint("VR_STAGED_TILE_BYTES", 0);
   int minStages = (int)env_uint("VR_STAGED_MIN_STAGES", 3);
   if (!tb) {
-    tb = 8192;
+    tb = 2048;
     while (tb > 512 && (long long)a.R * tb * minStages > room) tb >>= 1;
   }
   a.tileBytes = tb;
@@ -369,7 +379,8 @@ vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, 
     stack = std::max(p[0].depth, p[1].depth);
   }
   const bool vec = aligned16(sendbufs, R, 0) && aligned16(recvbufs, R, 0);
-  if (vec && !force_register_path()) {
+  const int forced = forced_path();
+  if (vec && forced != 1 && (forced == 2 || use_staged(R, count * E))) {
     const long long bytes = (long long)count * (long long)E;
     a.unitsAll = (bytes + 15) / 16;
     a.unitsFull = bytes / 16;
@@ -405,7 +416,8 @@ vr_result_t vr_reduce_scatter(const void* const* sendbufs, void* const* recvbufs
   a.nCh = nChannels;
   a.chunk = (long long)(chunkBytes / E);
   const bool vec = aligned16(sendbufs, R, recvcount * E) && aligned16(recvbufs, R, 0);
-  if (vec && !force_register_path()) {
+  const int forced = forced_path();
+  if (vec && forced != 1 && (forced == 2 || use_staged(R, recvcount * E * R))) {
     a.unitsFull = (long long)(recvcount * E / 16);
     a.unitsAll = a.unitsFull;
     return launch_staged(pick_staged(dtype, kReduceScatter, op), a, kReduceScatter, stream);

@@ -6,6 +6,8 @@ output buffer is surrounded by canary bytes that must survive the call.
 Inputs come from workloads.py only; no expected value comes from the GPU.
 """
 
+import os
+
 import numpy as np
 import pytest
 
@@ -29,6 +31,20 @@ RING, TREE = vr.VR_ALGO_RING, vr.VR_ALGO_TREE
 TDT = workloads.TORCH_DTYPE
 PAD = 64            # canary elements before and after every output
 CANARY = 0x5A
+
+
+@pytest.fixture(params=["register", "staged"])
+def path(request):
+    """Runs the test on one kernel family: the register path or the
+    shared-memory-staged path (unaligned buffers always take the register
+    path's element kernels)."""
+    old = os.environ.get("VR_KERNEL_PATH")
+    os.environ["VR_KERNEL_PATH"] = request.param
+    yield request.param
+    if old is None:
+        os.environ.pop("VR_KERNEL_PATH", None)
+    else:
+        os.environ["VR_KERNEL_PATH"] = old
 
 
 class Bufs:
@@ -99,7 +115,7 @@ def assert_bits_equal(got, want, what=""):
 
 
 # ------------------------------------------------------------ worked cases
-def test_two_rank_example_ring_and_tree():
+def test_two_rank_example_ring_and_tree(path):
     inp = workloads.two_rank()
     for algo in (RING, TREE):
         got = run_allreduce(inp, F32, SUM, algo, 1, 16)
@@ -117,7 +133,7 @@ def test_small_ring_workload_exact():
         assert np.array_equal(g.astype(np.float64), s)     # integers: exact
 
 
-def test_ring_trace_bitmask():
+def test_ring_trace_bitmask(path):
     # rank r holds 2**r: every output is 2**R - 1 whatever the order
     for R in (2, 3, 4, 8, 16, 24):
         inp = workloads.generate(R, 333, F32, "pow2", 0)
@@ -137,7 +153,7 @@ RING_CASES = [
 
 @pytest.mark.parametrize("dtype", [F32, F16, BF16])
 @pytest.mark.parametrize("R,count,nch,cb", RING_CASES)
-def test_ring_bit_exact(R, count, nch, cb, dtype):
+def test_ring_bit_exact(R, count, nch, cb, dtype, path):
     inp = workloads.generate(R, count, dtype, "normal", 100 + R)
     _, want = expect_allreduce(inp, dtype, SUM, RING, nch, cb)
     assert_bits_equal(run_allreduce(inp, dtype, SUM, RING, nch, cb), want)
@@ -155,7 +171,7 @@ TREE_CASES = [
 
 @pytest.mark.parametrize("dtype", [F32, F16, BF16])
 @pytest.mark.parametrize("R,L,count,nch,cb", TREE_CASES)
-def test_tree_bit_exact(R, L, count, nch, cb, dtype):
+def test_tree_bit_exact(R, L, count, nch, cb, dtype, path):
     inp = workloads.generate(R, count, dtype, "normal", 200 + R)
     _, want = expect_allreduce(inp, dtype, SUM, TREE, nch, cb, L)
     assert_bits_equal(run_allreduce(inp, dtype, SUM, TREE, nch, cb, L), want)
@@ -163,7 +179,7 @@ def test_tree_bit_exact(R, L, count, nch, cb, dtype):
 
 @pytest.mark.parametrize("algo", [RING, TREE])
 @pytest.mark.parametrize("dtype", [F32, F16, BF16])
-def test_max_exact(algo, dtype):
+def test_max_exact(algo, dtype, path):
     for R, L, count in [(2, 1, 1000), (7, 1, 4097), (64, 8, 3001)]:
         inp = workloads.generate(R, count, dtype, "uniform", 300 + R)
         raws, want = expect_allreduce(inp, dtype, MAX, algo, 12, 64, L)
@@ -173,7 +189,7 @@ def test_max_exact(algo, dtype):
         assert np.array_equal(numerics.to_f32(got[0], dtype).astype(np.float64), m)
 
 
-def test_max_signed_zero_total_order():
+def test_max_signed_zero_total_order(path):
     # +0 above -0, whatever the order in which they meet
     a = torch.tensor([0.0, -0.0, -0.0, -0.0, 0.0])
     b = torch.tensor([-0.0, 0.0, -0.0, -1.0, -0.0])
@@ -187,7 +203,7 @@ def test_max_signed_zero_total_order():
 
 
 @pytest.mark.parametrize("algo", [RING, TREE])
-def test_in_place(algo):
+def test_in_place(algo, path):
     for dtype in (F32, BF16):
         inp = workloads.generate(8, 50001, dtype, "normal", 400)
         _, want = expect_allreduce(inp, dtype, SUM, algo, 12, 1024)
@@ -203,7 +219,7 @@ def test_misaligned_buffers_take_element_path(algo):
 
 
 @pytest.mark.parametrize("dtype", [F32, F16, BF16])
-def test_within_fp64_tolerance(dtype):
+def test_within_fp64_tolerance(dtype, path):
     inp = workloads.generate(8, 200003, dtype, "normal", 600)
     raws = [workloads.raw_numpy(t) for t in inp]
     s = oracle.fp64_sum(raws, dtype)
@@ -224,7 +240,7 @@ def test_zero_count_is_a_no_op():
 # ------------------------------------------------- ReduceScatter, AllGather
 @pytest.mark.parametrize("dtype", [F32, F16, BF16])
 @pytest.mark.parametrize("op", [SUM, MAX])
-def test_reduce_scatter_bit_exact(dtype, op):
+def test_reduce_scatter_bit_exact(dtype, op, path):
     for R, rc, inplace in [(1, 5, False), (2, 3, False), (4, 1000, False), (7, 3001, True),
                            (8, 4096, False), (64, 513, False), (64, 1024, True)]:
         inp = workloads.generate(R, R * rc, dtype, "normal", 700 + R)
@@ -280,7 +296,7 @@ def _channel_slice_sim(raws_f32, count, E, R, nch, C, k, op):
     return cs, cn, out
 
 
-def test_ring_64mib_fp32_full_size():
+def test_ring_64mib_fp32_full_size(path):
     w = workloads.workload("ring_64mib")
     R, count, nch, cb = w["R"], w["count"], w["n_channels"], w["chunk_bytes"]
     src = [t.cuda() for t in w["inputs"]]
@@ -301,7 +317,7 @@ def test_ring_64mib_fp32_full_size():
 
 @pytest.mark.parametrize("name", ["tree_4mib_r8", "tree_4mib_r7"])
 @pytest.mark.parametrize("nch", [2, 12])
-def test_tree_4mib_bf16_full_size(name, nch):
+def test_tree_4mib_bf16_full_size(name, nch, path):
     w = workloads.workload(name)
     inp = w["inputs"]
     raws, want = expect_allreduce(inp, BF16, SUM, TREE, nch, w["chunk_bytes"])
