@@ -348,6 +348,9 @@ struct Cursor {
   long long lo, hi;
   int j;  // ring block number
   int t;  // tree index of the channel
+  // ring: the current loop's end and block sizes (q + 1 for the first m)
+  long long loopEnd, q;
+  int m;
 };
 
 template <int U>
@@ -400,7 +403,29 @@ __device__ __forceinline__ void locate(const KArgs& a, long long e, Cursor& c) {
     c.hi = c.lo + bl;
     c.j = (int)j;
     c.t = 0;
+    c.loopEnd = cs + ls + L;
+    c.q = q;
+    c.m = (int)m;
   }
+}
+
+// Move the cursor to element e.  A thread walks the message forwards, so
+// stepping through the following blocks of the same ring loop (adds and
+// compares) is the common case; anything else is located from scratch.
+template <int U, int MODE>
+__device__ __forceinline__ void seek(const KArgs& a, long long e, Cursor& c) {
+  if (e >= c.lo && e < c.hi) return;
+  if constexpr (MODE != kTreeAllReduce) {
+    if (e >= c.hi && e < c.loopEnd) {
+      do {
+        ++c.j;
+        c.lo = c.hi;
+        c.hi = c.lo + c.q + (c.j < c.m ? 1 : 0);
+      } while (e >= c.hi);
+      return;
+    }
+  }
+  locate<U, MODE>(a, e, c);
 }
 
 // One element of an AllReduce: its fold in the schedule of element e.
@@ -408,7 +433,7 @@ template <typename T, int OP, int MODE, int S, class Src>
 __device__ __forceinline__ typename Ty<T>::Bits fold_element(const KArgs& a, const Src& src,
                                                             const FoldProg* progs, long long e,
                                                             Cursor& cur) {
-  if (e < cur.lo || e >= cur.hi) locate<Ty<T>::U, MODE>(a, e, cur);
+  seek<Ty<T>::U, MODE>(a, e, cur);
   if constexpr (MODE == kTreeAllReduce) return tree_fold<T, OP, 1, S>(src, progs[cur.t], a.R);
   else return ring_fold<T, OP, 1>(src, a.R, cur.j);
 }

@@ -52,11 +52,11 @@ __global__ void __launch_bounds__(kBlock) allreduce_kernel(const __grid_constant
   const long long units = (count + NV - 1) / NV;
   const long long ub = units * blockIdx.x / gridDim.x;
   const long long ue = units * (blockIdx.x + 1) / gridDim.x;
-  Cursor cur{0, -1, 0, 0};
+  Cursor cur{0, -1, 0, 0, 0, 0, 0};
   for (long long u = ub + threadIdx.x; u < ue; u += blockDim.x) {
     const long long e0 = u * NV;
     const int n = (int)min((long long)NV, count - e0);
-    if (e0 < cur.lo || e0 >= cur.hi) locate<U, MODE>(a, e0, cur);
+    seek<U, MODE>(a, e0, cur);
     if (n == NV && e0 + NV <= cur.hi) {
       const GlobalSrc src{s_src, e0 * E};
       typename Unit<T, NV>::Raw o;

@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
   if (warp > NC) return;
   const int ct = threadIdx.x - kWarpSize;
   const int nct = kWarpSize * NC;
-  Cursor cur{0, -1, 0, 0};
+  Cursor cur{0, -1, 0, 0, 0, 0, 0};
   for (long long i = 0; i < n; ++i) {
     const int s = (int)(i % NS);
     const bool ok =
@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
         const long long u = g.u0 + lu;
         const long long e0 = u * U;
         if (u < a.unitsFull) {
-          if (e0 < cur.lo || e0 >= cur.hi) locate<U, MODE>(a, e0, cur);
+          seek<U, MODE>(a, e0, cur);
           if (e0 + U <= cur.hi) {
             const SharedSrc src{base + 16u * lu, TB};
             typename Unit<T, U>::Raw o;
