@@ -211,15 +211,20 @@ vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream) {
   return VR_SUCCESS;
 }
 
-// Which kernel family serves an aligned AllReduce / ReduceScatter: the
-// staged kernels need per-rank copies of at least 2 KB with several stages
-// resident (few ranks) and enough tiles per SM to amortise their pipeline
-// fill (large messages); otherwise the register path is faster.
-bool use_staged(int R, size_t bytesPerRank) {
-  const size_t minBytes = env_uint("VR_STAGED_MIN_BYTES", 8u << 20);
-  const int maxR = (int)env_uint("VR_STAGED_MAX_RANKS", 16);
-  return R <= maxR && bytesPerRank >= minBytes;
+// Which kernel family serves an aligned collective.  Measured on GB300
+// (ring and tree, R = 2..64, 1..128 MiB per rank): the staged kernel wins
+// for the ring with 8..32 ranks and at least 16 MiB per rank; its consumer
+// warps are too few to hide the latency of the tree's data-dependent fold
+// and of ReduceScatter's 64-rank folds, and with few ranks its stages hold
+// too few bytes in flight.  Everything else runs on the register path.
+bool use_staged(int mode, int R, size_t bytesPerRank) {
+  const size_t minBytes = env_uint("VR_STAGED_MIN_BYTES", 16u << 20);
+  return mode == kRingAllReduce && R >= 8 && R <= 32 && bytesPerRank >= minBytes;
 }
+
+// Per-rank tile bytes of the staged kernel (bulk copies below 2 KB lose
+// throughput; 4 KB measured best for 9..16 ranks).
+unsigned staged_tile_bytes(int R) { return R > 8 && R <= 16 ? 4096u : 2048u; }
 
 // Staged geometry: tiles of tileUnits 16-byte units per rank; as many stages
 // (at most 16) as fit in the opt-in shared memory; up to 8 consumer warps.
@@ -241,7 +246,7 @@ vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
   unsigned tb = env_uint("VR_STAGED_TILE_BYTES", 0);
   int minStages = (int)env_uint("VR_STAGED_MIN_STAGES", 3);
   if (!tb) {
-    tb = 2048;
+    tb = staged_tile_bytes(a.R);
     while (tb > 512 && (long long)a.R * tb * minStages > room) tb >>= 1;
   }
   a.tileBytes = tb;
@@ -380,7 +385,7 @@ vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, 
   }
   const bool vec = aligned16(sendbufs, R, 0) && aligned16(recvbufs, R, 0);
   const int forced = forced_path();
-  if (vec && forced != 1 && (forced == 2 || use_staged(R, count * E))) {
+  if (vec && forced != 1 && (forced == 2 || use_staged(mode, R, count * E))) {
     const long long bytes = (long long)count * (long long)E;
     a.unitsAll = (bytes + 15) / 16;
     a.unitsFull = bytes / 16;
@@ -417,7 +422,7 @@ vr_result_t vr_reduce_scatter(const void* const* sendbufs, void* const* recvbufs
   a.chunk = (long long)(chunkBytes / E);
   const bool vec = aligned16(sendbufs, R, recvcount * E) && aligned16(recvbufs, R, 0);
   const int forced = forced_path();
-  if (vec && forced != 1 && (forced == 2 || use_staged(R, recvcount * E * R))) {
+  if (vec && forced != 1 && (forced == 2 || use_staged(kReduceScatter, R, recvcount * E * R))) {
     a.unitsFull = (long long)(recvcount * E / 16);
     a.unitsAll = a.unitsFull;
     return launch_staged(pick_staged(dtype, kReduceScatter, op), a, kReduceScatter, stream);

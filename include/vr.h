@@ -130,10 +130,10 @@ vr_result_t vr_ring_block(size_t count, vr_dtype_t dtype, int R, int nChannels,
  * chunkBytes (a positive multiple of 16) is the per-rank chunk C of a ring
  * loop and the chunk of a tree channel.
  * In place: sendbufs[r] == recvbufs[r] is allowed.
- * Buffers: any alignment.  16-byte aligned buffers run 16-byte units: on a
- * kernel that stages each tile of all R ranks in shared memory with bulk
- * asynchronous copies when there are at most 16 ranks and at least 8 MiB per
- * rank, else on a kernel that loads the ranks' units into registers.  The
+ * Buffers: any alignment.  16-byte aligned buffers run 16-byte units: the
+ * ring with 8..32 ranks and at least 16 MiB per rank on a kernel that stages
+ * each tile of all R ranks in shared memory with bulk asynchronous copies,
+ * everything else on a kernel that loads the ranks' units into registers.  The
  * environment variable VR_KERNEL_PATH=staged|register (read on every call)
  * forces one of the two for testing and tuning; results are identical.
  * Unaligned buffers run element units on the register kernel.
