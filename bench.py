@@ -232,7 +232,7 @@ def gpu_arm(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": round(per_gpu, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(per_gpu / peak, 4), "traffic": traffic,
                      "peak_source": "%s copy bandwidth, burst" % peak_kind,
-                     "kernel": "allreduce_kernel<float, Sum, ring, vec>",
+                     "kernel": "staged_kernel<float, Sum, ring>",
                      "algorithmic_bytes_per_launch": nbytes},
         "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
     }
