@@ -67,23 +67,6 @@ __device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
                "r"(v.w)
                : "memory");
 }
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(a));
-  return v;
-}
-__device__ __forceinline__ unsigned ld_shared_u32(uint32_t a) {
-  unsigned v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ unsigned short ld_shared_u16(uint32_t a) {
-  unsigned short v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
-  return v;
-}
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -134,8 +117,8 @@ struct GlobalSrc {              // ptr[r] + off, global memory
   long long off;
 };
 struct SharedSrc {              // base + r * stride, shared memory
-  uint32_t base;
-  uint32_t stride;
+  const unsigned char* base;    // plain loads: the compiler may schedule them freely,
+  uint32_t stride;              // but not across the mbarrier wait (a memory clobber)
 };
 
 template <typename T, int NV>
@@ -146,10 +129,7 @@ __device__ __forceinline__ typename Unit<T, NV>::Raw load_unit(const GlobalSrc& 
 }
 template <typename T, int NV>
 __device__ __forceinline__ typename Unit<T, NV>::Raw load_unit(const SharedSrc& s, int r) {
-  const uint32_t a = s.base + (uint32_t)r * s.stride;
-  if constexpr (NV != 1) return ld_shared_v4(a);
-  else if constexpr (sizeof(T) == 4) return ld_shared_u32(a);
-  else return ld_shared_u16(a);
+  return *reinterpret_cast<const typename Unit<T, NV>::Raw*>(s.base + (uint32_t)r * s.stride);
 }
 
 // ----------------------------------------------------------- reduction op
@@ -253,6 +233,65 @@ __device__ __forceinline__ typename Unit<T, NV>::Raw ring_fold(const Src& src, i
     }
   }
   return Ln::encode(acc);
+}
+
+// A unit whose elements [0, split) lie in ring block j and [split, NV) in
+// block j+1 (the next block of the same loop): the first folds ranks
+// j, j+1, ..., j-1, the second j+1, ..., j-1, j -- the same loads, one rank
+// later.  Both folds run over one pass of vector loads (rank j's value is
+// kept and folded last into the second), and each element takes its own.
+template <typename T, int OP, class Src>
+__device__ __forceinline__ uint4 ring_fold_split(const Src& src, int R, int j, int split) {
+  constexpr int NV = Ty<T>::U;
+  typedef Unit<T, NV> Un;
+  typedef Lanes<T, OP, NV> Ln;
+  typename Ln::L a[Ln::N], b[Ln::N], first[Ln::N];
+#pragma unroll
+  for (int e = 0; e < Ln::N; ++e) a[e] = b[e] = first[e] = 0;
+  for (int k0 = 0; k0 < R; k0 += kBatch) {
+    uint4 v[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int k = k0 + i;
+      if (k < R) {
+        int r = j + k;
+        r -= r >= R ? R : 0;
+        v[i] = load_unit<T, NV>(src, r);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int k = k0 + i;
+      if (k < R) {
+        typename Ln::L x[Ln::N];
+        Ln::decode(v[i], x);
+#pragma unroll
+        for (int e = 0; e < Ln::N; ++e) {
+          if (k == 0) {
+            a[e] = x[e];
+            first[e] = x[e];
+          } else {
+            a[e] = Ln::op(a[e], x[e]);
+            b[e] = k == 1 ? x[e] : Ln::op(b[e], x[e]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < Ln::N; ++e) b[e] = R == 1 ? first[e] : Ln::op(b[e], first[e]);
+  const uint4 ra = Ln::encode(a), rb = Ln::encode(b);
+  // element e of the unit occupies bytes [e*E, (e+1)*E): keep ra's bytes below split*E
+  const int cut = split * (int)sizeof(T);
+  unsigned w[4];
+  const unsigned wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int lo = 4 * i;  // first byte of word i
+    const unsigned keepA = cut >= lo + 4 ? 0xFFFFFFFFu : (cut <= lo ? 0u : (1u << (8 * (cut - lo))) - 1u);
+    w[i] = (wa[i] & keepA) | (wb[i] & ~keepA);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // Partials of a tree fold.  The top partial lives in fixed registers, so

@@ -63,8 +63,14 @@ __global__ void __launch_bounds__(kBlock) allreduce_kernel(const __grid_constant
       if constexpr (MODE == kTreeAllReduce) o = tree_fold<T, OP, NV, S>(src, s_prog[cur.t], R);
       else o = ring_fold<T, OP, NV>(src, R, cur.j);
       for (int r = 0; r < R; ++r) Unit<T, NV>::store(s_dst[r] + e0 * E, o);
+    } else if (MODE == kRingAllReduce && VEC && n == NV && e0 + NV <= cur.loopEnd &&
+               e0 + NV <= cur.hi + cur.q + (cur.j + 1 < cur.m ? 1 : 0)) {
+      // a unit cut by one ring block boundary inside a loop
+      const GlobalSrc src{s_src, e0 * E};
+      const uint4 o = ring_fold_split<T, OP>(src, R, cur.j, (int)(cur.hi - e0));
+      for (int r = 0; r < R; ++r) st_global_v4(s_dst[r] + e0 * E, o);
     } else {
-      // a unit cut by the end of the message or by a ring block boundary
+      // a unit cut by the end of the message or by several block boundaries
       for (int i = 0; i < n; ++i) {
         const long long e = e0 + i;
         const GlobalSrc src{s_src, e * E};

@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
   static_assert(16 * kStagedMaxStages + 16 + 16 * kMaxRanks + 2 * sizeof(FoldProg) <= kStagedHeader,
                 "shared-memory header overflows");
   const uint32_t data = smem_addr(smem + kStagedHeader);
+  const unsigned char* stage0 = smem + kStagedHeader;
   const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kStagedMaxStages);
 
   const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
@@ -219,11 +220,11 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
       break;
     }
     const TileGeom g = tile_geom<MODE>(a, tb + i);
-    const uint32_t base = data + s * stageBytes;
+    const unsigned char* base = stage0 + (size_t)s * stageBytes;
     for (int lu = ct; lu < g.units; lu += nct) {
       if constexpr (MODE == kReduceScatter) {
         const int j = g.b + 1 == R ? 0 : g.b + 1;
-        const SharedSrc src{base + 16u * lu, TB};
+        const SharedSrc src{base + 16 * lu, TB};
         Unit<T, U>::store(s_dst[g.b] + (g.u0 + lu) * 16, ring_fold<T, OP, U>(src, R, j));
       } else {
         const long long u = g.u0 + lu;
@@ -231,15 +232,21 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
         if (u < a.unitsFull) {
           seek<U, MODE>(a, e0, cur);
           if (e0 + U <= cur.hi) {
-            const SharedSrc src{base + 16u * lu, TB};
+            const SharedSrc src{base + 16 * lu, TB};
             typename Unit<T, U>::Raw o;
             if constexpr (MODE == kTreeAllReduce) o = tree_fold<T, OP, U, S>(src, s_prog[cur.t], R);
             else o = ring_fold<T, OP, U>(src, R, cur.j);
             for (int r = 0; r < R; ++r) Unit<T, U>::store(s_dst[r] + e0 * E, o);
+          } else if (MODE == kRingAllReduce && e0 + U <= cur.loopEnd &&
+                     e0 + U <= cur.hi + cur.q + (cur.j + 1 < cur.m ? 1 : 0)) {
+            // a unit cut by one ring block boundary inside a loop
+            const SharedSrc src{base + 16 * lu, TB};
+            const uint4 o = ring_fold_split<T, OP>(src, R, cur.j, (int)(cur.hi - e0));
+            for (int r = 0; r < R; ++r) st_global_v4(s_dst[r] + e0 * E, o);
           } else {
-            // a unit cut by a ring block boundary: element by element
+            // a unit cut by several ring block boundaries: element by element
             for (int x = 0; x < U; ++x) {
-              const SharedSrc src{base + 16u * lu + (uint32_t)(x * E), TB};
+              const SharedSrc src{base + 16 * lu + x * E, TB};
               const typename Ty<T>::Bits o =
                   fold_element<T, OP, MODE, S>(a, src, s_prog, e0 + x, cur);
               for (int r = 0; r < R; ++r) Unit<T, 1>::store(s_dst[r] + (e0 + x) * E, o);
