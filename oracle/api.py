@@ -28,8 +28,13 @@ def _widen(raws, dtype):
 
 
 def allreduce(raws, dtype, op, algo, n_channels, chunk_bytes, local_ranks=1,
-              counters=None):
-    """AllReduce of the R raw buffers.  Returns R raw output buffers."""
+              counters=None, hop_rounding=False):
+    """AllReduce of the R raw buffers.  Returns R raw output buffers.
+
+    hop_rounding (ring only): every rank keeps its partials in the element
+    type between hops, as a ring whose messages travel in that type does --
+    each reduction's fp32 result is rounded to the element type (RNE) before
+    it is sent on.  Without it partials stay in fp32 until the end."""
     R = len(raws)
     count = int(raws[0].size)
     E = numerics.ELEM_SIZE[dtype]
@@ -41,10 +46,15 @@ def allreduce(raws, dtype, op, algo, n_channels, chunk_bytes, local_ranks=1,
     xs = _widen(raws, dtype)
     out = [np.empty(count, dtype=np.float32) for _ in range(R)]
     chans = partition.channel_ranges(count, E, n_channels)
+    hop = None
+    if hop_rounding:
+        if algo != RING:
+            raise ValueError("per-hop rounding is defined for the ring")
+        hop = lambda x: numerics.to_f32(numerics.from_f32(x, dtype), dtype)  # noqa: E731
     if algo == RING:
         for (cs, cn) in chans:
             for loop in partition.ring_blocks(cs, cn, R, C):
-                res = schedules.ring_allreduce_loop(xs, loop, op, counters)
+                res = schedules.ring_allreduce_loop(xs, loop, op, counters, hop=hop)
                 for r in range(R):
                     for (bs, bn), blk in zip(loop, res[r]):
                         out[r][bs:bs + bn] = blk

@@ -49,11 +49,13 @@ class Counters:
 
 
 # ------------------------------------------------------------------ ring
-def ring_allreduce_loop(xs, blocks, op, counters=None, trace=None):
+def ring_allreduce_loop(xs, blocks, op, counters=None, trace=None, hop=None):
     """One ring loop over ``blocks`` (R (start, length) pairs, block j) of the
     R float32 buffers ``xs``.  Returns per rank the list of R result blocks.
     ``trace``, when a list, receives a snapshot of every rank's blocks after
-    each step, reduce-scatter steps first."""
+    each step, reduce-scatter steps first.  ``hop``, when given, maps every
+    partial a rank holds after a reduction to the value it can keep between
+    hops (per-hop rounding to a narrower element type)."""
     R = len(xs)
     held = [[xs[r][s:s + n].copy() for (s, n) in blocks] for r in range(R)]
 
@@ -66,6 +68,8 @@ def ring_allreduce_loop(xs, blocks, op, counters=None, trace=None):
         for r, j, msg in out:
             dst = (r + 1) % R
             held[dst][j] = numerics.combine(op, held[dst][j], msg)
+            if hop is not None:
+                held[dst][j] = hop(held[dst][j])
             if counters is not None:
                 counters.sent[r] += msg.size
         if counters is not None:

@@ -458,3 +458,44 @@ def test_workloads_are_seeded():
     assert all(bool((x.view(__import__("torch").int16) == y.view(__import__("torch").int16)).all())
                for x, y in zip(a, b))
     assert list(itertools.chain(*[t.tolist() for t in workloads.two_rank()])) == [1.0, 2.0, 3.0, 4.0]
+
+
+# ------------------------------------------------------- per-hop rounding
+def test_hop_rounding_bf16_by_hand():
+    # R=3, one element per block; block 0 folds ranks 0, 1, 2.  Values
+    # (1, 2**-8, 2**-8) at element 0.  In fp32: (1 + 2**-8) + 2**-8 = 1 + 2**-7,
+    # exactly a bf16 value.  Rounded at each hop: 1 + 2**-8 lies halfway between
+    # the bf16 neighbours 1 and 1 + 2**-7 and rounds to even, 1; again 1.
+    x = [np.array([1.0, 0.0, 0.0], np.float32), np.array([2.0 ** -8, 0.0, 0.0], np.float32),
+         np.array([2.0 ** -8, 0.0, 0.0], np.float32)]
+    raws = [numerics.f32_to_bf16_bits(v) for v in x]
+    fused = oracle.allreduce(raws, BF16, SUM, RING, 1, 16)
+    hop = oracle.allreduce(raws, BF16, SUM, RING, 1, 16, hop_rounding=True)
+    assert numerics.bf16_bits_to_f32(fused[0])[0] == 1.0 + 2.0 ** -7
+    assert numerics.bf16_bits_to_f32(hop[0])[0] == 1.0
+
+
+def test_hop_rounding_is_identity_for_fp32_and_max():
+    rng = np.random.default_rng(21)
+    for R in (2, 5, 8):
+        f = [rng.standard_normal(777).astype(np.float32) for _ in range(R)]
+        a = oracle.allreduce(f, F32, SUM, RING, 3, 48)
+        b = oracle.allreduce(f, F32, SUM, RING, 3, 48, hop_rounding=True)
+        assert all(np.array_equal(x.view(np.uint32), y.view(np.uint32)) for x, y in zip(a, b))
+        h = [numerics.f32_to_f16_bits(v) for v in f]
+        a = oracle.allreduce(h, F16, MAX, RING, 3, 48)
+        b = oracle.allreduce(h, F16, MAX, RING, 3, 48, hop_rounding=True)
+        assert all(np.array_equal(x, y) for x, y in zip(a, b))
+
+
+def test_hop_rounding_small_integers_exact():
+    # integers in [-8, 8] over up to 8 ranks stay exact in bf16 and fp16
+    rng = np.random.default_rng(22)
+    for dtype in (F16, BF16):
+        for R in (2, 3, 8):
+            f = [rng.integers(-8, 9, 300).astype(np.float32) for _ in range(R)]
+            raws = [numerics.from_f32(v, dtype) for v in f]
+            out = oracle.allreduce(raws, dtype, SUM, RING, 2, 32, hop_rounding=True)
+            s = oracle.fp64_sum(raws, dtype)
+            for o in out:
+                assert np.array_equal(numerics.to_f32(o, dtype).astype(np.float64), s)
