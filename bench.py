@@ -342,6 +342,34 @@ def other_workloads(vr, torch, workloads, dev, stream):
             ms = time_calls(torch, stream, call, sets, 200)
             out["%s_tree_%dch" % (name, nch)] = entry(ms, nbytes, count * 2, R)
         del bufs
+    # non-fused variants on the bench workload and the tree workload
+    W = WORKLOAD
+    R8, n8 = W["R"], W["count"]
+    g8 = torch.Generator(device=dev)
+    g8.manual_seed(W["seed"])
+    s8 = [torch.randn(n8, generator=g8, device=dev) for _ in range(R8)]
+    d8 = [torch.empty_like(x) for x in s8]
+    fifo = torch.empty(vr.vr_ring_stepwise_scratch_bytes(n8, 0), dtype=torch.uint8, device=dev)
+
+    def call_step(i, st):
+        vr.vr_allreduce_ring_stepwise(s8, d8, R8, n8, 0, 0, W["n_channels"], W["chunk_bytes"],
+                                      fifo, fifo.numel(), st)
+    ms = time_calls(torch, stream, call_step, 1, 5)
+    out["ring_64mib_fp32_stepwise"] = entry(ms, ar_bytes(R8, n8, 0), n8 * 4, R8)
+    out["ring_64mib_fp32_stepwise"]["launches_per_call"] = 1 + 4 * (R8 - 1)
+
+    def call_updown(i, st):
+        vr.vr_allreduce_tree_updown(s8, d8, R8, n8, 0, 0, W["n_channels"], W["chunk_bytes"], 1,
+                                    st)
+    ms = time_calls(torch, stream, call_updown, 1, 20)
+    out["tree_64mib_fp32_updown"] = entry(ms, ar_bytes(R8, n8, 0), n8 * 4, R8)
+
+    def call_tree(i, st):
+        vr.vr_allreduce(s8, d8, R8, n8, 0, 0, 1, W["n_channels"], W["chunk_bytes"], st)
+    ms = time_calls(torch, stream, call_tree, 1, 20)
+    out["tree_64mib_fp32_fused"] = entry(ms, ar_bytes(R8, n8, 0), n8 * 4, R8)
+    del s8, d8, fifo
+
     # hierarchical 8 x 8, fp16, 16 MiB per rank
     w = workloads.WORKLOADS["hier_16mib"]
     R, count, L = w["R"], w["count"], w["local_ranks"]

@@ -47,6 +47,9 @@ _SIGNATURES = {
     "vr_allreduce_ex": (I, [PP, PP, I, S, I, I, I, I, S, I, VP]),
     "vr_reduce_scatter": (I, [PP, PP, I, S, I, I, I, I, S, VP]),
     "vr_allgather": (I, [PP, PP, I, S, I, I, I, S, VP]),
+    "vr_allreduce_tree_updown": (I, [PP, PP, I, S, I, I, I, S, I, VP]),
+    "vr_ring_stepwise_scratch_bytes": (S, [S, I]),
+    "vr_allreduce_ring_stepwise": (I, [PP, PP, I, S, I, I, I, S, VP, S, VP]),
     "vr_stream_status": (I, [VP]),
     "vr_launch_count": (ctypes.c_ulonglong, []),
     "vr_debug_stall_next": (I, [ctypes.c_longlong]),
@@ -165,6 +168,24 @@ def vr_allgather(sendbufs, recvbufs, R, sendcount, dtype, algo, nChannels, chunk
                  stream=None):
     _check(_L().vr_allgather(_ptrs(sendbufs), _ptrs(recvbufs), R, sendcount, dtype, algo,
                              nChannels, chunkBytes, _stream(stream)), "vr_allgather")
+
+
+def vr_allreduce_tree_updown(sendbufs, recvbufs, R, count, dtype, op, nChannels, chunkBytes,
+                             localRanks, stream=None):
+    _check(_L().vr_allreduce_tree_updown(_ptrs(sendbufs), _ptrs(recvbufs), R, count, dtype, op,
+                                         nChannels, chunkBytes, localRanks, _stream(stream)),
+           "vr_allreduce_tree_updown")
+
+
+def vr_ring_stepwise_scratch_bytes(count, dtype):
+    return _L().vr_ring_stepwise_scratch_bytes(count, dtype)
+
+
+def vr_allreduce_ring_stepwise(sendbufs, recvbufs, R, count, dtype, op, nChannels, chunkBytes,
+                               scratch, scratchBytes, stream=None):
+    _check(_L().vr_allreduce_ring_stepwise(_ptrs(sendbufs), _ptrs(recvbufs), R, count, dtype, op,
+                                           nChannels, chunkBytes, _ptr(scratch), scratchBytes,
+                                           _stream(stream)), "vr_allreduce_ring_stepwise")
 
 
 def vr_stream_status(stream=None):

@@ -123,12 +123,16 @@ bool overlap(uintptr_t a, size_t an, uintptr_t b, size_t bn) {
 // disjoint or in the collective's in-place position: recv == send + recvAt
 // (AllReduce: 0, ReduceScatter: r * recvBytes) or send == recv + sendAt
 // (AllGather: r * sendBytes).
+// Every buffer must also be aligned to the element size E: the element
+// path accesses whole elements.
 enum Kind { kAR, kRS, kAG };
 vr_result_t check_buffers(const void* const* send, void* const* recv, int R, size_t sendBytes,
-                          size_t recvBytes, Kind kind) {
+                          size_t recvBytes, Kind kind, size_t E) {
   if (!send || !recv) return VR_ERR_INVALID_ARGUMENT;
-  for (int r = 0; r < R; ++r)
+  for (int r = 0; r < R; ++r) {
     if ((sendBytes && !send[r]) || (recvBytes && !recv[r])) return VR_ERR_INVALID_ARGUMENT;
+    if (((uintptr_t)send[r] | (uintptr_t)recv[r]) % E) return VR_ERR_INVALID_ARGUMENT;
+  }
   for (int r = 0; r < R; ++r) {
     const uintptr_t s = (uintptr_t)send[r], d = (uintptr_t)recv[r];
     bool inPlace = false;
@@ -190,7 +194,8 @@ const void* pick_kernel(int dtype, int mode, int op, bool vec, int stack = 0) {
   }
 }
 
-vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream) {
+vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream,
+                   void** extra = nullptr, int nExtra = 0) {
   if (!fn) return VR_ERR_INTERNAL;
   DeviceInfo di;
   int device = 0;
@@ -203,7 +208,8 @@ vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream) {
   const long long resident = (long long)di.sms * blocks_per_sm(fn, device);
   const long long wanted = (units + kBlockThreads - 1) / kBlockThreads;
   const int grid = (int)std::max(1LL, std::min(resident, wanted));
-  void* args[] = {&a};
+  void* args[4] = {&a, nullptr, nullptr, nullptr};
+  for (int i = 0; i < nExtra && i < 3; ++i) args[1 + i] = extra[i];
   if (cudaLaunchKernel(fn, dim3(grid), dim3(kBlockThreads), args, 0, (cudaStream_t)stream) !=
       cudaSuccess)
     return VR_ERR_CUDA;
@@ -366,7 +372,7 @@ vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, 
       (algo != VR_ALGO_RING && algo != VR_ALGO_TREE) || localRanks < 1 || R % localRanks)
     return VR_ERR_INVALID_ARGUMENT;
   const size_t E = elem_size(dtype);
-  vr_result_t e = check_buffers(sendbufs, recvbufs, R, count * E, count * E, kAR);
+  vr_result_t e = check_buffers(sendbufs, recvbufs, R, count * E, count * E, kAR, E);
   if (e != VR_SUCCESS || count == 0) return e;
   KArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -411,7 +417,7 @@ vr_result_t vr_reduce_scatter(const void* const* sendbufs, void* const* recvbufs
     return VR_ERR_INVALID_ARGUMENT;
   if (algo == VR_ALGO_TREE) return VR_ERR_UNSUPPORTED;
   const size_t E = elem_size(dtype);
-  vr_result_t e = check_buffers(sendbufs, recvbufs, R, (size_t)R * recvcount * E, recvcount * E, kRS);
+  vr_result_t e = check_buffers(sendbufs, recvbufs, R, (size_t)R * recvcount * E, recvcount * E, kRS, E);
   if (e != VR_SUCCESS || recvcount == 0) return e;
   KArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -440,7 +446,8 @@ vr_result_t vr_allgather(const void* const* sendbufs, void* const* recvbufs, int
     return VR_ERR_INVALID_ARGUMENT;
   if (algo == VR_ALGO_TREE) return VR_ERR_UNSUPPORTED;
   const size_t bytes = sendcount * elem_size(dtype);
-  vr_result_t e = check_buffers(sendbufs, recvbufs, R, bytes, (size_t)R * bytes, kAG);
+  vr_result_t e = check_buffers(sendbufs, recvbufs, R, bytes, (size_t)R * bytes, kAG,
+                                elem_size(dtype));
   if (e != VR_SUCCESS || sendcount == 0) return e;
   KArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -452,6 +459,85 @@ vr_result_t vr_allgather(const void* const* sendbufs, void* const* recvbufs, int
   const long long NB = vec ? kGrainBytes : 1;
   const long long units = (long long)R * (((long long)bytes + NB - 1) / NB);
   return launch(kernel_ptr_allgather(vec), a, units, stream);
+}
+
+size_t vr_ring_stepwise_scratch_bytes(size_t count, vr_dtype_t dtype) {
+  const size_t E = elem_size(dtype);
+  return E ? (count * E + 15) / 16 * 16 : 0;
+}
+
+vr_result_t vr_allreduce_ring_stepwise(const void* const* sendbufs, void* const* recvbufs, int R,
+                                       size_t count, vr_dtype_t dtype, vr_op_t op,
+                                       int nChannels, size_t chunkBytes, void* scratch,
+                                       size_t scratchBytes, void* stream) {
+  if (!valid_common(R, dtype, nChannels, chunkBytes) || (op != VR_SUM && op != VR_MAX))
+    return VR_ERR_INVALID_ARGUMENT;
+  const size_t E = elem_size(dtype);
+  vr_result_t e = check_buffers(sendbufs, recvbufs, R, count * E, count * E, kAR, E);
+  if (e != VR_SUCCESS || count == 0) return e;
+  const size_t need = vr_ring_stepwise_scratch_bytes(count, dtype);
+  if (!scratch || scratchBytes < need || (uintptr_t)scratch % E) return VR_ERR_INVALID_ARGUMENT;
+  for (int r = 0; r < R; ++r)
+    if (overlap((uintptr_t)scratch, need, (uintptr_t)sendbufs[r], count * E) ||
+        overlap((uintptr_t)scratch, need, (uintptr_t)recvbufs[r], count * E))
+      return VR_ERR_INVALID_ARGUMENT;
+  KArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.R = R;
+  for (int r = 0; r < R; ++r) { a.src[r] = sendbufs[r]; a.dst[r] = recvbufs[r]; }
+  a.scratch = scratch;
+  const bool vec = aligned16(sendbufs, R, 0) && aligned16(recvbufs, R, 0) &&
+                   (((uintptr_t)scratch & 15) == 0);
+  // working copies: recv = send
+  a.count = (long long)(count * E);
+  const long long NB = vec ? 16 : 1;
+  if ((e = launch(ablation_kernel_ptr(kCopyRanks, dtype, op, vec, 0), a,
+                  (long long)R * ((a.count + NB - 1) / NB), stream)) != VR_SUCCESS)
+    return e;
+  fill_partition(a, count, E, nChannels, chunkBytes);
+  const void* step = ablation_kernel_ptr(kRingStep, dtype, op, vec, 0);
+  const long long NV = vec ? kGrainBytes / (long long)E : 1;
+  const long long units = ((long long)count + NV - 1) / NV;
+  for (int half = 0; half < 2; ++half) {
+    int gather = half;
+    for (int s = 0; s < R - 1; ++s) {
+      int phase = kStepSend;
+      void* extra[3] = {&phase, &s, &gather};
+      if ((e = launch(step, a, units, stream, extra, 3)) != VR_SUCCESS) return e;
+      phase = half ? kStepCopy : kStepReduce;
+      if ((e = launch(step, a, units, stream, extra, 3)) != VR_SUCCESS) return e;
+    }
+  }
+  return VR_SUCCESS;
+}
+
+vr_result_t vr_allreduce_tree_updown(const void* const* sendbufs, void* const* recvbufs, int R,
+                                     size_t count, vr_dtype_t dtype, vr_op_t op, int nChannels,
+                                     size_t chunkBytes, int localRanks, void* stream) {
+  if (!valid_common(R, dtype, nChannels, chunkBytes) || (op != VR_SUM && op != VR_MAX) ||
+      localRanks < 1 || R % localRanks)
+    return VR_ERR_INVALID_ARGUMENT;
+  const size_t E = elem_size(dtype);
+  vr_result_t e = check_buffers(sendbufs, recvbufs, R, count * E, count * E, kAR, E);
+  if (e != VR_SUCCESS || count == 0) return e;
+  KArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.R = R;
+  for (int r = 0; r < R; ++r) { a.src[r] = sendbufs[r]; a.dst[r] = recvbufs[r]; }
+  fill_partition(a, count, E, nChannels, chunkBytes);
+  std::array<FoldProg, 2> p;
+  if ((e = tree_programs(R / localRanks, localRanks, &p)) != VR_SUCCESS) return e;
+  a.prog[0] = p[0];
+  a.prog[1] = p[1];
+  a.treeSplit = (nChannels + 1) / 2;
+  const int stack = std::max(p[0].depth, p[1].depth);
+  const bool vec = aligned16(sendbufs, R, 0) && aligned16(recvbufs, R, 0);
+  const long long NV = vec ? kGrainBytes / (long long)E : 1;
+  const long long units = ((long long)count + NV - 1) / NV;
+  if ((e = launch(ablation_kernel_ptr(kTreeUp, dtype, op, vec, stack), a, units, stream)) !=
+      VR_SUCCESS)
+    return e;
+  return launch(ablation_kernel_ptr(kTreeDown, dtype, op, vec, stack), a, units, stream);
 }
 
 vr_result_t vr_stream_status(void* stream) {

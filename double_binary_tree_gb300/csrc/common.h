@@ -26,10 +26,13 @@ struct alignas(4) FoldProg {
   uint8_t n;      // == R
   uint8_t tail;
   uint8_t depth;  // deepest partial stack the stream needs
-  uint8_t pad;
+  uint8_t root;   // the tree's root rank
 };
 
 enum Mode : int { kRingAllReduce = 0, kTreeAllReduce = 1, kReduceScatter = 2, kAllGather = 3 };
+
+// Phases of one step of the stepwise ring (ablation.cuh).
+enum StepPhase : int { kStepSend = 0, kStepReduce = 1, kStepCopy = 2 };
 
 // Everything a collective kernel needs, passed by value as the kernel
 // parameter (about 1.2 KB).
@@ -46,6 +49,7 @@ struct KArgs {
   int treeSplit;        // channels [0, treeSplit) follow prog[0], the rest prog[1]
   int pad;
   unsigned* status;     // this device's status word
+  void* scratch;        // stepwise ring: the message FIFO (count elements)
   // TMA-staged kernels (staged.cuh)
   long long unitsAll;   // 16-byte units of the message, a trailing partial one included
   long long unitsFull;  // full 16-byte units (ReduceScatter: per block)

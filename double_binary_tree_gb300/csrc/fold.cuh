@@ -202,14 +202,13 @@ template <typename T, int NV> struct Lanes<T, VR_MAX, NV, false> {
 };
 
 // ------------------------------------------------------------------ folds
-// Ranks j, j+1, ..., j+R-1 (mod R), left to right.
+// Ranks j, j+1, ..., j+R-1 (mod R), left to right.  The first batch is
+// peeled so that no step has to ask whether it is the first.
 template <typename T, int OP, int NV, class Src>
 __device__ __forceinline__ typename Unit<T, NV>::Raw ring_fold(const Src& src, int R, int j) {
   typedef Unit<T, NV> Un;
   typedef Lanes<T, OP, NV> Ln;
   typename Ln::L acc[Ln::N];
-#pragma unroll
-  for (int e = 0; e < Ln::N; ++e) acc[e] = 0;
   for (int k0 = 0; k0 < R; k0 += kBatch) {
     typename Un::Raw v[kBatch];
 #pragma unroll
@@ -221,14 +220,19 @@ __device__ __forceinline__ typename Unit<T, NV>::Raw ring_fold(const Src& src, i
         v[i] = load_unit<T, NV>(src, r);
       }
     }
+    int i0 = 0;
+    if (k0 == 0) {
+      Ln::decode(v[0], acc);
+      i0 = 1;
+    }
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const int k = k0 + i;
-      if (k < R) {
+      if (i >= i0 && k < R) {
         typename Ln::L x[Ln::N];
         Ln::decode(v[i], x);
 #pragma unroll
-        for (int e = 0; e < Ln::N; ++e) acc[e] = k == 0 ? x[e] : Ln::op(acc[e], x[e]);
+        for (int e = 0; e < Ln::N; ++e) acc[e] = Ln::op(acc[e], x[e]);
       }
     }
   }
@@ -467,11 +471,19 @@ __device__ __forceinline__ void seek(const KArgs& a, long long e, Cursor& c) {
   locate<U, MODE>(a, e, c);
 }
 
+// The rare paths (a unit cut by a block boundary, single elements) are
+// called out of line so that their registers do not count against the
+// streaming loop's occupancy.
+template <typename T, int OP, class Src>
+__device__ __noinline__ uint4 ring_fold_split_rare(const Src src, int R, int j, int split) {
+  return ring_fold_split<T, OP>(src, R, j, split);
+}
+
 // One element of an AllReduce: its fold in the schedule of element e.
 template <typename T, int OP, int MODE, int S, class Src>
-__device__ __forceinline__ typename Ty<T>::Bits fold_element(const KArgs& a, const Src& src,
-                                                            const FoldProg* progs, long long e,
-                                                            Cursor& cur) {
+__device__ __noinline__ typename Ty<T>::Bits fold_element(const KArgs& a, const Src src,
+                                                         const FoldProg* progs, long long e,
+                                                         Cursor& cur) {
   seek<Ty<T>::U, MODE>(a, e, cur);
   if constexpr (MODE == kTreeAllReduce) return tree_fold<T, OP, 1, S>(src, progs[cur.t], a.R);
   else return ring_fold<T, OP, 1>(src, a.R, cur.j);

@@ -25,6 +25,10 @@ const void* staged_kernel_ptr_f32(int mode, int op, int stack);
 const void* staged_kernel_ptr_f16(int mode, int op, int stack);
 const void* staged_kernel_ptr_bf16(int mode, int op, int stack);
 
+// Non-fused variants (kernels_ablation.cu).
+enum AblationKernel : int { kTreeUp = 0, kTreeDown = 1, kRingStep = 2, kCopyRanks = 3 };
+const void* ablation_kernel_ptr(int which, int dtype, int op, bool vec, int stack);
+
 // The current device's status word: its address, and read-and-clear.
 cudaError_t status_word_address(unsigned** p);
 cudaError_t read_and_clear_status(unsigned* value);

@@ -17,6 +17,10 @@
 namespace vr {
 
 constexpr int kBlock = 256;  // threads per CTA of the register-path kernels
+// Resident CTAs per SM the register-path kernels are compiled for: the tree
+// fold keeps more partials live (up to 128 registers), the ring fold fewer.
+constexpr int kMinBlocksTree = 2;
+constexpr int kMinBlocksRing = 3;
 
 // Rank pointers (and tree programs) copied to shared memory: they are indexed
 // by a runtime rank.
@@ -38,7 +42,8 @@ __device__ __forceinline__ void stage_args(const KArgs& a, const char** s_src, c
 // AllReduce, ring or tree.  VEC: 16-byte units (aligned buffers), else one
 // element per unit.
 template <typename T, int OP, int MODE, bool VEC, int S>
-__global__ void __launch_bounds__(kBlock) allreduce_kernel(const __grid_constant__ KArgs a) {
+__global__ void __launch_bounds__(kBlock, MODE == kTreeAllReduce ? kMinBlocksTree : kMinBlocksRing)
+    allreduce_kernel(const __grid_constant__ KArgs a) {
   constexpr int U = Ty<T>::U;
   constexpr int NV = VEC ? U : 1;
   constexpr long long E = sizeof(T);
@@ -67,7 +72,7 @@ __global__ void __launch_bounds__(kBlock) allreduce_kernel(const __grid_constant
                e0 + NV <= cur.hi + cur.q + (cur.j + 1 < cur.m ? 1 : 0)) {
       // a unit cut by one ring block boundary inside a loop
       const GlobalSrc src{s_src, e0 * E};
-      const uint4 o = ring_fold_split<T, OP>(src, R, cur.j, (int)(cur.hi - e0));
+      const uint4 o = ring_fold_split_rare<T, OP>(src, R, cur.j, (int)(cur.hi - e0));
       for (int r = 0; r < R; ++r) st_global_v4(s_dst[r] + e0 * E, o);
     } else {
       // a unit cut by the end of the message or by several block boundaries
@@ -84,7 +89,8 @@ __global__ void __launch_bounds__(kBlock) allreduce_kernel(const __grid_constant
 // ReduceScatter: unit (b, p) folds block b at offset p over ranks b+1, ..., b
 // and stores it to rank b only.
 template <typename T, int OP, bool VEC>
-__global__ void __launch_bounds__(kBlock) reduce_scatter_kernel(const __grid_constant__ KArgs a) {
+__global__ void __launch_bounds__(kBlock, kMinBlocksRing)
+    reduce_scatter_kernel(const __grid_constant__ KArgs a) {
   constexpr int NV = VEC ? Ty<T>::U : 1;
   constexpr long long E = sizeof(T);
   __shared__ const char* s_src[kMaxRanks];

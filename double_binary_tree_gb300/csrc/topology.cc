@@ -158,6 +158,7 @@ vr_result_t compile_fold(const vr_tree_t* tr, int R, FoldProg* p) {
   e.emit(root, 0);
   if (!e.ok || e.slot != R || e.pendingPops > 15) return VR_ERR_INTERNAL;
   p->n = (uint8_t)R;
+  p->root = (uint8_t)root;
   p->tail = (uint8_t)e.pendingPops;
   p->depth = (uint8_t)e.maxSp;
   if (e.sp - e.pendingPops != 1 || e.maxSp > kMaxStack) return VR_ERR_INTERNAL;

@@ -138,9 +138,10 @@ vr_result_t vr_ring_block(size_t count, vr_dtype_t dtype, int R, int nChannels,
  * forces one of the two for testing and tuning; results are identical.
  * Unaligned buffers run element units on the register kernel.
  * Errors (nothing enqueued): VR_ERR_INVALID_ARGUMENT for R outside
- * [1, VR_MAX_RANKS], NULL arrays, a NULL buffer with count > 0, a bad enum,
- * bad nChannels or chunkBytes, or a recv buffer that overlaps another rank's
- * send or recv buffer or partly overlaps its own send buffer.
+ * [1, VR_MAX_RANKS], NULL arrays, a NULL buffer with count > 0, a buffer not
+ * aligned to the element size, a bad enum, bad nChannels or chunkBytes, or a
+ * recv buffer that overlaps another rank's send or recv buffer or partly
+ * overlaps its own send buffer.
  * count == 0 enqueues nothing.  R == 1 copies (or leaves in place). */
 vr_result_t vr_allreduce(const void* const* sendbufs, void* const* recvbufs, int R,
                          size_t count, vr_dtype_t dtype, vr_op_t op, vr_algo_t algo,
@@ -175,6 +176,44 @@ vr_result_t vr_reduce_scatter(const void* const* sendbufs, void* const* recvbufs
 vr_result_t vr_allgather(const void* const* sendbufs, void* const* recvbufs, int R,
                          size_t sendcount, vr_dtype_t dtype, vr_algo_t algo,
                          int nChannels, size_t chunkBytes, void* stream);
+
+/* ------------------------------------------------ non-fused variants
+ * Same results as the fused calls above, computed the way a schedule that
+ * moves messages between ranks does, to measure what fusion buys. */
+
+/* Two-phase tree AllReduce ([Course13] "当前环境命中哪个 device 实现":
+ * runTreeUpDown reduces the whole message up the tree before broadcasting it
+ * down; runTreeSplit overlaps the two).  First launch: every unit is folded
+ * over its channel's tree and stored to the tree root's receive buffer only;
+ * second launch: copied from there to every other rank.  Same arguments,
+ * errors and bits as vr_allreduce_ex with VR_ALGO_TREE; one more read and
+ * write of the message.  Two kernel launches. */
+vr_result_t vr_allreduce_tree_updown(const void* const* sendbufs, void* const* recvbufs, int R,
+                                     size_t count, vr_dtype_t dtype, vr_op_t op, int nChannels,
+                                     size_t chunkBytes, int localRanks, void* stream);
+
+/* Bytes of device scratch vr_allreduce_ring_stepwise needs: count elements
+ * of dtype, rounded up to 16 (0 for a bad dtype). */
+size_t vr_ring_stepwise_scratch_bytes(size_t count, vr_dtype_t dtype);
+
+/* Stepwise ring AllReduce ([Interview] "手撕代码"; [Internals] "Ring：带宽友好"):
+ * the ring's 2(R-1) steps run one after the other, each as two launches, and
+ * every message crosses device memory: each step first copies every rank's
+ * outgoing block (of every loop) into the caller's scratch FIFO, then folds
+ * the FIFO into the receiving rank's block (reduce-scatter half) or
+ * overwrites it (all-gather half).  recvbufs[r] is rank r's working copy
+ * (first set to sendbufs[r]) and keeps partials in the element type, so
+ * 16-bit partials are rounded (RNE) at every hop, as messages that travel in
+ * that type are; for fp32 and for Max the bits equal vr_allreduce's RING.
+ * `scratch` is caller-owned device memory of at least
+ * vr_ring_stepwise_scratch_bytes(count, dtype) bytes, aligned to the element
+ * size, that overlaps no buffer; its contents are overwritten.  Launches 1 + 4(R-1) kernels.
+ * Errors: those of vr_allreduce, plus VR_ERR_INVALID_ARGUMENT for a NULL,
+ * short, misaligned or overlapping scratch. */
+vr_result_t vr_allreduce_ring_stepwise(const void* const* sendbufs, void* const* recvbufs, int R,
+                                       size_t count, vr_dtype_t dtype, vr_op_t op,
+                                       int nChannels, size_t chunkBytes, void* scratch,
+                                       size_t scratchBytes, void* stream);
 
 /* ------------------------------------------------------------- status */
 

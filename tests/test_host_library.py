@@ -112,6 +112,12 @@ def test_argument_errors_are_synchronous():
     assert _err(ar, FAKE[:2], [FAKE_R[0], FAKE_R[0] + 8], 2, 4, F32, SUM, RING, 1, 16) == INV
     # a recv buffer overlaps another rank's send buffer
     assert _err(ar, FAKE[:2], [FAKE[1] + 4, FAKE_R[1]], 2, 4, F32, SUM, RING, 1, 16) == INV
+    # buffers must be aligned to the element size
+    assert _err(ar, [FAKE[0] + 2, FAKE[1]], FAKE_R[:2], 2, 4, F32, SUM, RING, 1, 16) == INV
+    assert _err(ar, FAKE[:2], [FAKE_R[0], FAKE_R[1] + 1], 2, 4, vr.VR_FLOAT16, SUM, RING, 1,
+                16) == INV
+    assert _err(vr.vr_allgather, FAKE[:2], [FAKE_R[0] + 2, FAKE_R[1]], 2, 4, F32, RING, 1,
+                16) == INV
     # partial overlap with the own send buffer (in place must be exact)
     assert _err(ar, FAKE[:2], [FAKE[0] + 4, FAKE_R[1]], 2, 4, F32, SUM, RING, 1, 16) == INV
     assert _err(vr.vr_allreduce_ex, FAKE[:8], FAKE_R[:8], 8, 16, F32, SUM, TREE, 1, 16, 3) == INV
@@ -178,3 +184,28 @@ def _stack_depth(tree):
         return d
 
     return need(root)
+
+
+def test_stepwise_ring_scratch_rules():
+    """Scratch validation happens before anything is launched."""
+    INV = vr.VR_ERR_INVALID_ARGUMENT
+    F32, F16 = vr.VR_FLOAT32, vr.VR_FLOAT16
+    assert vr.vr_ring_stepwise_scratch_bytes(1000, F32) == 4000
+    assert vr.vr_ring_stepwise_scratch_bytes(1001, F16) == 2016
+    assert vr.vr_ring_stepwise_scratch_bytes(5, 9) == 0
+    before = vr.vr_launch_count()
+    step = vr.vr_allreduce_ring_stepwise
+    # missing, short, or overlapping scratch
+    assert _err(step, FAKE[:4], FAKE_R[:4], 4, 16, F32, vr.VR_SUM, 1, 16, 0, 64) == INV
+    assert _err(step, FAKE[:4], FAKE_R[:4], 4, 16, F32, vr.VR_SUM, 1, 16, 0x9000000, 63) == INV
+    assert _err(step, FAKE[:4], FAKE_R[:4], 4, 16, F32, vr.VR_SUM, 1, 16, FAKE_R[2] + 8, 64) == INV
+    assert _err(step, FAKE[:4], FAKE_R[:4], 4, 16, F32, vr.VR_SUM, 1, 16, FAKE[3] - 8, 64) == INV
+    assert _err(step, FAKE[:4], FAKE_R[:4], 4, 16, F32, vr.VR_SUM, 1, 16, 0x9000002, 64) == INV
+    # the usual argument errors
+    assert _err(step, FAKE[:4], FAKE_R[:4], 4, 16, F32, 7, 1, 16, 0x9000000, 64) == INV
+    assert _err(vr.vr_allreduce_tree_updown, FAKE[:8], FAKE_R[:8], 8, 16, F32, vr.VR_SUM, 1, 16,
+                3) == INV
+    # count == 0: nothing to do, nothing launched
+    step(FAKE[:4], FAKE_R[:4], 4, 0, F32, vr.VR_SUM, 1, 16, 0, 0)
+    vr.vr_allreduce_tree_updown(FAKE[:4], FAKE_R[:4], 4, 0, F32, vr.VR_SUM, 1, 16, 1)
+    assert vr.vr_launch_count() == before
