@@ -80,9 +80,10 @@ __global__ void __launch_bounds__(kBlock) tree_down_kernel(const __grid_constant
     seek<U, kTreeAllReduce>(a, e0, cur);
     const int root = s_prog[cur.t].root;
     if (n == NV) {
-      const uint4 v = *reinterpret_cast<const uint4*>(s_dst[root] + e0 * E);
+      const typename Unit<T, NV>::Raw v =
+          *reinterpret_cast<const typename Unit<T, NV>::Raw*>(s_dst[root] + e0 * E);
       for (int r = 0; r < R; ++r)
-        if (r != root) st_global_v4(s_dst[r] + e0 * E, v);
+        if (r != root) Unit<T, NV>::store(s_dst[r] + e0 * E, v);
     } else {
       for (int i = 0; i < n; ++i) {
         const typename Ty<T>::Bits v =
@@ -135,10 +136,11 @@ __global__ void __launch_bounds__(kBlock)
       int from, to;
       step_ranks(R, routing, step, cur.j, from, to);
       char* m = fifo + e0 * E;
+      typedef typename Unit<T, NV>::Raw Raw;  // 16 bytes, or one element
       if (phase == kStepSend) {
-        st_global_v4(m, *reinterpret_cast<const uint4*>(s_dst[from] + e0 * E));
+        Unit<T, NV>::store(m, *reinterpret_cast<const Raw*>(s_dst[from] + e0 * E));
       } else if (phase == kStepCopy) {
-        st_global_v4(s_dst[to] + e0 * E, *reinterpret_cast<const uint4*>(m));
+        Unit<T, NV>::store(s_dst[to] + e0 * E, *reinterpret_cast<const Raw*>(m));
       } else {
         typename Ln::L x[Ln::N], y[Ln::N];
         Ln::decode(*reinterpret_cast<const typename Unit<T, NV>::Raw*>(s_dst[to] + e0 * E), x);

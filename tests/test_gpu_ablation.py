@@ -30,6 +30,17 @@ def _bits(t):
     return workloads.raw_numpy(t.cpu())
 
 
+def _status_ok():
+    st = vr.vr_stream_status()
+    if st != 0:
+        try:
+            torch.cuda.synchronize()
+            detail = "torch sees no CUDA error"
+        except Exception as ex:  # the CUDA error text, for the report
+            detail = repr(ex)[:300]
+        raise AssertionError("status %d (%s): %s" % (st, vr.vr_get_error_string(st), detail))
+
+
 def _check(got, want, what):
     for r, (g, w) in enumerate(zip(got, want)):
         assert np.array_equal(g, w), "%s: rank %d differs" % (what, r)
@@ -54,7 +65,7 @@ def test_tree_updown_matches_tree(dtype, op):
             src = [t.cuda() for t in inp]
         dst = src if inplace else [torch.empty_like(s) for s in src]
         vr.vr_allreduce_tree_updown(src, dst, R, count, dtype, op, nch, cb, L)
-        assert vr.vr_stream_status() == 0
+        _status_ok()
         _check([_bits(d) for d in dst], want, "updown R=%d" % R)
 
 
@@ -81,7 +92,7 @@ def test_ring_stepwise_matches_hop_rounding(dtype, op):
         sptr = scratch.data_ptr() + (vr.ELEM_SIZE[dtype] if shift else 0)  # element-aligned
         before = vr.vr_launch_count()
         vr.vr_allreduce_ring_stepwise(src, dst, R, count, dtype, op, nch, cb, sptr, nbytes)
-        assert vr.vr_stream_status() == 0
+        _status_ok()
         assert vr.vr_launch_count() - before == 1 + 4 * (R - 1)
         _check([_bits(d) for d in dst], want, "stepwise R=%d" % R)
         if dtype == F32 or op == MAX:
