@@ -60,6 +60,8 @@ def build(force=False, verbose=False, ptxas_info=False):
               "-I" + CSRC] + ARCH
     if ptxas_info:
         common += ["-Xptxas", "-v"]
+    # extra flags for tuning experiments (e.g. -DVR_MIN_BLOCKS_RING=2)
+    common += os.environ.get("VR_NVCC_FLAGS", "").split()
     procs, objs = [], []
     for src in SOURCES:
         obj = os.path.join(bdir, src + ".o")

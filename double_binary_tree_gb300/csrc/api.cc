@@ -233,7 +233,7 @@ bool use_staged(int mode, int R, size_t bytesPerRank) {
 unsigned staged_tile_bytes(int R) { return R > 8 && R <= 16 ? 4096u : 2048u; }
 
 // Staged geometry: tiles of tileUnits 16-byte units per rank; as many stages
-// (at most 16) as fit in the opt-in shared memory; up to 8 consumer warps.
+// (at most 16) as fit in the opt-in shared memory; up to 7 consumer warps.
 // a.unitsAll / a.unitsFull describe the message (AllReduce) or one block
 // (ReduceScatter); the tile count follows from the geometry.
 vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {

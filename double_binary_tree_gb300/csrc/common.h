@@ -12,7 +12,7 @@ constexpr int kMaxChannels = VR_MAX_CHANNELS;
 constexpr int kGrainBytes = 16;      // channel ranges are cut in 16-byte grains
 constexpr int kMaxStack = 8;         // partial sums a tree fold keeps live at once
 constexpr int kStagedMaxStages = 16; // shared-memory stages of a staged kernel
-constexpr int kStagedMaxConsumers = 8;  // its consumer warps (all of them fold every stage)
+constexpr int kStagedMaxConsumers = 7;  // its consumer warps (8 warps per CTA: 2 per SM sub-partition)
 constexpr int kStagedHeader = 2048;  // its barriers, flags, pointer tables and programs
 
 // A tree's reduction order as a stream of rank loads.  Slot i loads rank

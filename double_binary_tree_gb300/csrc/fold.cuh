@@ -471,22 +471,30 @@ __device__ __forceinline__ void seek(const KArgs& a, long long e, Cursor& c) {
   locate<U, MODE>(a, e, c);
 }
 
-// The rare paths (a unit cut by a block boundary, single elements) are
-// called out of line so that their registers do not count against the
-// streaming loop's occupancy.
+// One element of an AllReduce: its fold in the schedule of element e.
+template <typename T, int OP, int MODE, int S, class Src>
+__device__ __forceinline__ typename Ty<T>::Bits fold_element(const KArgs& a, const Src& src,
+                                                            const FoldProg* progs, long long e,
+                                                            Cursor& cur) {
+  seek<Ty<T>::U, MODE>(a, e, cur);
+  if constexpr (MODE == kTreeAllReduce) return tree_fold<T, OP, 1, S>(src, progs[cur.t], a.R);
+  else return ring_fold<T, OP, 1>(src, a.R, cur.j);
+}
+
+// Out-of-line copies of the rare paths (a unit cut by a block boundary,
+// single elements) for the register-path kernels, whose occupancy depends on
+// the streaming loop's registers.  The cursor is taken by value: a reference
+// would pin the caller's cursor to local memory for its whole loop.  The
+// shared-memory-staged kernels, which run one CTA per SM, inline them.
 template <typename T, int OP, class Src>
 __device__ __noinline__ uint4 ring_fold_split_rare(const Src src, int R, int j, int split) {
   return ring_fold_split<T, OP>(src, R, j, split);
 }
-
-// One element of an AllReduce: its fold in the schedule of element e.
 template <typename T, int OP, int MODE, int S, class Src>
-__device__ __noinline__ typename Ty<T>::Bits fold_element(const KArgs& a, const Src src,
-                                                         const FoldProg* progs, long long e,
-                                                         Cursor& cur) {
-  seek<Ty<T>::U, MODE>(a, e, cur);
-  if constexpr (MODE == kTreeAllReduce) return tree_fold<T, OP, 1, S>(src, progs[cur.t], a.R);
-  else return ring_fold<T, OP, 1>(src, a.R, cur.j);
+__device__ __noinline__ typename Ty<T>::Bits fold_element_rare(const KArgs& a, const Src src,
+                                                              const FoldProg* progs, long long e,
+                                                              Cursor cur) {
+  return fold_element<T, OP, MODE, S>(a, src, progs, e, cur);
 }
 
 }  // namespace vr

@@ -17,10 +17,14 @@
 namespace vr {
 
 constexpr int kBlock = 256;  // threads per CTA of the register-path kernels
-// Resident CTAs per SM the register-path kernels are compiled for: the tree
-// fold keeps more partials live (up to 128 registers), the ring fold fewer.
+// Resident CTAs per SM the register-path kernels are compiled for (up to
+// 128 registers each): measured faster than 3 CTAs at up to 85 registers,
+// which made the ring kernels spill.
+#ifndef VR_MIN_BLOCKS_RING
+#define VR_MIN_BLOCKS_RING 2
+#endif
 constexpr int kMinBlocksTree = 2;
-constexpr int kMinBlocksRing = 3;
+constexpr int kMinBlocksRing = VR_MIN_BLOCKS_RING;
 
 // Rank pointers (and tree programs) copied to shared memory: they are indexed
 // by a runtime rank.
@@ -79,7 +83,7 @@ __global__ void __launch_bounds__(kBlock, MODE == kTreeAllReduce ? kMinBlocksTre
       for (int i = 0; i < n; ++i) {
         const long long e = e0 + i;
         const GlobalSrc src{s_src, e * E};
-        const typename Ty<T>::Bits o = fold_element<T, OP, MODE, S>(a, src, s_prog, e, cur);
+        const typename Ty<T>::Bits o = fold_element_rare<T, OP, MODE, S>(a, src, s_prog, e, cur);
         for (int r = 0; r < R; ++r) Unit<T, 1>::store(s_dst[r] + e * E, o);
       }
     }

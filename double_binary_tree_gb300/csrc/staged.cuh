@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
                      e0 + U <= cur.hi + cur.q + (cur.j + 1 < cur.m ? 1 : 0)) {
             // a unit cut by one ring block boundary inside a loop
             const SharedSrc src{base + 16 * lu, TB};
-            const uint4 o = ring_fold_split_rare<T, OP>(src, R, cur.j, (int)(cur.hi - e0));
+            const uint4 o = ring_fold_split<T, OP>(src, R, cur.j, (int)(cur.hi - e0));
             for (int r = 0; r < R; ++r) st_global_v4(s_dst[r] + e0 * E, o);
           } else {
             // a unit cut by several ring block boundaries: element by element
