@@ -23,6 +23,7 @@ VR_SUM, VR_MAX = 0, 1
 VR_ALGO_RING, VR_ALGO_TREE = 0, 1
 VR_MAX_RANKS = 64
 VR_MAX_CHANNELS = 64
+VR_NOALLOC_SCRATCH_BYTES = 8 << 20
 ELEM_SIZE = {VR_FLOAT32: 4, VR_FLOAT16: 2, VR_BFLOAT16: 2}
 
 
@@ -50,6 +51,7 @@ _SIGNATURES = {
     "vr_allreduce_tree_updown": (I, [PP, PP, I, S, I, I, I, S, I, VP]),
     "vr_ring_stepwise_scratch_bytes": (S, [S, I]),
     "vr_allreduce_ring_stepwise": (I, [PP, PP, I, S, I, I, I, S, VP, S, VP]),
+    "vr_allreduce_ring_stepwise_noalloc": (I, [PP, PP, I, S, I, I, I, S, VP]),
     "vr_stream_status": (I, [VP]),
     "vr_launch_count": (ctypes.c_ulonglong, []),
     "vr_debug_stall_next": (I, [ctypes.c_longlong]),
@@ -186,6 +188,16 @@ def vr_allreduce_ring_stepwise(sendbufs, recvbufs, R, count, dtype, op, nChannel
     _check(_L().vr_allreduce_ring_stepwise(_ptrs(sendbufs), _ptrs(recvbufs), R, count, dtype, op,
                                            nChannels, chunkBytes, _ptr(scratch), scratchBytes,
                                            _stream(stream)), "vr_allreduce_ring_stepwise")
+
+
+def vr_allreduce_ring_stepwise_noalloc(sendbufs, recvbufs, R, count, dtype, op, nChannels,
+                                       chunkBytes, stream=None):
+    """vr_allreduce_ring_stepwise without caller scratch: for callers that
+    cannot allocate device memory (see include/vr.h)."""
+    _check(_L().vr_allreduce_ring_stepwise_noalloc(_ptrs(sendbufs), _ptrs(recvbufs), R, count,
+                                                   dtype, op, nChannels, chunkBytes,
+                                                   _stream(stream)),
+           "vr_allreduce_ring_stepwise_noalloc")
 
 
 def vr_stream_status(stream=None):

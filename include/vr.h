@@ -215,6 +215,35 @@ vr_result_t vr_allreduce_ring_stepwise(const void* const* sendbufs, void* const*
                                        int nChannels, size_t chunkBytes, void* scratch,
                                        size_t scratchBytes, void* stream);
 
+/* Size of the device array that vr_allreduce_ring_stepwise_noalloc uses as
+ * its message FIFO: 8 MiB per GPU that loads the library. */
+#define VR_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* vr_allreduce_ring_stepwise for callers that cannot allocate device memory
+ * (no counterpart in the pages: it exists for the callers, not the method).
+ * A runtime that has given all of the GPU's memory to its own allocator, or
+ * code on a latency-critical path that may not call cudaMalloc / cudaFree
+ * (both can synchronise the device), cannot supply the scratch FIFO; this
+ * entry point uses a file-scope device array of VR_NOALLOC_SCRATCH_BYTES
+ * bytes instead, which every GPU that loads the library holds until the
+ * process exits.  It allocates nothing, and calls neither cudaMalloc nor
+ * cudaFree nor any allocating library routine.
+ * Arguments, results and errors are those of vr_allreduce_ring_stepwise
+ * without scratch/scratchBytes, plus VR_ERR_UNSUPPORTED when count elements
+ * of dtype exceed VR_NOALLOC_SCRATCH_BYTES (2 Mi fp32 or 4 Mi 16-bit
+ * elements per rank at most).
+ * Set-up: the first call on a device looks up the array's device address on
+ * that device (the device current at the call); make that first call before
+ * any stream capture.
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's contents; nothing in it needs to start at zero (each step writes
+ * every message before it is read).  Calls whose executions overlap on the
+ * GPU (different streams, or different host threads) race on the array:
+ * order them. */
+vr_result_t vr_allreduce_ring_stepwise_noalloc(const void* const* sendbufs, void* const* recvbufs,
+                                               int R, size_t count, vr_dtype_t dtype, vr_op_t op,
+                                               int nChannels, size_t chunkBytes, void* stream);
+
 /* ------------------------------------------------------------- status */
 
 /* Synchronises `stream`, then returns and clears the current device's status
