@@ -19,9 +19,11 @@ Readings where the pages are silent:
   the first -1 slot of ``down[]`` (nothing when the child is -1) and fails past
   three slots.  Supported by the log "Tree 0 : -1 -> 0 -> 1/-1/-1" (a root's
   only child sits in slot 0) and by leaf detection through ``down[0] == -1``.
-* With no topology search, the intra-node order ``treeIntra`` is the identity:
-  local rank l of node k is global rank k*L + l, and the head of node k (pattern
-  TREE: parent, child0 and child1 heads are all treeIntra[0]) is k*L.
+* With no topology search, the intra-node order ``treeIntra`` is the identity
+  (local rank l of node k is global rank k*L + l) unless the caller gives one
+  per channel.  The head pattern picks the parent and child heads from that
+  order as section "节点内先形成链" shows: TREE uses position 0 for all three,
+  SPLIT_TREE 0 / 1 / 1, and any other pattern (BALANCED_TREE) 0 / 1 / 0.
 * The ring has no physical search either: every channel uses the identity ring.
 * Channel -> tree: the channel metadata is duplicated so that one copy joins
   tree 0 and the other tree 1, each carrying half the data.  Channels
@@ -133,38 +135,70 @@ def channel_tree_index(channel, n_channels):
     return 0 if channel < (n_channels + 1) // 2 else 1
 
 
-def build_dtree(n_nodes, local_ranks, n_channels):
+PATTERNS = ("tree", "split_tree", "balanced_tree")
+
+
+def head_indices(pattern):
+    """Positions in a node's intra order of the rank that joins the parent
+    node, the rank that takes child d0 and the rank that takes child d1:
+    TREE (0, 0, 0), SPLIT_TREE (0, 1, 1), BALANCED_TREE (0, 1, 0)."""
+    if pattern == "tree":
+        return 0, 0, 0
+    if pattern == "split_tree":
+        return 0, 1, 1
+    if pattern == "balanced_tree":
+        return 0, 1, 0
+    raise ValueError("unknown pattern %r" % (pattern,))
+
+
+def build_dtree(n_nodes, local_ranks, n_channels, pattern="tree", orders=None):
     """Per channel and rank, the hierarchical double-binary-tree record.
 
-    Step 1 (preset): each node's ranks form a chain in local order, up = the
-    previous local rank, down[0] = the next one.  Step 2 (connect): the
-    node-level double tree over node indices (not rank indices) is attached
-    to the heads: the head of node k gets up = head of its parent node and
-    appends the heads of its child nodes d0 then d1 to down[].  Every rank's
-    depth is L - 1 + floor(log2 nNodes), the page's approximation.
+    Step 1 (preset): on channel c each node's ranks form a chain in the
+    channel's intra order (``orders[c]``, a permutation of the local ranks;
+    identity when None): up = the previous rank of the order, down[0] = the
+    next one.  The pattern picks which positions of the order are the node's
+    parent head and its two child heads.  Step 2 (connect): the node-level
+    double tree over node indices (not rank indices) is attached: the parent
+    head of node k takes up = the child head (child0 or child1 by k's
+    parentChildType) of its parent node; the child0 head appends the parent
+    head of child node d0, then the child1 head appends that of d1.  Every
+    rank's depth is L - 1 + floor(log2 nNodes), the page's approximation.
 
     Returns trees[channel][rank] -> Tree."""
     if n_nodes < 1 or local_ranks < 1 or n_channels < 1:
         raise ValueError("sizes must be >= 1")
     L = local_ranks
     R = n_nodes * L
+    pi, c0i, c1i = head_indices(pattern)
+    if max(pi, c0i, c1i) >= L:
+        raise ValueError("pattern needs more local ranks")
     depth = L - 1 + log2i(n_nodes)
     node_trees = [dtree(n_nodes, k) for k in range(n_nodes)]
     out = []
     for c in range(n_channels):
         t_idx = channel_tree_index(c, n_channels)
-        per_rank = []
-        for rank in range(R):
-            k, l = divmod(rank, L)
-            t = Tree(depth=depth,
-                     up=-1 if l == 0 else rank - 1,
-                     down=[-1 if l == L - 1 else rank + 1, -1, -1])
-            if l == 0:
-                u, d0, d1, _ = node_trees[k][t_idx]
-                _set_up(t, -1 if u == -1 else u * L)
-                _set_down(t, -1 if d0 == -1 else d0 * L)
-                _set_down(t, -1 if d1 == -1 else d1 * L)
-            per_rank.append(t)
+        order = list(range(L)) if orders is None else list(orders[c])
+        if sorted(order) != list(range(L)):
+            raise ValueError("intra order must be a permutation of the local ranks")
+        intra = [[k * L + order[i] for i in range(L)] for k in range(n_nodes)]
+        per_rank = [None] * R
+        for k in range(n_nodes):
+            for i, rank in enumerate(intra[k]):
+                per_rank[rank] = Tree(depth=depth,
+                                      up=-1 if i == 0 else intra[k][i - 1],
+                                      down=[-1 if i == L - 1 else intra[k][i + 1], -1, -1])
+        ttp = [intra[k][pi] for k in range(n_nodes)]
+        ttc0 = [intra[k][c0i] for k in range(n_nodes)]
+        ttc1 = [intra[k][c1i] for k in range(n_nodes)]
+        for k in range(n_nodes):
+            u, d0, d1, ptype = node_trees[k][t_idx]
+            if u != -1:
+                _set_up(per_rank[ttp[k]], (ttc0 if ptype == 0 else ttc1)[u])
+            if d0 != -1:
+                _set_down(per_rank[ttc0[k]], ttp[d0])
+            if d1 != -1:
+                _set_down(per_rank[ttc1[k]], ttp[d1])
         out.append(per_rank)
     return out
 

@@ -499,3 +499,69 @@ def test_hop_rounding_small_integers_exact():
             s = oracle.fp64_sum(raws, dtype)
             for o in out:
                 assert np.array_equal(numerics.to_f32(o, dtype).astype(np.float64), s)
+
+
+# --------------------------------------------- intra orders, head patterns
+def _chain_from_root(tr):
+    order, v = [], topology.root_of(tr)[0]
+    while v != -1:
+        order.append(v)
+        v = tr[v].down[0]
+    return order
+
+
+def test_active_trees_table(golden):
+    # [Course13] "本机真实树形": one node, 12 channels, each channel's chain in
+    # its intra order; root-to-leaf order, depth N-1 and fan-out 1
+    rows = [r.split() for r in golden("active_trees_table.txt")]
+    for N in (2, 3, 4):
+        mine = [r for r in rows if int(r[0]) == N]
+        orders = [None] * 12
+        for _, chans, order, _, _ in mine:
+            for c in chans.split(","):
+                orders[int(c)] = [int(x) for x in order.split("-")]
+        ch = topology.build_dtree(1, N, 12, orders=orders)
+        for _, chans, order, depth, fan in mine:
+            for c in chans.split(","):
+                tr = ch[int(c)]
+                assert "-".join(map(str, _chain_from_root(tr))) == order
+                assert topology.exact_depth(tr) == int(depth)
+                assert max(sum(d != -1 for d in t.down) for t in tr) == int(fan)
+                _check_invariants(tr, N)
+
+
+def test_split_tree_two_by_two_by_hand():
+    # SPLIT_TREE: parent head = local 0, child heads = local 1.  Two nodes of
+    # two ranks; node tree 0 is node 0 -> node 1 (as node 0's d1).  Node 1's
+    # parent head (rank 2) goes up to node 0's child1 head (rank 1), which is
+    # the end of node 0's chain: the whole tree is the chain 0-1-2-3.
+    tr = topology.build_dtree(2, 2, 1, pattern="split_tree")[0]
+    assert _chain_from_root(tr) == [0, 1, 2, 3]
+    assert [t.up for t in tr] == [-1, 0, 1, 2]
+    # TREE on the same layout hangs node 1 under rank 0 beside its chain child
+    tr = topology.build_dtree(2, 2, 1, pattern="tree")[0]
+    assert tr[0].down == [1, 2, -1] and tr[2].up == 0
+
+
+def test_balanced_tree_four_by_two_by_hand():
+    # BALANCED_TREE: child0 head = local 1, child1 head = local 0.  Node tree
+    # 0 of 4 nodes: 0 -> 2 -> {1 (d0), 3 (d1)}.  Node 2 = ranks 4, 5: node 1's
+    # parent head (rank 2) hangs under rank 5 (child0 head), node 3's (rank 6)
+    # under rank 4 (child1 head); node 2's parent head (rank 4) hangs under
+    # node 0's child1 head (rank 0), since node 2 is node 0's d1.
+    tr = topology.build_dtree(4, 2, 1, pattern="balanced_tree")[0]
+    assert tr[2].up == 5 and tr[6].up == 4 and tr[4].up == 0
+    assert tr[5].down == [2, -1, -1] and tr[4].down == [5, 6, -1]
+    assert tr[0].down == [1, 4, -1]
+
+
+@pytest.mark.parametrize("pattern", ["tree", "split_tree", "balanced_tree"])
+def test_pattern_invariants(pattern):
+    rng = np.random.default_rng(30)
+    for L in (2, 3, 4, 8):
+        for n in range(1, 64 // L + 1):
+            orders = [list(rng.permutation(L)) for _ in range(3)]
+            for ch in (topology.build_dtree(n, L, 2, pattern=pattern),
+                       topology.build_dtree(n, L, 3, pattern=pattern, orders=orders)):
+                for tr in ch:
+                    _check_invariants(tr, n * L)
