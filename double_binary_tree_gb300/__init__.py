@@ -21,6 +21,7 @@ VR_ERR_CUDA, VR_ERR_TIMEOUT, VR_ERR_INTERNAL = 3, 4, 5
 VR_FLOAT32, VR_FLOAT16, VR_BFLOAT16 = 0, 1, 2
 VR_SUM, VR_MAX = 0, 1
 VR_ALGO_RING, VR_ALGO_TREE = 0, 1
+VR_PATTERN_TREE, VR_PATTERN_SPLIT_TREE, VR_PATTERN_BALANCED_TREE = 0, 1, 2
 VR_MAX_RANKS = 64
 VR_MAX_CHANNELS = 64
 VR_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -42,10 +43,12 @@ PP = P(VP)
 _SIGNATURES = {
     "vr_build_ring": (I, [I, I, P(I), P(I)]),
     "vr_build_dtree": (I, [I, I, I, P(vr_tree_t)]),
+    "vr_build_dtree_ex": (I, [I, I, I, I, P(I), P(vr_tree_t)]),
     "vr_partition": (I, [S, I, I, I, P(S), P(S)]),
     "vr_ring_block": (I, [S, I, I, I, S, S, P(I), P(I)]),
     "vr_allreduce": (I, [PP, PP, I, S, I, I, I, I, S, VP]),
     "vr_allreduce_ex": (I, [PP, PP, I, S, I, I, I, I, S, I, VP]),
+    "vr_allreduce_trees": (I, [PP, PP, I, S, I, I, I, S, P(vr_tree_t), VP]),
     "vr_reduce_scatter": (I, [PP, PP, I, S, I, I, I, I, S, VP]),
     "vr_allgather": (I, [PP, PP, I, S, I, I, I, S, VP]),
     "vr_allreduce_tree_updown": (I, [PP, PP, I, S, I, I, I, S, I, VP]),
@@ -129,6 +132,19 @@ def vr_build_dtree(nNodes, localRanks, nChannels):
     return list(out)[:R * nChannels]
 
 
+def vr_build_dtree_ex(nNodes, localRanks, nChannels, pattern=VR_PATTERN_TREE, intraOrders=None):
+    """intraOrders: None or nChannels rows of localRanks ints."""
+    R = nNodes * localRanks
+    out = (vr_tree_t * max(R * nChannels, 1))()
+    orders = None
+    if intraOrders is not None:
+        flat = [int(x) for row in intraOrders for x in row]
+        orders = (ctypes.c_int * max(len(flat), 1))(*flat)
+    _check(_L().vr_build_dtree_ex(nNodes, localRanks, nChannels, pattern, orders, out),
+           "vr_build_dtree_ex")
+    return list(out)[:R * nChannels]
+
+
 def vr_partition(count, dtype, nChannels, channel):
     """Returns (offset, channelCount)."""
     off, n = ctypes.c_size_t(), ctypes.c_size_t()
@@ -157,6 +173,15 @@ def vr_allreduce_ex(sendbufs, recvbufs, R, count, dtype, op, algo, nChannels, ch
     _check(_L().vr_allreduce_ex(_ptrs(sendbufs), _ptrs(recvbufs), R, count, dtype, op, algo,
                                 nChannels, chunkBytes, localRanks, _stream(stream)),
            "vr_allreduce_ex")
+
+
+def vr_allreduce_trees(sendbufs, recvbufs, R, count, dtype, op, nChannels, chunkBytes, trees,
+                       stream=None):
+    """trees: nChannels*R vr_tree_t records (as vr_build_dtree_ex returns)."""
+    arr = (vr_tree_t * max(len(trees), 1))(*trees) if trees is not None else None
+    _check(_L().vr_allreduce_trees(_ptrs(sendbufs), _ptrs(recvbufs), R, count, dtype, op,
+                                   nChannels, chunkBytes, arr, _stream(stream)),
+           "vr_allreduce_trees")
 
 
 def vr_reduce_scatter(sendbufs, recvbufs, R, recvcount, dtype, op, algo, nChannels, chunkBytes,

@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(kBlock, kMinBlocksTree) tree_up_kernel(const _
   constexpr long long E = sizeof(T);
   __shared__ const char* s_src[kMaxRanks];
   __shared__ char* s_dst[kMaxRanks];
-  __shared__ __align__(16) FoldProg s_prog[2];
+  __shared__ __align__(16) FoldProg s_prog[kMaxProgs];
   stage_args<kTreeAllReduce>(a, s_src, s_dst, s_prog);
 
   const int R = a.R;
@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(kBlock) tree_down_kernel(const __grid_constant
   constexpr long long E = sizeof(T);
   __shared__ const char* s_src[kMaxRanks];
   __shared__ char* s_dst[kMaxRanks];
-  __shared__ __align__(16) FoldProg s_prog[2];
+  __shared__ __align__(16) FoldProg s_prog[kMaxProgs];
   stage_args<kTreeAllReduce>(a, s_src, s_dst, s_prog);
 
   const int R = a.R;

@@ -114,6 +114,15 @@ vr_result_t tree_programs(int nNodes, int L, std::array<FoldProg, 2>* out) {
   return VR_SUCCESS;
 }
 
+// The double tree's two programs; channels [0, ceil(nCh/2)) fold with tree
+// 0, the others with tree 1.
+void set_dtree_programs(KArgs& a, const std::array<FoldProg, 2>& p, int nCh) {
+  a.prog[0] = p[0];
+  a.prog[1] = p[1];
+  a.nProgs = 2;
+  for (int c = 0; c < nCh; ++c) a.chanProg[c] = (uint8_t)channel_tree(c, nCh);
+}
+
 bool overlap(uintptr_t a, size_t an, uintptr_t b, size_t bn) {
   return an && bn && a < b + bn && b < a + an;
 }
@@ -185,11 +194,15 @@ const void* pick_staged(int dtype, int mode, int op, int stack = 0) {
   }
 }
 
-const void* pick_kernel(int dtype, int mode, int op, bool vec, int stack = 0) {
+// Register-path kernel; with at most 4 ranks a thread takes two units per
+// step (measured: one unit of 4 ranks keeps too few loads in flight).
+const void* pick_kernel(int dtype, int mode, int op, bool vec, int stack = 0, int R = 64) {
+  // VR_PAIR_UNITS=0 (read per call) turns the two-unit step off, for tuning
+  const bool pair = vec && R <= 4 && mode != kReduceScatter && env_uint("VR_PAIR_UNITS", 1) != 0;
   switch (dtype) {
-    case VR_FLOAT32: return kernel_ptr_f32(mode, op, vec, stack);
-    case VR_FLOAT16: return kernel_ptr_f16(mode, op, vec, stack);
-    case VR_BFLOAT16: return kernel_ptr_bf16(mode, op, vec, stack);
+    case VR_FLOAT32: return kernel_ptr_f32(mode, op, vec, stack, pair);
+    case VR_FLOAT16: return kernel_ptr_f16(mode, op, vec, stack, pair);
+    case VR_BFLOAT16: return kernel_ptr_bf16(mode, op, vec, stack, pair);
     default: return nullptr;
   }
 }
@@ -329,6 +342,17 @@ vr_result_t vr_build_dtree(int nNodes, int localRanks, int nChannels, vr_tree_t*
   return build_dtree(nNodes, localRanks, nChannels, trees);
 }
 
+vr_result_t vr_build_dtree_ex(int nNodes, int localRanks, int nChannels,
+                              vr_tree_pattern_t pattern, const int* intraOrders,
+                              vr_tree_t* trees) {
+  if (nNodes < 1 || localRanks < 1 || nNodes > kMaxRanks || localRanks > kMaxRanks ||
+      nNodes * localRanks > kMaxRanks || nChannels < 1 || nChannels > kMaxChannels || !trees ||
+      (pattern != VR_PATTERN_TREE && pattern != VR_PATTERN_SPLIT_TREE &&
+       pattern != VR_PATTERN_BALANCED_TREE))
+    return VR_ERR_INVALID_ARGUMENT;
+  return build_dtree_ex(nNodes, localRanks, nChannels, pattern, intraOrders, trees);
+}
+
 vr_result_t vr_partition(size_t count, vr_dtype_t dtype, int nChannels, int channel,
                          size_t* offset, size_t* channelCount) {
   const size_t E = elem_size(dtype);
@@ -384,9 +408,7 @@ vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, 
     mode = kTreeAllReduce;
     std::array<FoldProg, 2> p;
     if ((e = tree_programs(R / localRanks, localRanks, &p)) != VR_SUCCESS) return e;
-    a.prog[0] = p[0];
-    a.prog[1] = p[1];
-    a.treeSplit = (nChannels + 1) / 2;
+    set_dtree_programs(a, p, nChannels);
     stack = std::max(p[0].depth, p[1].depth);
   }
   const bool vec = aligned16(sendbufs, R, 0) && aligned16(recvbufs, R, 0);
@@ -398,8 +420,8 @@ vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, 
     return launch_staged(pick_staged(dtype, mode, op, stack), a, mode, stream);
   }
   const long long NV = vec ? kGrainBytes / (long long)E : 1;
-  return launch(pick_kernel(dtype, mode, op, vec, stack), a, ((long long)count + NV - 1) / NV,
-                stream);
+  return launch(pick_kernel(dtype, mode, op, vec, stack, R), a,
+                ((long long)count + NV - 1) / NV, stream);
 }
 
 vr_result_t vr_allreduce(const void* const* sendbufs, void* const* recvbufs, int R, size_t count,
@@ -407,6 +429,51 @@ vr_result_t vr_allreduce(const void* const* sendbufs, void* const* recvbufs, int
                          size_t chunkBytes, void* stream) {
   return vr_allreduce_ex(sendbufs, recvbufs, R, count, dtype, op, algo, nChannels, chunkBytes, 1,
                          stream);
+}
+
+vr_result_t vr_allreduce_trees(const void* const* sendbufs, void* const* recvbufs, int R,
+                               size_t count, vr_dtype_t dtype, vr_op_t op, int nChannels,
+                               size_t chunkBytes, const vr_tree_t* trees, void* stream) {
+  if (!valid_common(R, dtype, nChannels, chunkBytes) || (op != VR_SUM && op != VR_MAX) || !trees)
+    return VR_ERR_INVALID_ARGUMENT;
+  for (int c = 0; c < nChannels; ++c)
+    if (!valid_tree(trees + (size_t)c * R, R)) return VR_ERR_INVALID_ARGUMENT;
+  const size_t E = elem_size(dtype);
+  vr_result_t e = check_buffers(sendbufs, recvbufs, R, count * E, count * E, kAR, E);
+  if (e != VR_SUCCESS || count == 0) return e;
+  KArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.R = R;
+  for (int r = 0; r < R; ++r) { a.src[r] = sendbufs[r]; a.dst[r] = recvbufs[r]; }
+  fill_partition(a, count, E, nChannels, chunkBytes);
+  // one program per distinct tree
+  int stack = 0;
+  for (int c = 0; c < nChannels; ++c) {
+    const vr_tree_t* tc = trees + (size_t)c * R;
+    int found = -1;
+    for (int q = 0; q < c && found < 0; ++q)
+      if (std::memcmp(tc, trees + (size_t)q * R, sizeof(vr_tree_t) * R) == 0)
+        found = a.chanProg[q];
+    if (found < 0) {
+      if (a.nProgs == kMaxProgs) return VR_ERR_UNSUPPORTED;
+      if (compile_fold(tc, R, &a.prog[a.nProgs]) != VR_SUCCESS) return VR_ERR_UNSUPPORTED;
+      stack = std::max(stack, (int)a.prog[a.nProgs].depth);
+      found = a.nProgs++;
+    }
+    a.chanProg[c] = (uint8_t)found;
+  }
+  const bool vec = aligned16(sendbufs, R, 0) && aligned16(recvbufs, R, 0);
+  const int forced = forced_path();
+  if (vec && forced == 2) {
+    const long long bytes = (long long)count * (long long)E;
+    a.unitsAll = (bytes + 15) / 16;
+    a.unitsFull = bytes / 16;
+    return launch_staged(pick_staged(dtype, kTreeAllReduce, op, stack), a, kTreeAllReduce,
+                         stream);
+  }
+  const long long NV = vec ? kGrainBytes / (long long)E : 1;
+  return launch(pick_kernel(dtype, kTreeAllReduce, op, vec, stack, R), a,
+                ((long long)count + NV - 1) / NV, stream);
 }
 
 vr_result_t vr_reduce_scatter(const void* const* sendbufs, void* const* recvbufs, int R,
@@ -456,6 +523,23 @@ vr_result_t vr_allgather(const void* const* sendbufs, void* const* recvbufs, int
   a.count = (long long)bytes;
   a.nCh = nChannels;
   const bool vec = aligned16(sendbufs, R, bytes) && aligned16(recvbufs, R, 0);
+  if (vec && forced_path() != 1) {
+    // the TMA copy: one warp per CTA, tiles of gather_tile_bytes() of one rank
+    DeviceInfo di;
+    int device = 0;
+    if ((e = device_info(&di, &device)) != VR_SUCCESS) return e;
+    const long long tile = gather_tile_bytes();
+    a.tiles = (long long)R * (((long long)bytes + tile - 1) / tile);
+    a.status = di.status;
+    a.timeoutNs = wait_timeout_ns();
+    const long long grid = std::min<long long>(a.tiles, (long long)di.sms * gather_ctas_per_sm());
+    void* args[] = {&a};
+    if (cudaLaunchKernel(kernel_ptr_allgather_tma(), dim3((unsigned)grid), dim3(32), args, 0,
+                         (cudaStream_t)stream) != cudaSuccess)
+      return VR_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return VR_SUCCESS;
+  }
   const long long NB = vec ? kGrainBytes : 1;
   const long long units = (long long)R * (((long long)bytes + NB - 1) / NB);
   return launch(kernel_ptr_allgather(vec), a, units, stream);
@@ -527,9 +611,7 @@ vr_result_t vr_allreduce_tree_updown(const void* const* sendbufs, void* const* r
   fill_partition(a, count, E, nChannels, chunkBytes);
   std::array<FoldProg, 2> p;
   if ((e = tree_programs(R / localRanks, localRanks, &p)) != VR_SUCCESS) return e;
-  a.prog[0] = p[0];
-  a.prog[1] = p[1];
-  a.treeSplit = (nChannels + 1) / 2;
+  set_dtree_programs(a, p, nChannels);
   const int stack = std::max(p[0].depth, p[1].depth);
   const bool vec = aligned16(sendbufs, R, 0) && aligned16(recvbufs, R, 0);
   const long long NV = vec ? kGrainBytes / (long long)E : 1;

@@ -13,7 +13,8 @@ constexpr int kGrainBytes = 16;      // channel ranges are cut in 16-byte grains
 constexpr int kMaxStack = 8;         // partial sums a tree fold keeps live at once
 constexpr int kStagedMaxStages = 16; // shared-memory stages of a staged kernel
 constexpr int kStagedMaxConsumers = 7;  // its consumer warps (8 warps per CTA: 2 per SM sub-partition)
-constexpr int kStagedHeader = 2048;  // its barriers, flags, pointer tables and programs
+constexpr int kStagedHeader = 4096;  // its barriers, flags, pointer tables and programs
+constexpr int kMaxProgs = 16;        // distinct tree fold programs per call
 
 // A tree's reduction order as a stream of rank loads.  Slot i loads rank
 // rank[i]; before it, ctl[i] & 15 "pop-add" steps fold the top partial into
@@ -46,7 +47,7 @@ struct KArgs {
   long long chunk;      // C, elements per rank per ring loop block
   int R;
   int nCh;
-  int treeSplit;        // channels [0, treeSplit) follow prog[0], the rest prog[1]
+  int nProgs;           // fold programs in prog[]
   int pad;
   unsigned* status;     // this device's status word
   void* scratch;        // stepwise ring: the message FIFO (count elements)
@@ -61,7 +62,8 @@ struct KArgs {
   int tileUnits;        // 16-byte units per rank per tile
   unsigned tileBytes;   // bytes per rank per tile (16 * tileUnits)
   unsigned stageBytes;  // R * tileBytes
-  FoldProg prog[2];
+  uint8_t chanProg[kMaxChannels];  // channel c folds with prog[chanProg[c]]
+  FoldProg prog[kMaxProgs];
 };
 
 }  // namespace vr

@@ -204,15 +204,15 @@ template <typename T, int NV> struct Lanes<T, VR_MAX, NV, false> {
 // ------------------------------------------------------------------ folds
 // Ranks j, j+1, ..., j+R-1 (mod R), left to right.  The first batch is
 // peeled so that no step has to ask whether it is the first.
-template <typename T, int OP, int NV, class Src>
+template <typename T, int OP, int NV, class Src, int B = kBatch>
 __device__ __forceinline__ typename Unit<T, NV>::Raw ring_fold(const Src& src, int R, int j) {
   typedef Unit<T, NV> Un;
   typedef Lanes<T, OP, NV> Ln;
   typename Ln::L acc[Ln::N];
-  for (int k0 = 0; k0 < R; k0 += kBatch) {
-    typename Un::Raw v[kBatch];
+  for (int k0 = 0; k0 < R; k0 += B) {
+    typename Un::Raw v[B];
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
+    for (int i = 0; i < B; ++i) {
       const int k = k0 + i;
       if (k < R) {
         int r = j + k;
@@ -226,7 +226,7 @@ __device__ __forceinline__ typename Unit<T, NV>::Raw ring_fold(const Src& src, i
       i0 = 1;
     }
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
+    for (int i = 0; i < B; ++i) {
       const int k = k0 + i;
       if (i >= i0 && k < R) {
         typename Ln::L x[Ln::N];
@@ -341,7 +341,7 @@ __device__ __forceinline__ void below_fold(const Below<Ln, S>& bl, int d, typena
 }
 #undef VR_BELOW_SLOTS
 
-template <typename T, int OP, int NV, int S, class Src>
+template <typename T, int OP, int NV, int S, class Src, int B = kBatch>
 __device__ __forceinline__ typename Unit<T, NV>::Raw tree_fold(const Src& src, const FoldProg& p,
                                                               int R) {
   typedef Unit<T, NV> Un;
@@ -351,15 +351,15 @@ __device__ __forceinline__ typename Unit<T, NV>::Raw tree_fold(const Src& src, c
   for (int e = 0; e < Ln::N; ++e) top[e] = 0;
   Below<Ln, S> below;
   int sp = 0;  // live partials, the top included
-  for (int k0 = 0; k0 < R; k0 += kBatch) {
-    typename Un::Raw v[kBatch];
+  for (int k0 = 0; k0 < R; k0 += B) {
+    typename Un::Raw v[B];
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
+    for (int i = 0; i < B; ++i) {
       const int k = k0 + i;
       if (k < R) v[i] = load_unit<T, NV>(src, p.rank[k]);
     }
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
+    for (int i = 0; i < B; ++i) {
       const int k = k0 + i;
       if (k < R) {
         const int c = p.ctl[k];
@@ -422,7 +422,7 @@ __device__ __forceinline__ void locate(const KArgs& a, long long e, Cursor& c) {
   if constexpr (MODE == kTreeAllReduce) {
     c.lo = cs;
     c.hi = ce;
-    c.t = k < a.treeSplit ? 0 : 1;
+    c.t = a.chanProg[k];
     c.j = 0;
   } else {
     const long long R = a.R;

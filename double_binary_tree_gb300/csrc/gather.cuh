@@ -1,0 +1,96 @@
+// TMA AllGather (sm_103a): the copy runs on the Tensor Memory Accelerator.
+//
+// AllGather moves rank r's buffer into block r of every rank's output
+// ([Interview] "先弄清楚": the segments are concatenated back), so each byte
+// is read once and written R times.  Issuing R vector stores per loaded unit
+// from threads saturates the store issue path (the register-path kernel
+// stalls on MIO / LSU throttle); here one warp per CTA streams tiles of a
+// source rank into shared memory with a bulk copy and has the TMA engine
+// write each tile to the R destinations with bulk stores.  Threads move no
+// data.
+//
+// Stages are reused once the bulk stores that read them have finished
+// reading (cp.async.bulk.wait_group.read); the wait for a tile's load is
+// bounded like every wait of the staged kernels and reports VR_ERR_TIMEOUT.
+#pragma once
+
+#include "staged.cuh"
+
+namespace vr {
+
+constexpr int kGatherStages = 4;          // shared-memory stages per CTA
+constexpr unsigned kGatherTile = 8192;    // bytes per tile
+constexpr int kGatherCtasPerSm = 4;
+
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, unsigned bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+template <int N> __device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// a.count: bytes per source rank (a multiple of 16); a.tiles: tiles of
+// kGatherTile bytes over all ranks, rank by rank.  One warp per CTA.
+__global__ void __launch_bounds__(kWarpSize) allgather_tma_kernel(const __grid_constant__ KArgs a) {
+  __shared__ __align__(128) unsigned char stage[kGatherStages][kGatherTile];
+  __shared__ __align__(8) uint64_t full[kGatherStages];
+  __shared__ int abort_flag;
+  __shared__ const char* s_src[kMaxRanks];
+  __shared__ char* s_dst[kMaxRanks];
+  const int lane = threadIdx.x;
+  const int R = a.R;
+  for (int i = lane; i < R; i += kWarpSize) {
+    s_src[i] = static_cast<const char*>(a.src[i]);
+    s_dst[i] = static_cast<char*>(a.dst[i]);
+  }
+  if (lane == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < kGatherStages; ++s) mbar_init(smem_addr(&full[s]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncwarp();
+
+  const long long bytes = a.count;
+  const long long perRank = (bytes + kGatherTile - 1) / kGatherTile;
+  const long long tb = a.tiles * blockIdx.x / gridDim.x;
+  const long long te = a.tiles * (blockIdx.x + 1) / gridDim.x;
+  for (long long i = 0; tb + i < te; ++i) {
+    const int s = (int)(i % kGatherStages);
+    const long long t = tb + i;
+    const int r = (int)(t / perRank);
+    const long long off = (t - (long long)r * perRank) * kGatherTile;
+    const unsigned n = (unsigned)min((long long)kGatherTile, bytes - off);
+    const uint32_t buf = smem_addr(stage[s]);
+    if (i >= kGatherStages) bulk_wait_read<kGatherStages - 1>();  // stage s read out
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive_expect_tx(smem_addr(&full[s]), n);
+      bulk_load(buf, s_src[r] + off, n, smem_addr(&full[s]));
+    }
+    const bool ok = __any_sync(~0u, wait_phase(smem_addr(&full[s]),
+                                               (unsigned)((i / kGatherStages) & 1),
+                                               &abort_flag, false, a.timeoutNs));
+    if (!ok) {
+      if (lane == 0) raise_error(a.status, &abort_flag, VR_ERR_TIMEOUT);
+      break;
+    }
+    const char* from = s_src[r] + off;
+    for (int q = lane; q < R; q += kWarpSize) {
+      char* to = s_dst[q] + (long long)r * bytes + off;
+      if (to != from) bulk_store(to, buf, n);
+    }
+    bulk_commit();
+  }
+  bulk_wait_all();
+}
+
+}  // namespace vr

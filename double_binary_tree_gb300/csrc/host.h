@@ -11,16 +11,24 @@ void btree(int n, int r, int* up, int* d0, int* d1, int* childType);
 void dtree(int n, int r, int t[2][4]);
 int channel_tree(int c, int nCh);
 vr_result_t build_dtree(int nNodes, int L, int nCh, vr_tree_t* out);
+vr_result_t build_dtree_ex(int nNodes, int L, int nCh, int pattern, const int* orders,
+                           vr_tree_t* out);
+bool valid_tree(const vr_tree_t* tree, int R);
 vr_result_t compile_fold(const vr_tree_t* tree, int R, FoldProg* prog);
 
 // Kernel entry points, one getter per element type: `mode` is a Mode,
 // `vec` selects the 16-byte vector path (all buffers and block offsets
 // 16-byte aligned), else the element path; `stack` is the deepest partial
 // stack of the tree programs (selects the 4- or 8-slot tree kernel).
-const void* kernel_ptr_f32(int mode, int op, bool vec, int stack);
-const void* kernel_ptr_f16(int mode, int op, bool vec, int stack);
-const void* kernel_ptr_bf16(int mode, int op, bool vec, int stack);
+// `pair`: two units per thread step (vector path, at most 4 ranks).
+const void* kernel_ptr_f32(int mode, int op, bool vec, int stack, bool pair);
+const void* kernel_ptr_f16(int mode, int op, bool vec, int stack, bool pair);
+const void* kernel_ptr_bf16(int mode, int op, bool vec, int stack, bool pair);
 const void* kernel_ptr_allgather(bool vec);
+// TMA AllGather (16-byte aligned buffers): one warp per CTA.
+const void* kernel_ptr_allgather_tma();
+int gather_tile_bytes();
+int gather_ctas_per_sm();
 const void* staged_kernel_ptr_f32(int mode, int op, int stack);
 const void* staged_kernel_ptr_f16(int mode, int op, int stack);
 const void* staged_kernel_ptr_bf16(int mode, int op, int stack);

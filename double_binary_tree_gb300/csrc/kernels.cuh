@@ -38,22 +38,27 @@ __device__ __forceinline__ void stage_args(const KArgs& a, const char** s_src, c
   if constexpr (MODE == kTreeAllReduce) {
     const unsigned* from = reinterpret_cast<const unsigned*>(a.prog);
     unsigned* to = reinterpret_cast<unsigned*>(s_prog);
-    for (int i = threadIdx.x; i < (int)(2 * sizeof(FoldProg) / 4); i += blockDim.x) to[i] = from[i];
+    const int words = a.nProgs * (int)(sizeof(FoldProg) / 4);
+    for (int i = threadIdx.x; i < words; i += blockDim.x) to[i] = from[i];
   }
   __syncthreads();
 }
 
 // AllReduce, ring or tree.  VEC: 16-byte units (aligned buffers), else one
-// element per unit.
-template <typename T, int OP, int MODE, bool VEC, int S>
+// element per unit.  P = 2 (few ranks): a thread takes two units per step and
+// computes both results before storing either, so the second unit's loads
+// are in flight together with the first's -- with 4 ranks or fewer one unit
+// alone keeps too few bytes in flight.
+template <typename T, int OP, int MODE, bool VEC, int S, int P>
 __global__ void __launch_bounds__(kBlock, MODE == kTreeAllReduce ? kMinBlocksTree : kMinBlocksRing)
     allreduce_kernel(const __grid_constant__ KArgs a) {
   constexpr int U = Ty<T>::U;
   constexpr int NV = VEC ? U : 1;
   constexpr long long E = sizeof(T);
+  static_assert(P == 1 || (P == 2 && VEC), "two units per step on the vector path only");
   __shared__ const char* s_src[kMaxRanks];
   __shared__ char* s_dst[kMaxRanks];
-  __shared__ __align__(16) FoldProg s_prog[2];
+  __shared__ __align__(16) FoldProg s_prog[kMaxProgs];
   stage_args<MODE>(a, s_src, s_dst, s_prog);
 
   const int R = a.R;
@@ -62,7 +67,9 @@ __global__ void __launch_bounds__(kBlock, MODE == kTreeAllReduce ? kMinBlocksTre
   const long long ub = units * blockIdx.x / gridDim.x;
   const long long ue = units * (blockIdx.x + 1) / gridDim.x;
   Cursor cur{0, -1, 0, 0, 0, 0, 0};
-  for (long long u = ub + threadIdx.x; u < ue; u += blockDim.x) {
+
+  // one unit, whatever its shape
+  auto one = [&](long long u) {
     const long long e0 = u * NV;
     const int n = (int)min((long long)NV, count - e0);
     seek<U, MODE>(a, e0, cur);
@@ -87,6 +94,40 @@ __global__ void __launch_bounds__(kBlock, MODE == kTreeAllReduce ? kMinBlocksTre
         for (int r = 0; r < R; ++r) Unit<T, 1>::store(s_dst[r] + e * E, o);
       }
     }
+  };
+
+  for (long long u = ub + threadIdx.x; u < ue; u += P * blockDim.x) {
+    if constexpr (P == 2) {
+      const long long u2 = u + blockDim.x;
+      if (u2 < ue) {
+        const long long e0 = u * NV, e1 = u2 * NV;
+        seek<U, MODE>(a, e0, cur);
+        const bool f0 = count - e0 >= NV && e0 + NV <= cur.hi;
+        const int j0 = cur.j, t0 = cur.t;
+        seek<U, MODE>(a, e1, cur);
+        const bool f1 = count - e1 >= NV && e1 + NV <= cur.hi;
+        if (f0 && f1) {
+          const GlobalSrc s0{s_src, e0 * E}, s1{s_src, e1 * E};
+          typename Unit<T, NV>::Raw o0, o1;
+          if constexpr (MODE == kTreeAllReduce) {
+            o0 = tree_fold<T, OP, NV, S, GlobalSrc, 4>(s0, s_prog[t0], R);
+            o1 = tree_fold<T, OP, NV, S, GlobalSrc, 4>(s1, s_prog[cur.t], R);
+          } else {
+            o0 = ring_fold<T, OP, NV, GlobalSrc, 4>(s0, R, j0);
+            o1 = ring_fold<T, OP, NV, GlobalSrc, 4>(s1, R, cur.j);
+          }
+          for (int r = 0; r < R; ++r) {
+            Unit<T, NV>::store(s_dst[r] + e0 * E, o0);
+            Unit<T, NV>::store(s_dst[r] + e1 * E, o1);
+          }
+        } else {
+          one(u);
+          one(u2);
+        }
+        continue;
+      }
+    }
+    one(u);
   }
 }
 

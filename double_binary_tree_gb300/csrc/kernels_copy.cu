@@ -1,4 +1,5 @@
 // AllGather kernel instantiations and the per-device status word.
+#include "gather.cuh"
 #include "host.h"
 #include "kernels.cuh"
 
@@ -11,6 +12,10 @@ __device__ unsigned g_status_word = 0;
 const void* kernel_ptr_allgather(bool vec) {
   return vec ? (const void*)allgather_kernel<true> : (const void*)allgather_kernel<false>;
 }
+
+const void* kernel_ptr_allgather_tma() { return (const void*)allgather_tma_kernel; }
+int gather_tile_bytes() { return (int)kGatherTile; }
+int gather_ctas_per_sm() { return kGatherCtasPerSm; }
 
 cudaError_t read_and_clear_status(unsigned* value) {
   cudaError_t e = cudaMemcpyFromSymbol(value, g_status_word, sizeof(unsigned));

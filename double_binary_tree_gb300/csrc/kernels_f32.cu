@@ -7,20 +7,27 @@
 namespace vr {
 
 // Register-path kernels: `vec` = 16-byte units, else element units.
-const void* kernel_ptr_f32(int mode, int op, bool vec, int stack) {
-#define VR_PICK(OP, VEC)                                                                         \
+const void* kernel_ptr_f32(int mode, int op, bool vec, int stack, bool pair) {
+#define VR_PICK(OP, VEC, PAIR)                                                                   \
   switch (mode) {                                                                                \
-    case kRingAllReduce: return (const void*)allreduce_kernel<float, OP, kRingAllReduce, VEC, 4>; \
+    case kRingAllReduce:                                                                         \
+      return (const void*)allreduce_kernel<float, OP, kRingAllReduce, VEC, 4, (VEC && PAIR) ? 2 : 1>; \
     case kTreeAllReduce:                                                                         \
-      return stack <= 4 ? (const void*)allreduce_kernel<float, OP, kTreeAllReduce, VEC, 4>        \
-                        : (const void*)allreduce_kernel<float, OP, kTreeAllReduce, VEC, 8>;       \
+      if (PAIR)                                                                                  \
+        return (const void*)allreduce_kernel<float, OP, kTreeAllReduce, VEC, 4, (VEC && PAIR) ? 2 : 1>; \
+      return stack <= 4 ? (const void*)allreduce_kernel<float, OP, kTreeAllReduce, VEC, 4, 1>     \
+                        : (const void*)allreduce_kernel<float, OP, kTreeAllReduce, VEC, 8, 1>;    \
     case kReduceScatter: return (const void*)reduce_scatter_kernel<float, OP, VEC>;               \
     default: return nullptr;                                                                     \
   }
+  // two units per step: vector path, at most 4 ranks (trees of <= 4 ranks
+  // fold with at most 4 partials)
   if (op == VR_SUM) {
-    if (vec) { VR_PICK(VR_SUM, true) } else { VR_PICK(VR_SUM, false) }
+    if (vec && pair) { VR_PICK(VR_SUM, true, true) }
+    else if (vec) { VR_PICK(VR_SUM, true, false) } else { VR_PICK(VR_SUM, false, false) }
   } else {
-    if (vec) { VR_PICK(VR_MAX, true) } else { VR_PICK(VR_MAX, false) }
+    if (vec && pair) { VR_PICK(VR_MAX, true, true) }
+    else if (vec) { VR_PICK(VR_MAX, true, false) } else { VR_PICK(VR_MAX, false, false) }
   }
 #undef VR_PICK
 }

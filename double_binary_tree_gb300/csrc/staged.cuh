@@ -136,7 +136,8 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
   const char** s_src = reinterpret_cast<const char**>(smem + 16 * kStagedMaxStages + 16);
   char** s_dst = reinterpret_cast<char**>(smem + 16 * kStagedMaxStages + 16 + 8 * kMaxRanks);
   FoldProg* s_prog = reinterpret_cast<FoldProg*>(s_dst + kMaxRanks);
-  static_assert(16 * kStagedMaxStages + 16 + 16 * kMaxRanks + 2 * sizeof(FoldProg) <= kStagedHeader,
+  static_assert(16 * kStagedMaxStages + 16 + 16 * kMaxRanks + kMaxProgs * sizeof(FoldProg) <=
+                    kStagedHeader,
                 "shared-memory header overflows");
   const uint32_t data = smem_addr(smem + kStagedHeader);
   const unsigned char* stage0 = smem + kStagedHeader;
@@ -150,7 +151,8 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
   if constexpr (MODE == kTreeAllReduce) {
     const unsigned* from = reinterpret_cast<const unsigned*>(a.prog);
     unsigned* to = reinterpret_cast<unsigned*>(s_prog);
-    for (int i = threadIdx.x; i < (int)(2 * sizeof(FoldProg) / 4); i += blockDim.x) to[i] = from[i];
+    const int words = a.nProgs * (int)(sizeof(FoldProg) / 4);
+    for (int i = threadIdx.x; i < words; i += blockDim.x) to[i] = from[i];
   }
   if (threadIdx.x == 0) {
     *abort = 0;

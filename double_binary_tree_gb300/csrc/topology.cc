@@ -83,32 +83,93 @@ static bool add_child(vr_tree_t* t, int child) {
   return false;
 }
 
-vr_result_t build_dtree(int nNodes, int L, int nCh, vr_tree_t* out) {
+// Positions, in a node's intra order, of its parent head and its child0 and
+// child1 heads ([Course13] "节点内先形成链": TREE 0/0/0, SPLIT_TREE 0/1/1,
+// any other pattern 0/1/0).
+static void head_positions(int pattern, int* p, int* c0, int* c1) {
+  *p = 0;
+  *c0 = pattern == VR_PATTERN_TREE ? 0 : 1;
+  *c1 = pattern == VR_PATTERN_SPLIT_TREE ? 1 : 0;
+}
+
+vr_result_t build_dtree_ex(int nNodes, int L, int nCh, int pattern, const int* orders,
+                           vr_tree_t* out) {
   const int R = nNodes * L;
   const int depth = L - 1 + floor_log2(nNodes);
+  int pi, c0i, c1i;
+  head_positions(pattern, &pi, &c0i, &c1i);
+  if (c0i >= L || c1i >= L) return VR_ERR_INVALID_ARGUMENT;
   int nodeTree[kMaxRanks][2][4];
   for (int k = 0; k < nNodes; ++k) dtree(nNodes, k, nodeTree[k]);
   for (int c = 0; c < nCh; ++c) {
     const int t = channel_tree(c, nCh);
-    for (int k = 0; k < nNodes; ++k) {
-      for (int l = 0; l < L; ++l) {
-        const int rank = k * L + l;
-        vr_tree_t* x = &out[(size_t)c * R + rank];
-        // intra-node chain in local order
+    // the channel's intra order: a permutation of the local ranks
+    int order[kMaxRanks];
+    unsigned long long seen = 0;
+    for (int i = 0; i < L; ++i) {
+      order[i] = orders ? orders[(size_t)c * L + i] : i;
+      if (order[i] < 0 || order[i] >= L || (seen >> order[i] & 1)) return VR_ERR_INVALID_ARGUMENT;
+      seen |= 1ull << order[i];
+    }
+    vr_tree_t* tc = out + (size_t)c * R;
+    // preset: each node's chain in intra order
+    for (int k = 0; k < nNodes; ++k)
+      for (int i = 0; i < L; ++i) {
+        vr_tree_t* x = &tc[k * L + order[i]];
         x->depth = depth;
-        x->up = l == 0 ? -1 : rank - 1;
-        x->down[0] = l == L - 1 ? -1 : rank + 1;
+        x->up = i == 0 ? -1 : k * L + order[i - 1];
+        x->down[0] = i == L - 1 ? -1 : k * L + order[i + 1];
         x->down[1] = x->down[2] = -1;
-        if (l != 0) continue;
-        // the node's head joins the node-level tree t
-        const int pu = nodeTree[k][t][0], c0 = nodeTree[k][t][1], c1 = nodeTree[k][t][2];
-        if (pu >= 0) x->up = pu * L;
-        if (!add_child(x, c0 < 0 ? -1 : c0 * L)) return VR_ERR_INTERNAL;
-        if (!add_child(x, c1 < 0 ? -1 : c1 * L)) return VR_ERR_INTERNAL;
       }
+    // connect: the node-level tree t attached at the heads
+    for (int k = 0; k < nNodes; ++k) {
+      const int u = nodeTree[k][t][0], d0 = nodeTree[k][t][1], d1 = nodeTree[k][t][2];
+      const int type = nodeTree[k][t][3];
+      if (u >= 0) tc[k * L + order[pi]].up = u * L + order[type == 0 ? c0i : c1i];
+      if (!add_child(&tc[k * L + order[c0i]], d0 < 0 ? -1 : d0 * L + order[pi]))
+        return VR_ERR_INTERNAL;
+      if (!add_child(&tc[k * L + order[c1i]], d1 < 0 ? -1 : d1 * L + order[pi]))
+        return VR_ERR_INTERNAL;
     }
   }
   return VR_SUCCESS;
+}
+
+vr_result_t build_dtree(int nNodes, int L, int nCh, vr_tree_t* out) {
+  return build_dtree_ex(nNodes, L, nCh, VR_PATTERN_TREE, nullptr, out);
+}
+
+// A caller's tree over R ranks: up/down agree both ways, down[] is compacted,
+// exactly one root, every rank reaches it (hence R-1 edges and no cycle).
+bool valid_tree(const vr_tree_t* tr, int R) {
+  int roots = 0;
+  for (int r = 0; r < R; ++r) {
+    const vr_tree_t& t = tr[r];
+    if (t.up < -1 || t.up >= R || t.up == r) return false;
+    if (t.up < 0) ++roots;
+    else {
+      const int* d = tr[t.up].down;
+      if (d[0] != r && d[1] != r && d[2] != r) return false;
+    }
+    bool gap = false;
+    for (int s = 0; s < 3; ++s) {
+      const int c = t.down[s];
+      if (c < -1 || c >= R) return false;
+      if (c < 0) { gap = true; continue; }
+      if (gap || tr[c].up != r) return false;
+      for (int q = 0; q < s; ++q)
+        if (t.down[q] == c) return false;
+    }
+  }
+  if (roots != 1) return false;
+  for (int r = 0; r < R; ++r) {
+    int v = r, steps = 0;
+    while (tr[v].up >= 0) {
+      v = tr[v].up;
+      if (++steps > R) return false;
+    }
+  }
+  return true;
 }
 
 // ------------------------------------------------------------ fold program

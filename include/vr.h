@@ -93,6 +93,31 @@ vr_result_t vr_build_ring(int R, int nChannels, int* next, int* prev);
  * localRanks < 1, nChannels outside [1, VR_MAX_CHANNELS], NULL `trees`. */
 vr_result_t vr_build_dtree(int nNodes, int localRanks, int nChannels, vr_tree_t* trees);
 
+/* Which rank of a node's intra order joins the node-level tree
+ * ([Course13] "节点内先形成链"): the parent head is always the first; the
+ * heads that take child nodes d0 / d1 are the first / first (TREE), the
+ * second / second (SPLIT_TREE) or the second / first (BALANCED_TREE). */
+typedef enum {
+  VR_PATTERN_TREE = 0,
+  VR_PATTERN_SPLIT_TREE = 1,
+  VR_PATTERN_BALANCED_TREE = 2
+} vr_tree_pattern_t;
+
+/* vr_build_dtree with a head pattern and per-channel intra-node orders
+ * ([Course13] "节点内先形成链": the chain follows treeIntra, which a topology
+ * search may order differently per channel; "本机真实树形" shows such
+ * channels).  intraOrders: NULL (identity) or nChannels*localRanks ints, row
+ * c a permutation of 0..localRanks-1 giving channel c's chain order inside
+ * every node.  The parent head of node k takes up = the child0 or child1
+ * head of its parent node (by k's parentChildType in the node-level tree);
+ * the child0 head appends child node d0's parent head, then the child1 head
+ * appends d1's.  Errors: those of vr_build_dtree, plus
+ * VR_ERR_INVALID_ARGUMENT for a bad pattern, SPLIT_TREE / BALANCED_TREE
+ * with one local rank, or a row that is not a permutation. */
+vr_result_t vr_build_dtree_ex(int nNodes, int localRanks, int nChannels,
+                              vr_tree_pattern_t pattern, const int* intraOrders,
+                              vr_tree_t* trees);
+
 /* Channel c's element range of a message of `count` elements ([Course13]
  * "前置知识": channels take different ranges of one message).  The message
  * is cut into 16-byte grains, split over channels so that the first
@@ -154,6 +179,20 @@ vr_result_t vr_allreduce(const void* const* sendbufs, void* const* recvbufs, int
 vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, int R,
                             size_t count, vr_dtype_t dtype, vr_op_t op, vr_algo_t algo,
                             int nChannels, size_t chunkBytes, int localRanks, void* stream);
+
+/* Tree AllReduce over caller-given trees: channel c folds every element over
+ * trees[c*R .. c*R + R-1] (vr_tree_t records, e.g. from vr_build_dtree_ex)
+ * in the order of vr_allreduce's TREE: each rank folds its local input with
+ * its children's partials in down[] order, the root's value goes to every
+ * rank.  Each channel's records must form one tree over the R ranks: up and
+ * down[] agree both ways, down[] has its present children first, one root,
+ * every rank reaches it.  At most 16 distinct trees per call.  Host-side
+ * errors: those of vr_allreduce, VR_ERR_INVALID_ARGUMENT for a NULL or
+ * invalid tree, VR_ERR_UNSUPPORTED for more than 16 distinct trees or a tree
+ * whose fold keeps more than 8 partials live. */
+vr_result_t vr_allreduce_trees(const void* const* sendbufs, void* const* recvbufs, int R,
+                               size_t count, vr_dtype_t dtype, vr_op_t op, int nChannels,
+                               size_t chunkBytes, const vr_tree_t* trees, void* stream);
 
 /* ReduceScatter ([Interview] "先弄清楚": each rank keeps the reduced 1/n
  * segment it is responsible for): sendbufs[r] holds R*recvcount elements;

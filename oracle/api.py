@@ -28,13 +28,16 @@ def _widen(raws, dtype):
 
 
 def allreduce(raws, dtype, op, algo, n_channels, chunk_bytes, local_ranks=1,
-              counters=None, hop_rounding=False):
+              counters=None, hop_rounding=False, pattern="tree", orders=None):
     """AllReduce of the R raw buffers.  Returns R raw output buffers.
 
     hop_rounding (ring only): every rank keeps its partials in the element
     type between hops, as a ring whose messages travel in that type does --
     each reduction's fp32 result is rounded to the element type (RNE) before
-    it is sent on.  Without it partials stay in fp32 until the end."""
+    it is sent on.  Without it partials stay in fp32 until the end.
+
+    pattern / orders (tree only): the head pattern and per-channel intra-node
+    orders of the trees (``topology.build_dtree``)."""
     R = len(raws)
     count = int(raws[0].size)
     E = numerics.ELEM_SIZE[dtype]
@@ -59,7 +62,8 @@ def allreduce(raws, dtype, op, algo, n_channels, chunk_bytes, local_ranks=1,
                     for (bs, bn), blk in zip(loop, res[r]):
                         out[r][bs:bs + bn] = blk
     elif algo == TREE:
-        trees = topology.build_dtree(R // local_ranks, local_ranks, n_channels)
+        trees = topology.build_dtree(R // local_ranks, local_ranks, n_channels,
+                                     pattern=pattern, orders=orders)
         for k, (cs, cn) in enumerate(chans):
             for (s, n) in partition.tree_chunks(cs, cn, C):
                 res = schedules.tree_allreduce_chunk(xs, trees[k], s, n, op, counters)

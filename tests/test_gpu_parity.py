@@ -262,7 +262,7 @@ def test_reduce_scatter_bit_exact(dtype, op, path):
 
 
 @pytest.mark.parametrize("dtype", [F32, F16, BF16])
-def test_allgather_exact(dtype):
+def test_allgather_exact(dtype, path):
     for R, sc, inplace, shift in [(1, 7, False, 0), (2, 1, False, 0), (3, 1001, False, 0),
                                   (8, 4096, True, 0), (64, 333, False, 0), (5, 100, False, 1)]:
         inp = workloads.generate(R, sc, dtype, "normal", 800 + R)
@@ -393,3 +393,45 @@ def test_hier_16mib_reduce_scatter_and_allgather(hier):
     cat = np.concatenate(want_rs)
     for t in ag:
         assert np.array_equal(bits(t), cat)
+
+
+# --------------------------------------------- caller trees: orders, patterns
+@pytest.mark.parametrize("pattern", [vr.VR_PATTERN_TREE, vr.VR_PATTERN_SPLIT_TREE,
+                                     vr.VR_PATTERN_BALANCED_TREE])
+@pytest.mark.parametrize("dtype", [F32, BF16])
+def test_allreduce_trees_patterns_and_orders(pattern, dtype, path):
+    names = {0: "tree", 1: "split_tree", 2: "balanced_tree"}
+    rng = np.random.default_rng(50 + pattern)
+    for n, L, count, nch in [(1, 4, 30001, 12), (2, 2, 9999, 3), (4, 2, 65537, 12),
+                             (8, 8, 4099, 5), (3, 3, 7777, 2)]:
+        R = n * L
+        pool = [list(map(int, rng.permutation(L))) for _ in range(3)]
+        orders = [pool[c % 3] for c in range(nch)]   # at most 6 distinct trees
+        trees = vr.vr_build_dtree_ex(n, L, nch, pattern, orders)
+        inp = workloads.generate(R, count, dtype, "normal", 60 + R)
+        want = oracle.allreduce([workloads.raw_numpy(t) for t in inp], dtype, SUM, TREE, nch,
+                                1024, local_ranks=L, pattern=names[pattern], orders=orders)
+        src = [t.cuda() for t in inp]
+        bufs = Bufs(R, count, dtype)
+        vr.vr_allreduce_trees(src, bufs.views, R, count, dtype, SUM, nch, 1024, trees)
+        assert_status_ok()
+        bufs.check_canaries()
+        assert_bits_equal([bits(d) for d in bufs.views], want, "trees n=%d L=%d" % (n, L))
+
+
+def test_active_trees_of_the_pages_on_gpu():
+    # one node of 4 ranks, 12 channels in the three chain orders the pages
+    # show ([Course13] "本机真实树形")
+    per = {0: [0, 1, 2, 3], 1: [0, 1, 2, 3], 6: [0, 1, 2, 3], 7: [0, 1, 2, 3],
+           2: [0, 2, 1, 3], 3: [0, 2, 1, 3], 8: [0, 2, 1, 3], 9: [0, 2, 1, 3],
+           4: [1, 0, 3, 2], 5: [1, 0, 3, 2], 10: [1, 0, 3, 2], 11: [1, 0, 3, 2]}
+    orders = [per[c] for c in range(12)]
+    trees = vr.vr_build_dtree_ex(1, 4, 12, vr.VR_PATTERN_TREE, orders)
+    inp = workloads.generate(4, 1 << 20, F32, "normal", 70)
+    want = oracle.allreduce([workloads.raw_numpy(t) for t in inp], F32, SUM, TREE, 12,
+                            512 * 1024, local_ranks=4, orders=orders)
+    src = [t.cuda() for t in inp]
+    dst = [torch.empty_like(s) for s in src]
+    vr.vr_allreduce_trees(src, dst, 4, 1 << 20, F32, SUM, 12, 512 * 1024, trees)
+    assert_status_ok()
+    assert_bits_equal([bits(d) for d in dst], want, "active trees")

@@ -209,3 +209,62 @@ def test_stepwise_ring_scratch_rules():
     step(FAKE[:4], FAKE_R[:4], 4, 0, F32, vr.VR_SUM, 1, 16, 0, 0)
     vr.vr_allreduce_tree_updown(FAKE[:4], FAKE_R[:4], 4, 0, F32, vr.VR_SUM, 1, 16, 1)
     assert vr.vr_launch_count() == before
+
+
+PATTERN_NAMES = {vr.VR_PATTERN_TREE: "tree", vr.VR_PATTERN_SPLIT_TREE: "split_tree",
+                 vr.VR_PATTERN_BALANCED_TREE: "balanced_tree"}
+
+
+@pytest.mark.parametrize("pattern", sorted(PATTERN_NAMES))
+def test_dtree_ex_matches_oracle(pattern):
+    rng = np.random.default_rng(40)
+    for L in (1, 2, 3, 4, 8):
+        if L == 1 and pattern != vr.VR_PATTERN_TREE:
+            continue
+        for n in range(1, 64 // L + 1, 3):
+            for nch in (1, 2, 5):
+                orders = [list(map(int, rng.permutation(L))) for _ in range(nch)]
+                for o in (None, orders):
+                    got = vr.vr_build_dtree_ex(n, L, nch, pattern, o)
+                    want = otopo.build_dtree(n, L, nch, pattern=PATTERN_NAMES[pattern], orders=o)
+                    R = n * L
+                    for c in range(nch):
+                        for r in range(R):
+                            g, w = got[c * R + r], want[c][r]
+                            assert (g.depth, g.up, list(g.down)) == (w.depth, w.up, w.down)
+
+
+def test_dtree_ex_argument_errors():
+    INV = vr.VR_ERR_INVALID_ARGUMENT
+    assert _err(vr.vr_build_dtree_ex, 4, 1, 1, vr.VR_PATTERN_SPLIT_TREE) == INV
+    assert _err(vr.vr_build_dtree_ex, 4, 2, 1, 7) == INV
+    assert _err(vr.vr_build_dtree_ex, 2, 3, 1, vr.VR_PATTERN_TREE, [[0, 0, 1]]) == INV
+    assert _err(vr.vr_build_dtree_ex, 2, 3, 1, vr.VR_PATTERN_TREE, [[0, 1, 3]]) == INV
+
+
+def test_allreduce_trees_rejects_invalid_trees():
+    INV, UNS = vr.VR_ERR_INVALID_ARGUMENT, vr.VR_ERR_UNSUPPORTED
+    F32, SUM = vr.VR_FLOAT32, vr.VR_SUM
+    good = vr.vr_build_dtree_ex(2, 2, 1)
+
+    def copy(ts):
+        return [vr.vr_tree_t(t.depth, t.up, (ctypes_int3)(*t.down)) for t in ts]
+    import ctypes
+    ctypes_int3 = ctypes.c_int * 3
+    before = vr.vr_launch_count()
+    bad = copy(good); bad[3].up = -1                 # two roots
+    assert _err(vr.vr_allreduce_trees, FAKE[:4], FAKE_R[:4], 4, 16, F32, SUM, 1, 16, bad) == INV
+    bad = copy(good); bad[0].down[2] = 3             # child whose up disagrees
+    assert _err(vr.vr_allreduce_trees, FAKE[:4], FAKE_R[:4], 4, 16, F32, SUM, 1, 16, bad) == INV
+    bad = copy(good); bad[1].up = 1                  # self loop
+    assert _err(vr.vr_allreduce_trees, FAKE[:4], FAKE_R[:4], 4, 16, F32, SUM, 1, 16, bad) == INV
+    bad = copy(good); bad[0].down[0], bad[0].down[1] = -1, bad[0].down[0]   # not compacted
+    assert _err(vr.vr_allreduce_trees, FAKE[:4], FAKE_R[:4], 4, 16, F32, SUM, 1, 16, bad) == INV
+    # seventeen distinct trees over seventeen channels: more than a call carries
+    many = []
+    for c in range(17):
+        order = [(c + i) % 17 for i in range(17)]
+        many += vr.vr_build_dtree_ex(1, 17, 1, vr.VR_PATTERN_TREE, [order])
+    assert _err(vr.vr_allreduce_trees, FAKE[:17], FAKE_R[:17], 17, 64, F32, SUM, 17, 16,
+                many) == UNS
+    assert vr.vr_launch_count() == before
