@@ -194,15 +194,15 @@ const void* pick_staged(int dtype, int mode, int op, int stack = 0) {
   }
 }
 
-// Register-path kernel; with at most 4 ranks a thread takes two units per
-// step (measured: one unit of 4 ranks keeps too few loads in flight).
+// Register-path kernel; at most 4 ranks take the variant compiled for 3 CTAs
+// per SM (VR_SMALL_RANKS=0, read per call, turns it off for tuning).
 const void* pick_kernel(int dtype, int mode, int op, bool vec, int stack = 0, int R = 64) {
-  // VR_PAIR_UNITS=0 (read per call) turns the two-unit step off, for tuning
-  const bool pair = vec && R <= 4 && mode != kReduceScatter && env_uint("VR_PAIR_UNITS", 1) != 0;
+  const bool small = vec && R <= 4 && stack <= 4 && mode != kReduceScatter &&
+                     env_uint("VR_SMALL_RANKS", 1) != 0;
   switch (dtype) {
-    case VR_FLOAT32: return kernel_ptr_f32(mode, op, vec, stack, pair);
-    case VR_FLOAT16: return kernel_ptr_f16(mode, op, vec, stack, pair);
-    case VR_BFLOAT16: return kernel_ptr_bf16(mode, op, vec, stack, pair);
+    case VR_FLOAT32: return kernel_ptr_f32(mode, op, vec, stack, small);
+    case VR_FLOAT16: return kernel_ptr_f16(mode, op, vec, stack, small);
+    case VR_BFLOAT16: return kernel_ptr_bf16(mode, op, vec, stack, small);
     default: return nullptr;
   }
 }

@@ -20,10 +20,10 @@ vr_result_t compile_fold(const vr_tree_t* tree, int R, FoldProg* prog);
 // `vec` selects the 16-byte vector path (all buffers and block offsets
 // 16-byte aligned), else the element path; `stack` is the deepest partial
 // stack of the tree programs (selects the 4- or 8-slot tree kernel).
-// `pair`: two units per thread step (vector path, at most 4 ranks).
-const void* kernel_ptr_f32(int mode, int op, bool vec, int stack, bool pair);
-const void* kernel_ptr_f16(int mode, int op, bool vec, int stack, bool pair);
-const void* kernel_ptr_bf16(int mode, int op, bool vec, int stack, bool pair);
+// `small`: the register-path variant for at most 4 ranks (vector path).
+const void* kernel_ptr_f32(int mode, int op, bool vec, int stack, bool small);
+const void* kernel_ptr_f16(int mode, int op, bool vec, int stack, bool small);
+const void* kernel_ptr_bf16(int mode, int op, bool vec, int stack, bool small);
 const void* kernel_ptr_allgather(bool vec);
 // TMA AllGather (16-byte aligned buffers): one warp per CTA.
 const void* kernel_ptr_allgather_tma();

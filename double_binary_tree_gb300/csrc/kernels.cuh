@@ -25,6 +25,7 @@ constexpr int kBlock = 256;  // threads per CTA of the register-path kernels
 #endif
 constexpr int kMinBlocksTree = 2;
 constexpr int kMinBlocksRing = VR_MIN_BLOCKS_RING;
+constexpr int kMinBlocksSmall = 3;
 
 // Rank pointers (and tree programs) copied to shared memory: they are indexed
 // by a runtime rank.
@@ -45,17 +46,18 @@ __device__ __forceinline__ void stage_args(const KArgs& a, const char** s_src, c
 }
 
 // AllReduce, ring or tree.  VEC: 16-byte units (aligned buffers), else one
-// element per unit.  P = 2 (few ranks): a thread takes two units per step and
-// computes both results before storing either, so the second unit's loads
-// are in flight together with the first's -- with 4 ranks or fewer one unit
-// alone keeps too few bytes in flight.
-template <typename T, int OP, int MODE, bool VEC, int S, int P>
-__global__ void __launch_bounds__(kBlock, MODE == kTreeAllReduce ? kMinBlocksTree : kMinBlocksRing)
+// element per unit.  SMALL (at most 4 ranks): a 4-load batch is enough, so
+// the kernel fits 3 CTAs per SM (85 registers) -- with few ranks a thread
+// has few loads in flight, and only more resident threads make up for it.
+template <typename T, int OP, int MODE, bool VEC, int S, bool SMALL>
+__global__ void __launch_bounds__(kBlock, SMALL ? kMinBlocksSmall
+                                               : (MODE == kTreeAllReduce ? kMinBlocksTree
+                                                                         : kMinBlocksRing))
     allreduce_kernel(const __grid_constant__ KArgs a) {
   constexpr int U = Ty<T>::U;
   constexpr int NV = VEC ? U : 1;
   constexpr long long E = sizeof(T);
-  static_assert(P == 1 || (P == 2 && VEC), "two units per step on the vector path only");
+  constexpr int B = SMALL ? 4 : kBatch;
   __shared__ const char* s_src[kMaxRanks];
   __shared__ char* s_dst[kMaxRanks];
   __shared__ __align__(16) FoldProg s_prog[kMaxProgs];
@@ -67,17 +69,17 @@ __global__ void __launch_bounds__(kBlock, MODE == kTreeAllReduce ? kMinBlocksTre
   const long long ub = units * blockIdx.x / gridDim.x;
   const long long ue = units * (blockIdx.x + 1) / gridDim.x;
   Cursor cur{0, -1, 0, 0, 0, 0, 0};
-
-  // one unit, whatever its shape
-  auto one = [&](long long u) {
+  for (long long u = ub + threadIdx.x; u < ue; u += blockDim.x) {
     const long long e0 = u * NV;
     const int n = (int)min((long long)NV, count - e0);
     seek<U, MODE>(a, e0, cur);
     if (n == NV && e0 + NV <= cur.hi) {
       const GlobalSrc src{s_src, e0 * E};
       typename Unit<T, NV>::Raw o;
-      if constexpr (MODE == kTreeAllReduce) o = tree_fold<T, OP, NV, S>(src, s_prog[cur.t], R);
-      else o = ring_fold<T, OP, NV>(src, R, cur.j);
+      if constexpr (MODE == kTreeAllReduce)
+        o = tree_fold<T, OP, NV, S, GlobalSrc, B>(src, s_prog[cur.t], R);
+      else
+        o = ring_fold<T, OP, NV, GlobalSrc, B>(src, R, cur.j);
       for (int r = 0; r < R; ++r) Unit<T, NV>::store(s_dst[r] + e0 * E, o);
     } else if (MODE == kRingAllReduce && VEC && n == NV && e0 + NV <= cur.loopEnd &&
                e0 + NV <= cur.hi + cur.q + (cur.j + 1 < cur.m ? 1 : 0)) {
@@ -94,40 +96,6 @@ __global__ void __launch_bounds__(kBlock, MODE == kTreeAllReduce ? kMinBlocksTre
         for (int r = 0; r < R; ++r) Unit<T, 1>::store(s_dst[r] + e * E, o);
       }
     }
-  };
-
-  for (long long u = ub + threadIdx.x; u < ue; u += P * blockDim.x) {
-    if constexpr (P == 2) {
-      const long long u2 = u + blockDim.x;
-      if (u2 < ue) {
-        const long long e0 = u * NV, e1 = u2 * NV;
-        seek<U, MODE>(a, e0, cur);
-        const bool f0 = count - e0 >= NV && e0 + NV <= cur.hi;
-        const int j0 = cur.j, t0 = cur.t;
-        seek<U, MODE>(a, e1, cur);
-        const bool f1 = count - e1 >= NV && e1 + NV <= cur.hi;
-        if (f0 && f1) {
-          const GlobalSrc s0{s_src, e0 * E}, s1{s_src, e1 * E};
-          typename Unit<T, NV>::Raw o0, o1;
-          if constexpr (MODE == kTreeAllReduce) {
-            o0 = tree_fold<T, OP, NV, S, GlobalSrc, 4>(s0, s_prog[t0], R);
-            o1 = tree_fold<T, OP, NV, S, GlobalSrc, 4>(s1, s_prog[cur.t], R);
-          } else {
-            o0 = ring_fold<T, OP, NV, GlobalSrc, 4>(s0, R, j0);
-            o1 = ring_fold<T, OP, NV, GlobalSrc, 4>(s1, R, cur.j);
-          }
-          for (int r = 0; r < R; ++r) {
-            Unit<T, NV>::store(s_dst[r] + e0 * E, o0);
-            Unit<T, NV>::store(s_dst[r] + e1 * E, o1);
-          }
-        } else {
-          one(u);
-          one(u2);
-        }
-        continue;
-      }
-    }
-    one(u);
   }
 }
 

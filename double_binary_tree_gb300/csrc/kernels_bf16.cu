@@ -7,26 +7,24 @@
 namespace vr {
 
 // Register-path kernels: `vec` = 16-byte units, else element units.
-const void* kernel_ptr_bf16(int mode, int op, bool vec, int stack, bool pair) {
-#define VR_PICK(OP, VEC, PAIR)                                                                   \
-  switch (mode) {                                                                                \
-    case kRingAllReduce:                                                                         \
-      return (const void*)allreduce_kernel<__nv_bfloat16, OP, kRingAllReduce, VEC, 4, (VEC && PAIR) ? 2 : 1>; \
-    case kTreeAllReduce:                                                                         \
-      if (PAIR)                                                                                  \
-        return (const void*)allreduce_kernel<__nv_bfloat16, OP, kTreeAllReduce, VEC, 4, (VEC && PAIR) ? 2 : 1>; \
-      return stack <= 4 ? (const void*)allreduce_kernel<__nv_bfloat16, OP, kTreeAllReduce, VEC, 4, 1>     \
-                        : (const void*)allreduce_kernel<__nv_bfloat16, OP, kTreeAllReduce, VEC, 8, 1>;    \
-    case kReduceScatter: return (const void*)reduce_scatter_kernel<__nv_bfloat16, OP, VEC>;               \
-    default: return nullptr;                                                                     \
+// Register-path kernels: `vec` = 16-byte units, else element units;
+// `small`: the variant for at most 4 ranks.
+const void* kernel_ptr_bf16(int mode, int op, bool vec, int stack, bool small) {
+#define VR_PICK(OP, VEC, SMALL)                                                                   \
+  switch (mode) {                                                                                 \
+    case kRingAllReduce:                                                                          \
+      return (const void*)allreduce_kernel<__nv_bfloat16, OP, kRingAllReduce, VEC, 4, SMALL>;              \
+    case kTreeAllReduce:                                                                          \
+      return stack <= 4 ? (const void*)allreduce_kernel<__nv_bfloat16, OP, kTreeAllReduce, VEC, 4, SMALL>  \
+                        : (const void*)allreduce_kernel<__nv_bfloat16, OP, kTreeAllReduce, VEC, 8, false>; \
+    case kReduceScatter: return (const void*)reduce_scatter_kernel<__nv_bfloat16, OP, VEC>;                \
+    default: return nullptr;                                                                      \
   }
-  // two units per step: vector path, at most 4 ranks (trees of <= 4 ranks
-  // fold with at most 4 partials)
   if (op == VR_SUM) {
-    if (vec && pair) { VR_PICK(VR_SUM, true, true) }
+    if (vec && small) { VR_PICK(VR_SUM, true, true) }
     else if (vec) { VR_PICK(VR_SUM, true, false) } else { VR_PICK(VR_SUM, false, false) }
   } else {
-    if (vec && pair) { VR_PICK(VR_MAX, true, true) }
+    if (vec && small) { VR_PICK(VR_MAX, true, true) }
     else if (vec) { VR_PICK(VR_MAX, true, false) } else { VR_PICK(VR_MAX, false, false) }
   }
 #undef VR_PICK
