@@ -565,3 +565,51 @@ def test_pattern_invariants(pattern):
                        topology.build_dtree(n, L, 3, pattern=pattern, orders=orders)):
                 for tr in ch:
                     _check_invariants(tr, n * L)
+
+
+# -------------------------------------------------------------- cost model
+def test_cost_model_step_counts_and_traffic():
+    from oracle import costmodel as cm
+    # [Interview] Figure 2 / "推导": n = 8: ring 14 stages, tree 2 log2 8 = 6;
+    # n = 1024: 2046 and about 20; ring traffic 2(n-1)/n S, 1.5 S at n = 4
+    tr8 = topology.build_dtree(8, 1, 1)[0]
+    assert cm.ring_terms(8, 1)[0] == 14
+    assert cm.tree_terms(topology.exact_depth(tr8), 1)[0] == 6
+    assert cm.ring_terms(1024, 1)[0] == 2046
+    assert cm.tree_terms(topology.exact_depth(topology.build_dtree(1024, 1, 1)[0]), 1)[0] == 20
+    assert cm.ring_terms(4, 64)[1] == 96.0 and cm.tree_terms(2, 64)[1] == 128.0
+    # [Course13] "理想成本模型": a 4-rank chain (depth N-1 = 3) has no latency
+    # advantage over the ring: 2D = 6 = 2(N-1)
+    chain = topology.build_dtree(1, 4, 1)[0]
+    assert cm.tree_terms(topology.exact_depth(chain), 1)[0] == cm.ring_terms(4, 1)[0]
+
+
+def test_cost_model_crossover_matches_search():
+    from oracle import costmodel as cm
+    rng = np.random.default_rng(31)
+    for _ in range(200):
+        N = int(rng.integers(2, 65))
+        D = int(rng.integers(1, 8))
+        ring = (float(rng.uniform(0.1, 10)), float(rng.uniform(1e-6, 1e-3)))
+        tree = (float(rng.uniform(0.1, 10)), float(rng.uniform(1e-6, 1e-3)))
+        m = cm.crossover(N, D, ring, tree)
+        grid = np.geomspace(1e-3, 1e12, 4000)
+        diff = np.array([cm.t_ring(N, x, *ring) - cm.t_tree(D, x, *tree) for x in grid])
+        sign_change = np.nonzero(np.sign(diff[1:]) != np.sign(diff[:-1]))[0]
+        if m is None:
+            assert sign_change.size == 0
+        else:
+            assert sign_change.size == 1
+            lo, hi = grid[sign_change[0]], grid[sign_change[0] + 1]
+            assert lo <= m * (1 + 1e-9) and m <= hi * (1 + 1e-9)
+            # the choice flips at the crossover
+            assert cm.select(N, D, m * 0.5, ring, tree) != cm.select(N, D, m * 2, ring, tree)
+
+
+def test_cost_model_fit_recovers_parameters():
+    from oracle import costmodel as cm
+    stages = [6] * 10 + [14] * 10
+    traffic = list(np.geomspace(8, 1e9, 10)) * 2
+    times = [cm.predict(s, b, 2.5, 3e-4) for s, b in zip(stages, traffic)]
+    a, ib = cm.fit(stages, traffic, times)
+    assert abs(a - 2.5) < 1e-9 and abs(ib - 3e-4) < 1e-12
