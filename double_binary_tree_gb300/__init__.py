@@ -20,7 +20,7 @@ VR_SUCCESS, VR_ERR_INVALID_ARGUMENT, VR_ERR_UNSUPPORTED = 0, 1, 2
 VR_ERR_CUDA, VR_ERR_TIMEOUT, VR_ERR_INTERNAL = 3, 4, 5
 VR_FLOAT32, VR_FLOAT16, VR_BFLOAT16 = 0, 1, 2
 VR_SUM, VR_MAX = 0, 1
-VR_ALGO_RING, VR_ALGO_TREE = 0, 1
+VR_ALGO_RING, VR_ALGO_TREE, VR_ALGO_AUTO = 0, 1, 2
 VR_PATTERN_TREE, VR_PATTERN_SPLIT_TREE, VR_PATTERN_BALANCED_TREE = 0, 1, 2
 VR_MAX_RANKS = 64
 VR_MAX_CHANNELS = 64
@@ -32,6 +32,10 @@ class VrError(RuntimeError):
     def __init__(self, code, where):
         self.code = code
         super().__init__("%s: %s (%d)" % (where, vr_get_error_string(code), code))
+
+
+class vr_cost_model_t(ctypes.Structure):
+    _fields_ = [("alphaUs", ctypes.c_double * 2), ("usPerByte", ctypes.c_double * 2)]
 
 
 class vr_tree_t(ctypes.Structure):
@@ -55,6 +59,9 @@ _SIGNATURES = {
     "vr_ring_stepwise_scratch_bytes": (S, [S, I]),
     "vr_allreduce_ring_stepwise": (I, [PP, PP, I, S, I, I, I, S, VP, S, VP]),
     "vr_allreduce_ring_stepwise_noalloc": (I, [PP, PP, I, S, I, I, I, S, VP]),
+    "vr_predict_us": (I, [I, I, I, S, P(vr_cost_model_t), P(ctypes.c_double)]),
+    "vr_select_algo": (I, [I, I, S, P(vr_cost_model_t), P(I)]),
+    "vr_set_cost_model": (I, [P(vr_cost_model_t)]),
     "vr_stream_status": (I, [VP]),
     "vr_launch_count": (ctypes.c_ulonglong, []),
     "vr_debug_stall_next": (I, [ctypes.c_longlong]),
@@ -223,6 +230,38 @@ def vr_allreduce_ring_stepwise_noalloc(sendbufs, recvbufs, R, count, dtype, op, 
                                                    dtype, op, nChannels, chunkBytes,
                                                    _stream(stream)),
            "vr_allreduce_ring_stepwise_noalloc")
+
+
+def _model(m):
+    """None, a vr_cost_model_t, or ((alpha_ring, alpha_tree), (b_ring, b_tree))."""
+    if m is None or isinstance(m, vr_cost_model_t):
+        return m
+    (a0, a1), (b0, b1) = m
+    return vr_cost_model_t((ctypes.c_double * 2)(a0, a1), (ctypes.c_double * 2)(b0, b1))
+
+
+def vr_predict_us(algo, R, localRanks, bytesPerRank, model=None):
+    out = ctypes.c_double()
+    m = _model(model)
+    _check(_L().vr_predict_us(algo, R, localRanks, bytesPerRank,
+                              ctypes.byref(m) if m is not None else None, ctypes.byref(out)),
+           "vr_predict_us")
+    return out.value
+
+
+def vr_select_algo(R, localRanks, bytesPerRank, model=None):
+    out = ctypes.c_int()
+    m = _model(model)
+    _check(_L().vr_select_algo(R, localRanks, bytesPerRank,
+                               ctypes.byref(m) if m is not None else None, ctypes.byref(out)),
+           "vr_select_algo")
+    return out.value
+
+
+def vr_set_cost_model(model=None):
+    m = _model(model)
+    _check(_L().vr_set_cost_model(ctypes.byref(m) if m is not None else None),
+           "vr_set_cost_model")
 
 
 def vr_stream_status(stream=None):

@@ -5,6 +5,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstdlib>
+#include <cmath>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -30,6 +31,22 @@ std::map<std::pair<const void*, int>, int> g_occupancy;          // (kernel, dev
 std::map<std::pair<int, int>, std::array<FoldProg, 2>> g_progs;  // (nNodes, localRanks)
 std::map<std::pair<const void*, int>, int> g_smemSet;            // (kernel, device) -> bytes
 std::atomic<long long> g_stallNext{-1};                          // test hook
+
+// The alpha-beta cost model: built-in constants fitted on GB300 (4 ranks,
+// 8 B .. 256 MiB per rank), replaceable through vr_set_cost_model.
+const vr_cost_model_t kBuiltinModel = {{0.58989, 0.79715}, {1.17824e-6, 8.81738e-7}};
+vr_cost_model_t g_model = kBuiltinModel;
+
+// Exact depth (edges from the root to the deepest leaf) of one tree.
+int exact_depth(const vr_tree_t* tr, int R) {
+  int worst = 0;
+  for (int r = 0; r < R; ++r) {
+    int d = 0;
+    for (int v = r; tr[v].up >= 0 && d <= R; v = tr[v].up) ++d;
+    worst = std::max(worst, d);
+  }
+  return worst;
+}
 
 // Tuning overrides read from the environment (0 when unset).
 unsigned env_uint(const char* name, unsigned dflt) {
@@ -194,10 +211,13 @@ const void* pick_staged(int dtype, int mode, int op, int stack = 0) {
   }
 }
 
-// Register-path kernel; at most 4 ranks take the variant compiled for 3 CTAs
-// per SM (VR_SMALL_RANKS=0, read per call, turns it off for tuning).
+// Register-path kernel; fp32 with at most 4 ranks takes the variant compiled
+// for 3 CTAs per SM (1.2-1.5x faster from 16 MiB per rank; slower for 16-bit
+// types, which keep the general kernel).  VR_SMALL_RANKS=0, read per call,
+// turns it off for tuning.
 const void* pick_kernel(int dtype, int mode, int op, bool vec, int stack = 0, int R = 64) {
-  const bool small = vec && R <= 4 && stack <= 4 && mode != kReduceScatter &&
+  const bool small = dtype == VR_FLOAT32 && vec && R <= 4 && stack <= 4 &&
+                     mode != kReduceScatter &&
                      env_uint("VR_SMALL_RANKS", 1) != 0;
   switch (dtype) {
     case VR_FLOAT32: return kernel_ptr_f32(mode, op, vec, stack, small);
@@ -392,6 +412,10 @@ vr_result_t vr_ring_block(size_t count, vr_dtype_t dtype, int R, int nChannels,
 vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, int R,
                             size_t count, vr_dtype_t dtype, vr_op_t op, vr_algo_t algo,
                             int nChannels, size_t chunkBytes, int localRanks, void* stream) {
+  if (algo == VR_ALGO_AUTO && valid_common(R, dtype, nChannels, chunkBytes) && localRanks >= 1 &&
+      R % localRanks == 0 &&
+      vr_select_algo(R, localRanks, count * elem_size(dtype), nullptr, &algo) != VR_SUCCESS)
+    return VR_ERR_INTERNAL;
   if (!valid_common(R, dtype, nChannels, chunkBytes) || (op != VR_SUM && op != VR_MAX) ||
       (algo != VR_ALGO_RING && algo != VR_ALGO_TREE) || localRanks < 1 || R % localRanks)
     return VR_ERR_INVALID_ARGUMENT;
@@ -422,6 +446,51 @@ vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, 
   const long long NV = vec ? kGrainBytes / (long long)E : 1;
   return launch(pick_kernel(dtype, mode, op, vec, stack, R), a,
                 ((long long)count + NV - 1) / NV, stream);
+}
+
+vr_result_t vr_predict_us(vr_algo_t algo, int R, int localRanks, size_t bytesPerRank,
+                          const vr_cost_model_t* model, double* us) {
+  if ((algo != VR_ALGO_RING && algo != VR_ALGO_TREE) || R < 1 || R > kMaxRanks ||
+      localRanks < 1 || R % localRanks || !us)
+    return VR_ERR_INVALID_ARGUMENT;
+  vr_cost_model_t m;
+  {
+    std::lock_guard<std::mutex> g(g_mu);
+    m = model ? *model : g_model;
+  }
+  const double M = (double)bytesPerRank, N = (double)R;
+  if (algo == VR_ALGO_RING) {
+    *us = 2.0 * (N - 1) * m.alphaUs[0] + (2.0 * (N - 1) / N * M) * m.usPerByte[0];
+    return VR_SUCCESS;
+  }
+  vr_tree_t trees[2 * kMaxRanks];
+  vr_result_t e = build_dtree(R / localRanks, localRanks, 2, trees);
+  if (e != VR_SUCCESS) return e;
+  const int D = std::max(exact_depth(trees, R), exact_depth(trees + R, R));
+  *us = 2.0 * D * m.alphaUs[1] + (2.0 * M) * m.usPerByte[1];
+  return VR_SUCCESS;
+}
+
+vr_result_t vr_select_algo(int R, int localRanks, size_t bytesPerRank,
+                           const vr_cost_model_t* model, vr_algo_t* algo) {
+  if (!algo) return VR_ERR_INVALID_ARGUMENT;
+  double tr = 0, tt = 0;
+  vr_result_t e = vr_predict_us(VR_ALGO_RING, R, localRanks, bytesPerRank, model, &tr);
+  if (e == VR_SUCCESS) e = vr_predict_us(VR_ALGO_TREE, R, localRanks, bytesPerRank, model, &tt);
+  if (e != VR_SUCCESS) return e;
+  *algo = tr <= tt ? VR_ALGO_RING : VR_ALGO_TREE;
+  return VR_SUCCESS;
+}
+
+vr_result_t vr_set_cost_model(const vr_cost_model_t* model) {
+  if (model)
+    for (int i = 0; i < 2; ++i)
+      if (!(model->alphaUs[i] >= 0 && model->usPerByte[i] >= 0) ||
+          !std::isfinite(model->alphaUs[i]) || !std::isfinite(model->usPerByte[i]))
+        return VR_ERR_INVALID_ARGUMENT;
+  std::lock_guard<std::mutex> g(g_mu);
+  g_model = model ? *model : kBuiltinModel;
+  return VR_SUCCESS;
 }
 
 vr_result_t vr_allreduce(const void* const* sendbufs, void* const* recvbufs, int R, size_t count,

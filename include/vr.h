@@ -54,7 +54,9 @@ typedef enum {
 
 typedef enum { VR_FLOAT32 = 0, VR_FLOAT16 = 1, VR_BFLOAT16 = 2 } vr_dtype_t;
 typedef enum { VR_SUM = 0, VR_MAX = 1 } vr_op_t;
-typedef enum { VR_ALGO_RING = 0, VR_ALGO_TREE = 1 } vr_algo_t;
+/* VR_ALGO_AUTO (AllReduce only): ring or tree, whichever the cost model
+ * (vr_select_algo) predicts faster. */
+typedef enum { VR_ALGO_RING = 0, VR_ALGO_TREE = 1, VR_ALGO_AUTO = 2 } vr_algo_t;
 
 #define VR_MAX_RANKS 64
 #define VR_MAX_CHANNELS 64
@@ -151,6 +153,7 @@ vr_result_t vr_ring_block(size_t count, vr_dtype_t dtype, int R, int nChannels,
  *        on the channel's tree every rank folds its local input with its
  *        children's partials in down[] order and passes the result up; the
  *        root's value is broadcast down to all ranks.  localRanks = 1 here.
+ *   AUTO the one of the two that vr_select_algo predicts faster.
  * nChannels in [1, VR_MAX_CHANNELS] splits the message (vr_partition);
  * chunkBytes (a positive multiple of 16) is the per-rank chunk C of a ring
  * loop and the chunk of a tree channel.
@@ -282,6 +285,36 @@ vr_result_t vr_allreduce_ring_stepwise(const void* const* sendbufs, void* const*
 vr_result_t vr_allreduce_ring_stepwise_noalloc(const void* const* sendbufs, void* const* recvbufs,
                                                int R, size_t count, vr_dtype_t dtype, vr_op_t op,
                                                int nChannels, size_t chunkBytes, void* stream);
+
+/* ---------------------------------------------------------- cost model
+ * The pages' alpha-beta model ([Course13] "理想成本模型"; [Interview]
+ * "推导 / 关键公式"), with N ranks, tree depth D (the deeper of the two
+ * trees, edges from root to deepest leaf) and M bytes per rank:
+ *   T_ring = 2(N-1) * alpha[0] + 2(N-1)/N * M * usPerByte[0]
+ *   T_tree = 2D     * alpha[1] + 2 M       * usPerByte[1]
+ * in microseconds.  The built-in model is fitted (least squares of relative
+ * error) to the ring and tree times this library measures on GB300 for
+ * 4 ranks, 8 B .. 256 MiB per rank. */
+typedef struct {
+  double alphaUs[2];    /* per dependent stage: [0] ring, [1] tree */
+  double usPerByte[2];  /* per byte of the traffic term: [0] ring, [1] tree */
+} vr_cost_model_t;
+
+/* Predicted time of an AllReduce (algo RING or TREE) over R ranks in nodes of
+ * localRanks, bytesPerRank each, under `model` (NULL: the current model).
+ * Errors: VR_ERR_INVALID_ARGUMENT for a bad algo, R, localRanks or NULL us. */
+vr_result_t vr_predict_us(vr_algo_t algo, int R, int localRanks, size_t bytesPerRank,
+                          const vr_cost_model_t* model, double* us);
+
+/* The algorithm with the smaller prediction (RING on a tie); what
+ * VR_ALGO_AUTO uses with model NULL.  Errors as vr_predict_us. */
+vr_result_t vr_select_algo(int R, int localRanks, size_t bytesPerRank,
+                           const vr_cost_model_t* model, vr_algo_t* algo);
+
+/* Installs `model` as the current model for this process (NULL restores the
+ * built-in one), e.g. one fitted to other hardware.  Errors:
+ * VR_ERR_INVALID_ARGUMENT for negative or non-finite entries. */
+vr_result_t vr_set_cost_model(const vr_cost_model_t* model);
 
 /* ------------------------------------------------------------- status */
 

@@ -435,3 +435,28 @@ def test_active_trees_of_the_pages_on_gpu():
     vr.vr_allreduce_trees(src, dst, 4, 1 << 20, F32, SUM, 12, 512 * 1024, trees)
     assert_status_ok()
     assert_bits_equal([bits(d) for d in dst], want, "active trees")
+
+
+# ------------------------------------------------------- VR_ALGO_AUTO
+def test_auto_runs_the_algorithm_the_oracle_cost_model_picks():
+    """With a model whose crossover sits near 2.8 MB (cheap tree stages,
+    cheap ring bytes), AUTO takes the tree below it and the ring above; the
+    output equals the oracle of the algorithm the oracle's model selects."""
+    from oracle import costmodel
+    ring_m, tree_m = (5.0, 1e-5), (1.0, 2e-5)
+    R = 8
+    trees = topology.build_dtree(R, 1, 2)
+    D = max(topology.exact_depth(trees[0]), topology.exact_depth(trees[1]))
+    vr.vr_set_cost_model(((ring_m[0], tree_m[0]), (ring_m[1], tree_m[1])))
+    try:
+        picked = set()
+        for count, seed in ((3000, 11), (1 << 20, 12)):
+            inp = workloads.generate(R, count, F32, "normal", seed)
+            algo = costmodel.select(R, D, count * 4, ring_m, tree_m)
+            picked.add(algo)
+            _, want = expect_allreduce(inp, F32, SUM, RING if algo == "ring" else TREE, 4, 1 << 16)
+            got = run_allreduce(inp, F32, SUM, vr.VR_ALGO_AUTO, 4, 1 << 16)
+            assert_bits_equal(got, want, "AUTO(%s)" % algo)
+        assert picked == {"ring", "tree"}
+    finally:
+        vr.vr_set_cost_model(None)

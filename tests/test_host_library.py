@@ -122,6 +122,12 @@ def test_argument_errors_are_synchronous():
     assert _err(ar, FAKE[:2], [FAKE[0] + 4, FAKE_R[1]], 2, 4, F32, SUM, RING, 1, 16) == INV
     assert _err(vr.vr_allreduce_ex, FAKE[:8], FAKE_R[:8], 8, 16, F32, SUM, TREE, 1, 16, 3) == INV
     assert _err(vr.vr_allreduce_ex, FAKE[:8], FAKE_R[:8], 8, 16, F32, SUM, TREE, 1, 16, 0) == INV
+    # AUTO resolves only for valid arguments, and is AllReduce-only
+    AUTO = vr.VR_ALGO_AUTO
+    assert _err(vr.vr_allreduce_ex, FAKE[:8], FAKE_R[:8], 8, 16, F32, SUM, AUTO, 1, 16, 3) == INV
+    assert _err(ar, FAKE[:4], FAKE_R[:4], 4, 16, F32, SUM, AUTO, 0, 16) == INV
+    assert _err(ar, FAKE[:3] + [0], FAKE_R[:4], 4, 16, F32, SUM, AUTO, 1, 16) == INV
+    assert _err(vr.vr_reduce_scatter, FAKE[:4], FAKE_R[:4], 4, 16, F32, SUM, AUTO, 1, 16) == INV
     # tree is AllReduce-only
     assert _err(vr.vr_reduce_scatter, FAKE[:4], FAKE_R[:4], 4, 16, F32, SUM, TREE, 1, 16) == UNS
     assert _err(vr.vr_allgather, FAKE[:4], FAKE_R[:4], 4, 16, F32, TREE, 1, 16) == UNS
@@ -134,6 +140,7 @@ def test_argument_errors_are_synchronous():
     vr.vr_allreduce(FAKE[:4], FAKE_R[:4], 4, 0, F32, SUM, RING, 1, 16)
     vr.vr_reduce_scatter(FAKE[:4], FAKE_R[:4], 4, 0, F32, SUM, RING, 1, 16)
     vr.vr_allgather(FAKE[:4], FAKE_R[:4], 4, 0, F32, RING, 1, 16)
+    vr.vr_allreduce(FAKE[:4], FAKE_R[:4], 4, 0, F32, SUM, AUTO, 1, 16)
     assert vr.vr_launch_count() == before
 
 
@@ -268,3 +275,69 @@ def test_allreduce_trees_rejects_invalid_trees():
     assert _err(vr.vr_allreduce_trees, FAKE[:17], FAKE_R[:17], 17, 64, F32, SUM, 17, 16,
                 many) == UNS
     assert vr.vr_launch_count() == before
+
+
+# ------------------------------------------------------------ cost model
+from oracle import costmodel as ocost  # noqa: E402
+
+# The library's built-in constants (fitted on GB300, 4 ranks); the oracle is
+# evaluated with the same numbers so that only the formulas are compared.
+BUILTIN = ((0.58989, 0.79715), (1.17824e-6, 8.81738e-7))
+# Cheap tree stages, cheap ring bytes (the pages' picture: the tree for small
+# messages, the ring for large ones): a crossover exists.
+OTHER = ((5.0, 1.0), (1e-5, 2e-5))
+
+
+def _oracle_depth(R, L):
+    trees = otopo.build_dtree(R // L, L, 2)
+    return max(otopo.exact_depth(trees[0]), otopo.exact_depth(trees[1]))
+
+
+@pytest.mark.parametrize("R,L", [(1, 1), (2, 1), (4, 1), (7, 1), (8, 1), (16, 4), (64, 8), (48, 3)])
+@pytest.mark.parametrize("model", [None, OTHER])
+def test_predict_matches_oracle(R, L, model):
+    (a0, a1), (b0, b1) = model or BUILTIN
+    D = _oracle_depth(R, L)
+    for M in (0, 8, 4096, 1 << 20, 64 << 20, 3 << 30):
+        ring = vr.vr_predict_us(vr.VR_ALGO_RING, R, L, M, model)
+        tree = vr.vr_predict_us(vr.VR_ALGO_TREE, R, L, M, model)
+        assert ring == pytest.approx(ocost.t_ring(R, M, a0, b0), rel=1e-12, abs=1e-12)
+        assert tree == pytest.approx(ocost.t_tree(D, M, a1, b1), rel=1e-12, abs=1e-12)
+        want = ocost.select(R, D, M, (a0, b0), (a1, b1))
+        got = vr.vr_select_algo(R, L, M, model)
+        assert got == (vr.VR_ALGO_RING if want == "ring" else vr.VR_ALGO_TREE)
+
+
+def test_select_switches_at_the_oracle_crossover():
+    """The tree wins small messages and the ring large ones; the switch sits
+    at the closed-form crossover."""
+    R, L = 8, 1
+    (a0, a1), (b0, b1) = OTHER
+    m = ocost.crossover(R, _oracle_depth(R, L), (a0, b0), (a1, b1))
+    assert m is not None and m > 0
+    assert vr.vr_select_algo(R, L, int(m * 0.9), OTHER) == vr.VR_ALGO_TREE
+    assert vr.vr_select_algo(R, L, int(m * 1.1), OTHER) == vr.VR_ALGO_RING
+
+
+def test_set_cost_model_replaces_the_default():
+    try:
+        vr.vr_set_cost_model(OTHER)
+        assert vr.vr_predict_us(vr.VR_ALGO_RING, 8, 1, 0) == pytest.approx(14 * 5.0)
+        vr.vr_set_cost_model(None)
+        assert vr.vr_predict_us(vr.VR_ALGO_RING, 8, 1, 0) == pytest.approx(14 * BUILTIN[0][0])
+        for bad in (((-1.0, 0.0), (0.0, 0.0)), ((0.0, float("nan")), (0.0, 0.0)),
+                    ((0.0, 0.0), (float("inf"), 0.0))):
+            with pytest.raises(vr.VrError):
+                vr.vr_set_cost_model(bad)
+    finally:
+        vr.vr_set_cost_model(None)
+
+
+def test_cost_model_argument_errors():
+    for args in ((vr.VR_ALGO_AUTO, 8, 1, 0), (vr.VR_ALGO_RING, 0, 1, 0),
+                 (vr.VR_ALGO_RING, 65, 1, 0), (vr.VR_ALGO_TREE, 8, 3, 0),
+                 (vr.VR_ALGO_TREE, 8, 0, 0)):
+        with pytest.raises(vr.VrError):
+            vr.vr_predict_us(*args)
+    with pytest.raises(vr.VrError):
+        vr.vr_select_algo(6, 4, 0)
