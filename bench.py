@@ -58,6 +58,23 @@ THROTTLE_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_p
                  0x100: "display_clock_setting"}
 
 
+def max_over_ranks(torch, value, device):
+    """The largest of every rank's `value`: the job takes as long as its
+    slowest replica.  Identity without an initialised process group."""
+    dist = torch.distributed
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world, nbytes_per_replica, steps, ms):
+    """Whole-job throughput: the work of all `world` replicas over the
+    slowest replica's time."""
+    return world * nbytes_per_replica * steps / (ms * 1e-3) / 1e9
+
+
 def elem_size(dtype):
     return 4 if dtype == 0 else 2
 
@@ -197,14 +214,10 @@ def gpu_arm(args, rank, world, local_rank):
         launches = vr.vr_launch_count() - launches0
     if vr.vr_stream_status(stream) != 0:
         raise RuntimeError("device status error in the timed region")
-    ms = start.elapsed_time(stop)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(torch, start.elapsed_time(stop), dev)
     ms_per_step = ms / args.steps
     nbytes = ar_bytes(R, count, dtype)
-    value = world * nbytes * args.steps / (ms * 1e-3) / 1e9
+    value = job_gbs(world, nbytes, args.steps, ms)
     per_gpu = nbytes / (ms_per_step * 1e-3) / 1e9
     S = count * elem_size(dtype)
     algbw = S / (ms_per_step * 1e-3) / 1e9
@@ -273,14 +286,10 @@ def e2e_arm(args, vr, torch, inputs, dev, stream, world):
         step()
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(torch, a.elapsed_time(b), dev)
     nbytes = ar_bytes(R, count, dtype)
     io = R * count * elem_size(dtype)
-    return {"value": round(world * nbytes * steps / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+    return {"value": round(job_gbs(world, nbytes, steps, ms), 1), "unit": "GB/s",
             "h2d_bytes_per_step": io, "d2h_bytes_per_step": io, "steps": steps,
             "ms_per_step": round(ms / steps, 4)}
 

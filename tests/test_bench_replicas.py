@@ -1,0 +1,67 @@
+"""bench.py's multi-GPU path on the CPU: N independent replicas, timed by the
+slowest rank, the job value summing the work of every replica.  World size 2
+over gloo (the GPU run uses NCCL for the same two calls)."""
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from tests.conftest import ROOT  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, times, out):
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    torch.distributed.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = bench.max_over_ranks(torch, times[rank], "cpu")
+        out.put((rank, ms, bench.job_gbs(world, 1e9, 10, ms)))
+    finally:
+        torch.distributed.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_value_world_2():
+    ctx = torch.multiprocessing.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    times = [12.5, 20.0]
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, times, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, ms, gbs in got:
+        assert ms == 20.0                       # the slowest replica
+        assert gbs == pytest.approx(2 * 1e9 * 10 / 20e-3 / 1e9)
+
+
+def test_single_process_is_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(torch, 3.25, "cpu") == 3.25
+    assert bench.job_gbs(1, 2e9, 5, 1000.0) == pytest.approx(10.0)
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    """Under torchrun only rank 0 runs and prints the reference arm."""
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], env=env, capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
