@@ -14,7 +14,7 @@ Rank 0 prints one JSON line.  It also carries algbw/busbw, a roofline object
 for the kernel, the CPU oracle timed on the host cores (cpu_baseline), an
 end-to-end figure through the same C ABI with the inputs copied in from
 pinned host memory and every rank's result copied back inside the timed
-region (e2e), SM clocks sampled during the timed region, and the other
+region, pipelined in pieces by vr_allreduce_host (e2e), SM clocks sampled during the timed region, and the other
 workloads (tree bf16 R=8 / R=7, hierarchical fp16 R=64 ring / tree / Sum /
 Max, ReduceScatter, AllGather) timed the same way under "workloads".
 
@@ -257,25 +257,22 @@ def gpu_arm(args, rank, world, local_rank):
 
 
 def e2e_arm(args, vr, torch, inputs, dev, stream, world):
-    """Same AllReduce through the C ABI, each step copying the R inputs in
-    from pinned host memory and every rank's result back out."""
+    """The same AllReduce through the C ABI's host-buffer entry point: each
+    step copies the R inputs in from pinned host memory, folds, and copies
+    every rank's result back out, pipelined in pieces (vr_allreduce_host)."""
     W = WORKLOAD
     R, count, dtype = W["R"], W["count"], W["dtype"]
     host_in = [t.pin_memory() for t in inputs]
     host_out = [torch.empty_like(t).pin_memory() for t in inputs]
-    src = [torch.empty_like(t, device=dev) for t in inputs]
-    dst = [torch.empty_like(t, device=dev) for t in inputs]
+    work = [torch.empty_like(t, device=dev) for t in inputs]
 
     def step():
-        for h, d in zip(host_in, src):
-            d.copy_(h, non_blocking=True)
-        vr.vr_allreduce(src, dst, R, count, dtype, W["op"], W["algo"], W["n_channels"],
-                        W["chunk_bytes"], stream)
-        for d, h in zip(dst, host_out):
-            h.copy_(d, non_blocking=True)
+        vr.vr_allreduce_host(host_in, host_out, R, count, dtype, W["op"], W["algo"],
+                             W["n_channels"], W["chunk_bytes"], W["local_ranks"], work,
+                             args.piece_bytes, stream)
 
     steps = max(1, min(args.steps, args.e2e_steps))
-    for _ in range(2):
+    for _ in range(3):
         step()
     torch.cuda.synchronize()
     if world > 1:
@@ -286,12 +283,16 @@ def e2e_arm(args, vr, torch, inputs, dev, stream, world):
         step()
     b.record(stream)
     torch.cuda.synchronize()
+    if vr.vr_stream_status(stream) != 0:
+        raise RuntimeError("device status error in the end-to-end region")
     ms = max_over_ranks(torch, a.elapsed_time(b), dev)
     nbytes = ar_bytes(R, count, dtype)
     io = R * count * elem_size(dtype)
     return {"value": round(job_gbs(world, nbytes, steps, ms), 1), "unit": "GB/s",
             "h2d_bytes_per_step": io, "d2h_bytes_per_step": io, "steps": steps,
-            "ms_per_step": round(ms / steps, 4)}
+            "ms_per_step": round(ms / steps, 4),
+            "api": "vr_allreduce_host (pinned host buffers, %s per rank per piece)" % (
+                "%d MiB" % ((args.piece_bytes or vr.VR_HOST_PIECE_BYTES) >> 20))}
 
 
 def time_calls(torch, stream, call, sets, iters):
@@ -568,6 +569,8 @@ def main():
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--piece-bytes", type=int, default=0,
+                   help="vr_allreduce_host piece size per rank (0: the library default)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--quick", action="store_true", help="skip the other workloads")

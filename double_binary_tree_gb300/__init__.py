@@ -25,6 +25,7 @@ VR_PATTERN_TREE, VR_PATTERN_SPLIT_TREE, VR_PATTERN_BALANCED_TREE = 0, 1, 2
 VR_MAX_RANKS = 64
 VR_MAX_CHANNELS = 64
 VR_NOALLOC_SCRATCH_BYTES = 8 << 20
+VR_HOST_PIECE_BYTES = 8 << 20
 ELEM_SIZE = {VR_FLOAT32: 4, VR_FLOAT16: 2, VR_BFLOAT16: 2}
 
 
@@ -52,6 +53,7 @@ _SIGNATURES = {
     "vr_ring_block": (I, [S, I, I, I, S, S, P(I), P(I)]),
     "vr_allreduce": (I, [PP, PP, I, S, I, I, I, I, S, VP]),
     "vr_allreduce_ex": (I, [PP, PP, I, S, I, I, I, I, S, I, VP]),
+    "vr_allreduce_host": (I, [PP, PP, I, S, I, I, I, I, S, I, PP, S, VP]),
     "vr_allreduce_trees": (I, [PP, PP, I, S, I, I, I, S, P(vr_tree_t), VP]),
     "vr_reduce_scatter": (I, [PP, PP, I, S, I, I, I, I, S, VP]),
     "vr_allgather": (I, [PP, PP, I, S, I, I, I, S, VP]),
@@ -180,6 +182,16 @@ def vr_allreduce_ex(sendbufs, recvbufs, R, count, dtype, op, algo, nChannels, ch
     _check(_L().vr_allreduce_ex(_ptrs(sendbufs), _ptrs(recvbufs), R, count, dtype, op, algo,
                                 nChannels, chunkBytes, localRanks, _stream(stream)),
            "vr_allreduce_ex")
+
+
+def vr_allreduce_host(sendbufs, recvbufs, R, count, dtype, op, algo, nChannels, chunkBytes,
+                      localRanks, workbufs, pieceBytes=0, stream=None):
+    """sendbufs / recvbufs: host tensors (pinned for overlap); workbufs:
+    device tensors of count elements each."""
+    _check(_L().vr_allreduce_host(_ptrs(sendbufs), _ptrs(recvbufs), R, count, dtype, op, algo,
+                                  nChannels, chunkBytes, localRanks, _ptrs(workbufs),
+                                  pieceBytes, _stream(stream)),
+           "vr_allreduce_host")
 
 
 def vr_allreduce_trees(sendbufs, recvbufs, R, count, dtype, op, nChannels, chunkBytes, trees,

@@ -292,7 +292,7 @@ vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
   a.tileUnits = (int)(tb / 16);
   const long long TU = a.tileUnits;
   a.tiles = mode == kReduceScatter ? (long long)a.R * ((a.unitsFull + TU - 1) / TU)
-                                   : (a.unitsAll + TU - 1) / TU;
+                                   : (a.unitsAll - a.unitLo + TU - 1) / TU;
   a.stageBytes = ((unsigned)a.R * a.tileBytes + 127u) & ~127u;
   const int fit = room / (int)a.stageBytes;
   a.stages = std::min(kStagedMaxStages, fit);
@@ -335,6 +335,55 @@ void fill_partition(KArgs& a, size_t count, size_t E, int nCh, size_t chunkBytes
   a.gm = a.grains % nCh;
   a.chunk = (long long)(chunkBytes / E);
   a.nCh = nCh;
+  a.lo = 0;
+  a.hi = (long long)count;
+}
+
+// The AllReduce kernel over the elements [lo, hi) of the message `a`
+// describes (lo at a 16-byte boundary): the staged kernel, or the register
+// kernel (16-byte units when `vec`, else elements).  Every element's fold
+// reads only that element of each rank, and its order comes from the whole
+// message's partition, so pieces give the whole message's bits.
+vr_result_t launch_allreduce_range(KArgs& a, int dtype, int mode, int op, int stack, bool vec,
+                                   bool staged, long long lo, long long hi, void* stream) {
+  const long long E = (long long)elem_size(dtype);
+  a.lo = lo;
+  a.hi = hi;
+  if (staged) {
+    a.unitLo = lo * E / 16;
+    a.unitsAll = (hi * E + 15) / 16;
+    a.unitsFull = hi * E / 16;
+    return launch_staged(pick_staged(dtype, mode, op, stack), a, mode, stream);
+  }
+  const long long NV = vec ? kGrainBytes / E : 1;
+  return launch(pick_kernel(dtype, mode, op, vec, stack, a.R), a, (hi + NV - 1) / NV - lo / NV,
+                stream);
+}
+
+// Per device: the two copy streams and three events of vr_allreduce_host,
+// created on first use with that device current.
+struct HostPipe {
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, loaded = nullptr, folded = nullptr, stored = nullptr;
+};
+std::map<int, HostPipe> g_pipes;
+std::mutex g_pipeMu;  // held for a whole vr_allreduce_host enqueue (the events are shared)
+
+vr_result_t host_pipe(int device, HostPipe** out) {
+  auto it = g_pipes.find(device);
+  if (it == g_pipes.end()) {
+    HostPipe p;
+    if (cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.loaded, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.folded, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.stored, cudaEventDisableTiming) != cudaSuccess)
+      return VR_ERR_CUDA;
+    it = g_pipes.emplace(device, p).first;
+  }
+  *out = &it->second;
+  return VR_SUCCESS;
 }
 
 }  // namespace
@@ -409,9 +458,17 @@ vr_result_t vr_ring_block(size_t count, vr_dtype_t dtype, int R, int nChannels,
   return VR_ERR_INTERNAL;
 }
 
-vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, int R,
-                            size_t count, vr_dtype_t dtype, vr_op_t op, vr_algo_t algo,
-                            int nChannels, size_t chunkBytes, int localRanks, void* stream) {
+}  // extern "C"
+
+namespace vr {
+namespace {
+
+// Validates an AllReduce and fills `a` (ranks, partition, tree programs),
+// `mode` and `stack`.  AUTO resolves through the current cost model.
+vr_result_t plan_allreduce(const void* const* sendbufs, void* const* recvbufs, int R,
+                           size_t count, vr_dtype_t dtype, vr_op_t op, vr_algo_t algo,
+                           int nChannels, size_t chunkBytes, int localRanks, KArgs& a, int& mode,
+                           int& stack) {
   if (algo == VR_ALGO_AUTO && valid_common(R, dtype, nChannels, chunkBytes) && localRanks >= 1 &&
       R % localRanks == 0 &&
       vr_select_algo(R, localRanks, count * elem_size(dtype), nullptr, &algo) != VR_SUCCESS)
@@ -421,31 +478,132 @@ vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, 
     return VR_ERR_INVALID_ARGUMENT;
   const size_t E = elem_size(dtype);
   vr_result_t e = check_buffers(sendbufs, recvbufs, R, count * E, count * E, kAR, E);
-  if (e != VR_SUCCESS || count == 0) return e;
-  KArgs a;
+  if (e != VR_SUCCESS) return e;
   std::memset(&a, 0, sizeof(a));
   a.R = R;
   for (int r = 0; r < R; ++r) { a.src[r] = sendbufs[r]; a.dst[r] = recvbufs[r]; }
   fill_partition(a, count, E, nChannels, chunkBytes);
-  int mode = kRingAllReduce, stack = 0;
-  if (algo == VR_ALGO_TREE) {
+  mode = kRingAllReduce;
+  stack = 0;
+  if (algo == VR_ALGO_TREE && count > 0) {
     mode = kTreeAllReduce;
     std::array<FoldProg, 2> p;
     if ((e = tree_programs(R / localRanks, localRanks, &p)) != VR_SUCCESS) return e;
     set_dtree_programs(a, p, nChannels);
     stack = std::max(p[0].depth, p[1].depth);
   }
+  return VR_SUCCESS;
+}
+
+// Host memory (page-locked or not) for the host buffers, memory of the
+// current device for the workspace.
+bool is_device_memory(const void* p, int device) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) &&
+         at.device == device;
+}
+bool is_host_memory(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeUnregistered;
+}
+
+}  // namespace
+}  // namespace vr
+
+extern "C" {
+
+vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, int R,
+                            size_t count, vr_dtype_t dtype, vr_op_t op, vr_algo_t algo,
+                            int nChannels, size_t chunkBytes, int localRanks, void* stream) {
+  KArgs a;
+  int mode = 0, stack = 0;
+  vr_result_t e = plan_allreduce(sendbufs, recvbufs, R, count, dtype, op, algo, nChannels,
+                                 chunkBytes, localRanks, a, mode, stack);
+  if (e != VR_SUCCESS || count == 0) return e;
+  const size_t E = elem_size(dtype);
   const bool vec = aligned16(sendbufs, R, 0) && aligned16(recvbufs, R, 0);
   const int forced = forced_path();
-  if (vec && forced != 1 && (forced == 2 || use_staged(mode, R, count * E))) {
-    const long long bytes = (long long)count * (long long)E;
-    a.unitsAll = (bytes + 15) / 16;
-    a.unitsFull = bytes / 16;
-    return launch_staged(pick_staged(dtype, mode, op, stack), a, mode, stream);
+  const bool staged = vec && forced != 1 && (forced == 2 || use_staged(mode, R, count * E));
+  return launch_allreduce_range(a, dtype, mode, op, stack, vec, staged, 0, (long long)count,
+                                stream);
+}
+
+vr_result_t vr_allreduce_host(const void* const* sendbufs, void* const* recvbufs, int R,
+                              size_t count, vr_dtype_t dtype, vr_op_t op, vr_algo_t algo,
+                              int nChannels, size_t chunkBytes, int localRanks,
+                              void* const* workbufs, size_t pieceBytes, void* stream) {
+  if (pieceBytes == 0) pieceBytes = VR_HOST_PIECE_BYTES;
+  if (pieceBytes % kGrainBytes || !sendbufs || !recvbufs || !workbufs ||
+      !valid_common(R, dtype, nChannels, chunkBytes))
+    return VR_ERR_INVALID_ARGUMENT;
+  const size_t E = elem_size(dtype);
+  // the host side: distinct buffers, in place allowed
+  vr_result_t e = check_buffers(sendbufs, recvbufs, R, count * E, count * E, kAR, E);
+  if (e != VR_SUCCESS) return e;
+  // the device side: the workspace, folded in place
+  KArgs a;
+  int mode = 0, stack = 0;
+  e = plan_allreduce(const_cast<const void* const*>(workbufs), workbufs, R, count, dtype, op,
+                     algo, nChannels, chunkBytes, localRanks, a, mode, stack);
+  if (e != VR_SUCCESS || count == 0) return e;
+  DeviceInfo di;
+  int device = 0;
+  if ((e = device_info(&di, &device)) != VR_SUCCESS) return e;
+  for (int r = 0; r < R; ++r)
+    if (!is_device_memory(workbufs[r], device) || !is_host_memory(sendbufs[r]) ||
+        !is_host_memory(recvbufs[r]))
+      return VR_ERR_INVALID_ARGUMENT;
+  const bool vec = aligned16(const_cast<const void* const*>(workbufs), R, 0);
+  const int forced = forced_path();
+  const bool staged = vec && forced != 1 && (forced == 2 || use_staged(mode, R, count * E));
+  const long long piece = (long long)(pieceBytes / E);
+  const cudaStream_t s = (cudaStream_t)stream;
+
+  std::lock_guard<std::mutex> g(g_pipeMu);
+  HostPipe* hp = nullptr;
+  {
+    std::lock_guard<std::mutex> g2(g_mu);
+    if ((e = host_pipe(device, &hp)) != VR_SUCCESS) return e;
   }
-  const long long NV = vec ? kGrainBytes / (long long)E : 1;
-  return launch(pick_kernel(dtype, mode, op, vec, stack, R), a,
-                ((long long)count + NV - 1) / NV, stream);
+  // Nothing is copied in before the caller's earlier work on `stream` is done.
+  if (cudaEventRecord(hp->start, s) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->in, hp->start, 0) != cudaSuccess)
+    return VR_ERR_CUDA;
+  for (long long lo = 0; lo < (long long)count; lo += piece) {
+    const long long hi = std::min((long long)count, lo + piece);
+    const size_t off = (size_t)lo * E, bytes = (size_t)(hi - lo) * E;
+    for (int r = 0; r < R; ++r)
+      if (cudaMemcpyAsync((char*)workbufs[r] + off, (const char*)sendbufs[r] + off, bytes,
+                          cudaMemcpyHostToDevice, hp->in) != cudaSuccess)
+        return VR_ERR_CUDA;
+    // a wait takes the event's latest record, so one event serves every piece
+    if (cudaEventRecord(hp->loaded, hp->in) != cudaSuccess ||
+        cudaStreamWaitEvent(s, hp->loaded, 0) != cudaSuccess)
+      return VR_ERR_CUDA;
+    if ((e = launch_allreduce_range(a, dtype, mode, op, stack, vec, staged, lo, hi, stream)) !=
+        VR_SUCCESS)
+      return e;
+    if (cudaEventRecord(hp->folded, s) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->out, hp->folded, 0) != cudaSuccess)
+      return VR_ERR_CUDA;
+    for (int r = 0; r < R; ++r)
+      if (cudaMemcpyAsync((char*)recvbufs[r] + off, (const char*)workbufs[r] + off, bytes,
+                          cudaMemcpyDeviceToHost, hp->out) != cudaSuccess)
+        return VR_ERR_CUDA;
+  }
+  // Work enqueued on `stream` after this call runs after the last copy out.
+  if (cudaEventRecord(hp->stored, hp->out) != cudaSuccess ||
+      cudaStreamWaitEvent(s, hp->stored, 0) != cudaSuccess)
+    return VR_ERR_CUDA;
+  return VR_SUCCESS;
 }
 
 vr_result_t vr_predict_us(vr_algo_t algo, int R, int localRanks, size_t bytesPerRank,
@@ -532,17 +690,8 @@ vr_result_t vr_allreduce_trees(const void* const* sendbufs, void* const* recvbuf
     a.chanProg[c] = (uint8_t)found;
   }
   const bool vec = aligned16(sendbufs, R, 0) && aligned16(recvbufs, R, 0);
-  const int forced = forced_path();
-  if (vec && forced == 2) {
-    const long long bytes = (long long)count * (long long)E;
-    a.unitsAll = (bytes + 15) / 16;
-    a.unitsFull = bytes / 16;
-    return launch_staged(pick_staged(dtype, kTreeAllReduce, op, stack), a, kTreeAllReduce,
-                         stream);
-  }
-  const long long NV = vec ? kGrainBytes / (long long)E : 1;
-  return launch(pick_kernel(dtype, kTreeAllReduce, op, vec, stack, R), a,
-                ((long long)count + NV - 1) / NV, stream);
+  return launch_allreduce_range(a, dtype, kTreeAllReduce, op, stack, vec,
+                                vec && forced_path() == 2, 0, (long long)count, stream);
 }
 
 vr_result_t vr_reduce_scatter(const void* const* sendbufs, void* const* recvbufs, int R,
@@ -719,6 +868,22 @@ const char* vr_get_error_string(vr_result_t result) {
 }
 
 void vr_finalize(void) {
+  {
+    std::lock_guard<std::mutex> gp(g_pipeMu);
+    int current = 0;
+    const bool haveDevice = cudaGetDevice(&current) == cudaSuccess;
+    for (auto& kv : g_pipes) {
+      if (cudaSetDevice(kv.first) != cudaSuccess) continue;
+      HostPipe& p = kv.second;
+      cudaStreamSynchronize(p.in);
+      cudaStreamSynchronize(p.out);
+      cudaStreamDestroy(p.in);
+      cudaStreamDestroy(p.out);
+      for (cudaEvent_t ev : {p.start, p.loaded, p.folded, p.stored}) cudaEventDestroy(ev);
+    }
+    g_pipes.clear();
+    if (haveDevice) cudaSetDevice(current);
+  }
   std::lock_guard<std::mutex> g(g_mu);
   g_progs.clear();
   g_occupancy.clear();

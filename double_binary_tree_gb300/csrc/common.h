@@ -45,6 +45,9 @@ struct KArgs {
   long long grains;     // AllReduce: 16-byte grains of the message
   long long gq, gm;     // grains / nChannels, grains % nChannels
   long long chunk;      // C, elements per rank per ring loop block
+  long long lo, hi;     // AllReduce: the elements [lo, hi) this launch folds, a piece of the
+                        // count-element message whose partition the fields above describe
+                        // (lo at a 16-byte boundary); [0, count) for a whole message
   int R;
   int nCh;
   int nProgs;           // fold programs in prog[]
@@ -52,8 +55,10 @@ struct KArgs {
   unsigned* status;     // this device's status word
   void* scratch;        // stepwise ring: the message FIFO (count elements)
   // TMA-staged kernels (staged.cuh)
-  long long unitsAll;   // 16-byte units of the message, a trailing partial one included
-  long long unitsFull;  // full 16-byte units (ReduceScatter: per block)
+  long long unitLo;     // AllReduce: first 16-byte unit of the range
+  long long unitsAll;   // AllReduce: end unit of the range, a trailing partial one included
+  long long unitsFull;  // AllReduce: end of the full units of the range; ReduceScatter: units
+                        // per block
   long long tiles;      // tiles of tileUnits units
   unsigned long long timeoutNs;  // limit of every bounded wait
   long long injectStall;         // test hook: CTA 0 never loads its tile of this index (-1: off)

@@ -64,10 +64,11 @@ __global__ void __launch_bounds__(kBlock, SMALL ? kMinBlocksSmall
   stage_args<MODE>(a, s_src, s_dst, s_prog);
 
   const int R = a.R;
-  const long long count = a.count;
-  const long long units = (count + NV - 1) / NV;
-  const long long ub = units * blockIdx.x / gridDim.x;
-  const long long ue = units * (blockIdx.x + 1) / gridDim.x;
+  const long long count = a.hi;  // end of this launch's range of the message
+  const long long u0 = a.lo / NV;
+  const long long units = (count + NV - 1) / NV - u0;
+  const long long ub = u0 + units * blockIdx.x / gridDim.x;
+  const long long ue = u0 + units * (blockIdx.x + 1) / gridDim.x;
   Cursor cur{0, -1, 0, 0, 0, 0, 0};
   for (long long u = ub + threadIdx.x; u < ue; u += blockDim.x) {
     const long long e0 = u * NV;

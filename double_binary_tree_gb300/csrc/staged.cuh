@@ -112,7 +112,7 @@ __device__ __forceinline__ TileGeom tile_geom(const KArgs& a, long long t) {
     g.srcOff = (long long)g.b * perB * 16 + g.u0 * 16;
   } else {
     g.b = 0;
-    g.u0 = t * TU;
+    g.u0 = a.unitLo + t * TU;
     g.units = (int)min((long long)TU, a.unitsAll - g.u0);
     const long long full = min((long long)TU, max(0LL, a.unitsFull - g.u0));
     g.bytes = (unsigned)full * 16u;
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
           }
         } else {
           // the partial unit at the end of the message: not copied, read here
-          for (long long e = e0; e < a.count; ++e) {
+          for (long long e = e0; e < a.hi; ++e) {
             const GlobalSrc src{s_src, e * E};
             const typename Ty<T>::Bits o = fold_element<T, OP, MODE, S>(a, src, s_prog, e, cur);
             for (int r = 0; r < R; ++r) Unit<T, 1>::store(s_dst[r] + e * E, o);

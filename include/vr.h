@@ -183,6 +183,37 @@ vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, 
                             size_t count, vr_dtype_t dtype, vr_op_t op, vr_algo_t algo,
                             int nChannels, size_t chunkBytes, int localRanks, void* stream);
 
+/* vr_allreduce_ex on HOST buffers, pipelined through a device workspace.
+ * [Internals] "API 返回只意味着提交边界": the call enqueues and returns; here
+ * the enqueued work also moves the data in and out.  The message is cut into
+ * pieces of pieceBytes per rank (0: VR_HOST_PIECE_BYTES; else a multiple of
+ * 16).  Piece p is copied in to workbufs on one internal stream, folded in
+ * place there on `stream`, and copied out to recvbufs on another internal
+ * stream, so copies in both directions overlap the fold of other pieces.
+ * The result equals vr_allreduce_ex's bit for bit: an element's fold reads
+ * only that element of each rank, in the order the whole message's
+ * partition gives it.
+ *   sendbufs[r], recvbufs[r]: host memory, count elements; page-locked for
+ *     the copies to overlap (pageable memory works, serialised); in place
+ *     (recvbufs[r] == sendbufs[r]) allowed.  They must stay valid, and
+ *     sendbufs unchanged, until `stream` has passed this call.
+ *   workbufs[r]: device memory of the current device, count elements each,
+ *     owned by the caller; overwritten.
+ *   stream: nothing is copied in before the caller's earlier work on it is
+ *     done, and work the caller enqueues on it after this call waits for the
+ *     last copy out.
+ * The internal streams and events are created per device on first use and
+ * destroyed by vr_finalize.  Calls from several threads are serialised on
+ * the host.  Errors as vr_allreduce_ex, plus VR_ERR_INVALID_ARGUMENT for a
+ * NULL workbufs, a pieceBytes not a multiple of 16, a workspace buffer that
+ * is not device memory of the current device, or a host buffer that is
+ * device memory. */
+#define VR_HOST_PIECE_BYTES ((size_t)8 << 20)
+vr_result_t vr_allreduce_host(const void* const* sendbufs, void* const* recvbufs, int R,
+                              size_t count, vr_dtype_t dtype, vr_op_t op, vr_algo_t algo,
+                              int nChannels, size_t chunkBytes, int localRanks,
+                              void* const* workbufs, size_t pieceBytes, void* stream);
+
 /* Tree AllReduce over caller-given trees: channel c folds every element over
  * trees[c*R .. c*R + R-1] (vr_tree_t records, e.g. from vr_build_dtree_ex)
  * in the order of vr_allreduce's TREE: each rank folds its local input with

@@ -460,3 +460,69 @@ def test_auto_runs_the_algorithm_the_oracle_cost_model_picks():
         assert picked == {"ring", "tree"}
     finally:
         vr.vr_set_cost_model(None)
+
+
+# ------------------------------------------------ host buffers, pipelined
+def _host_run(inputs, dtype, op, algo, nch, cb, L=1, piece=0, pinned=True, inplace=False,
+              shift=0):
+    R, count = len(inputs), inputs[0].numel()
+    send = [t.clone().pin_memory() if pinned else t.clone() for t in inputs]
+    recv = send if inplace else [torch.full_like(t, 7).pin_memory() if pinned
+                                 else torch.full_like(t, 7) for t in inputs]
+    work = [torch.empty(count + shift, dtype=t.dtype, device="cuda")[shift:] for t in inputs]
+    st = torch.cuda.current_stream()
+    vr.vr_allreduce_host(send, recv, R, count, dtype, op, algo, nch, cb, L, work, piece, st)
+    st.synchronize()
+    assert_status_ok()
+    return [workloads.raw_numpy(t) for t in recv]
+
+
+@pytest.mark.parametrize("dtype", [F32, F16, BF16])
+@pytest.mark.parametrize("algo", [RING, TREE])
+def test_allreduce_host_equals_oracle(dtype, algo, path):
+    """Pieces of 48 KiB per rank (the last one ragged) over a message whose
+    ring blocks and channels do not line up with them."""
+    R, count = 8, 100_003 if dtype == F32 else 200_011
+    inp = workloads.generate(R, count, dtype, "normal", 21)
+    _, want = expect_allreduce(inp, dtype, SUM, algo, 5, 1 << 14)
+    got = _host_run(inp, dtype, SUM, algo, 5, 1 << 14, piece=48 << 10)
+    assert_bits_equal(got, want, "host pieces")
+
+
+def test_allreduce_host_variants():
+    """Default piece size, pageable memory, in place, Max, a hierarchical
+    tree, an unaligned workspace (element kernels) and one piece."""
+    R, count = 8, 3 * (1 << 20) + 5
+    inp = workloads.generate(R, count, F32, "normal", 22)
+    _, want = expect_allreduce(inp, F32, SUM, RING, 12, 1 << 19)
+    assert_bits_equal(_host_run(inp, F32, SUM, RING, 12, 1 << 19), want, "default")
+    assert_bits_equal(_host_run(inp, F32, SUM, RING, 12, 1 << 19, pinned=False), want, "pageable")
+    assert_bits_equal(_host_run(inp, F32, SUM, RING, 12, 1 << 19, inplace=True), want, "in place")
+    assert_bits_equal(_host_run(inp, F32, SUM, RING, 12, 1 << 19, piece=1 << 30), want, "1 piece")
+    assert_bits_equal(_host_run(inp, F32, SUM, RING, 12, 1 << 19, piece=1 << 16, shift=1), want,
+                      "unaligned workspace")
+    _, want = expect_allreduce(inp, F32, MAX, TREE, 3, 1 << 16, L=4)
+    assert_bits_equal(_host_run(inp, F32, MAX, TREE, 3, 1 << 16, L=4, piece=1 << 20), want,
+                      "hier tree max")
+
+
+def test_allreduce_host_orders_with_the_stream():
+    """Work enqueued before the call is done before the copy in; work after
+    it sees the copied-out result."""
+    R, count = 4, 1 << 20
+    st = torch.cuda.current_stream()
+    dev_in = [torch.zeros(count, device="cuda") for _ in range(R)]
+    send = [torch.empty(count).pin_memory() for _ in range(R)]
+    recv = [torch.empty(count).pin_memory() for _ in range(R)]
+    work = [torch.empty(count, device="cuda") for _ in range(R)]
+    for r in range(R):
+        dev_in[r].fill_(float(r + 1))
+        send[r].copy_(dev_in[r], non_blocking=True)   # on the stream, before the call
+    vr.vr_allreduce_host(send, recv, R, count, F32, SUM, RING, 2, 1 << 16, 1, work, 1 << 18, st)
+    back = torch.empty(count, device="cuda")
+    back.copy_(recv[0], non_blocking=True)            # on the stream, after the call
+    st.synchronize()
+    assert_status_ok()
+    assert bool((back == 10.0).all())
+    for r in range(R):
+        assert bool((recv[r] == 10.0).all())

@@ -341,3 +341,27 @@ def test_cost_model_argument_errors():
             vr.vr_predict_us(*args)
     with pytest.raises(vr.VrError):
         vr.vr_select_algo(6, 4, 0)
+
+
+def test_allreduce_host_argument_errors():
+    """Rejected before any CUDA call: nothing is enqueued, no stream is made."""
+    INV = vr.VR_ERR_INVALID_ARGUMENT
+    F32, SUM, RING = vr.VR_FLOAT32, vr.VR_SUM, vr.VR_ALGO_RING
+    W = [0x40000000 + 0x100000 * (i + 1) for i in range(64)]
+    h = vr.vr_allreduce_host
+    before = vr.vr_launch_count()
+    assert _err(h, FAKE[:4], FAKE_R[:4], 4, 64, F32, SUM, RING, 1, 16, 1, W[:4], 8) == INV
+    assert _err(h, FAKE[:4], FAKE_R[:4], 4, 64, F32, SUM, RING, 1, 16, 1, None, 0) == INV
+    assert _err(h, FAKE[:4], FAKE_R[:4], 4, 64, F32, SUM, RING, 0, 16, 1, W[:4], 0) == INV
+    assert _err(h, FAKE[:4], FAKE_R[:4], 4, 64, F32, SUM, 7, 1, 16, 1, W[:4], 0) == INV
+    assert _err(h, FAKE[:4], FAKE_R[:4], 4, 64, F32, SUM, RING, 1, 16, 3, W[:4], 0) == INV
+    # overlapping host buffers, overlapping workspace buffers
+    assert _err(h, FAKE[:2], [FAKE_R[0], FAKE_R[0] + 8], 2, 4, F32, SUM, RING, 1, 16, 1, W[:2],
+                0) == INV
+    assert _err(h, FAKE[:2], FAKE_R[:2], 2, 4, F32, SUM, RING, 1, 16, 1, [W[0], W[0] + 4],
+                0) == INV
+    assert _err(h, FAKE[:2], FAKE_R[:2], 2, 4, F32, SUM, RING, 1, 16, 1, [W[0] + 2, W[1]],
+                0) == INV
+    # count == 0 enqueues nothing
+    h(FAKE[:4], FAKE_R[:4], 4, 0, F32, SUM, RING, 1, 16, 1, W[:4], 0)
+    assert vr.vr_launch_count() == before
