@@ -2,9 +2,10 @@
 //
 // Each thread loads the R ranks' copies of a unit straight from global
 // memory (up to kBatch loads in flight), folds them (fold.cuh) and stores the
-// result to every receiving rank.  These serve buffers that are not 16-byte
-// aligned (element units) and AllGather; aligned AllReduce / ReduceScatter
-// run the TMA-staged kernels of staged.cuh.
+// result to every receiving rank.  They serve the tree, rings of fewer than
+// 8 or more than 32 ranks, messages under 16 MiB per rank, ReduceScatter, and
+// buffers that are not 16-byte aligned (element units); the ring of 8-32
+// ranks from 16 MiB per rank runs the TMA-staged kernel of staged.cuh.
 //
 // Persistent grid: CTA b owns a contiguous run of units and its threads
 // stride through it, so a warp touches 512 contiguous bytes of each rank per
