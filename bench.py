@@ -13,8 +13,9 @@ so no flush is needed between steps.
 Rank 0 prints one JSON line.  It also carries algbw/busbw, a roofline object
 for the kernel, the CPU oracle timed on the host cores (cpu_baseline), an
 end-to-end figure through the same C ABI with the inputs copied in from
-pinned host memory and every rank's result copied back inside the timed
-region, pipelined in pieces by vr_allreduce_host (e2e), SM clocks sampled during the timed region, and the other
+pinned host memory and the result (rank 0's copy; every rank holds the same
+bits) copied back inside the timed region, pipelined in pieces by
+vr_allreduce_host (e2e), SM clocks sampled during the timed region, and the other
 workloads (tree bf16 R=8 / R=7, hierarchical fp16 R=64 ring / tree / Sum /
 Max, ReduceScatter, AllGather) timed the same way under "workloads".
 
@@ -263,7 +264,9 @@ def e2e_arm(args, vr, torch, inputs, dev, stream, world):
     W = WORKLOAD
     R, count, dtype = W["R"], W["count"], W["dtype"]
     host_in = [t.pin_memory() for t in inputs]
-    host_out = [torch.empty_like(t).pin_memory() for t in inputs]
+    # The step's result is one vector (every rank receives the same bits):
+    # rank 0's copy comes back to the host, the others stay on the device.
+    host_out = [torch.empty_like(inputs[0]).pin_memory()] + [None] * (R - 1)
     work = [torch.empty_like(t, device=dev) for t in inputs]
 
     def step():
@@ -287,12 +290,13 @@ def e2e_arm(args, vr, torch, inputs, dev, stream, world):
         raise RuntimeError("device status error in the end-to-end region")
     ms = max_over_ranks(torch, a.elapsed_time(b), dev)
     nbytes = ar_bytes(R, count, dtype)
-    io = R * count * elem_size(dtype)
+    S = count * elem_size(dtype)
     return {"value": round(job_gbs(world, nbytes, steps, ms), 1), "unit": "GB/s",
-            "h2d_bytes_per_step": io, "d2h_bytes_per_step": io, "steps": steps,
+            "h2d_bytes_per_step": R * S, "d2h_bytes_per_step": S, "steps": steps,
             "ms_per_step": round(ms / steps, 4),
-            "api": "vr_allreduce_host (pinned host buffers, %s per rank per piece)" % (
-                "%d MiB" % ((args.piece_bytes or vr.VR_HOST_PIECE_BYTES) >> 20))}
+            "api": "vr_allreduce_host: R inputs in from pinned host memory, the result "
+                   "(rank 0's copy) out, %d MiB per rank per piece" % (
+                       (args.piece_bytes or vr.VR_HOST_PIECE_BYTES) >> 20)}
 
 
 def time_calls(torch, stream, call, sets, iters):
@@ -473,6 +477,8 @@ PROFILE_CASES = {
     # --count (elements per rank for AllReduce, per block for the others)
     "ring_r8_fp32": ("ar", 8, 1, 0, 0, 0),
     "tree_r8_bf16": ("ar", 8, 1, 2, 0, 1),
+    "tree_r8_fp32": ("ar", 8, 1, 0, 0, 1),
+    "ring_r4_fp32": ("ar", 4, 1, 0, 0, 0),
     "tree_r7_bf16": ("ar", 7, 1, 2, 0, 1),
     "tree_r64_fp16_hier": ("ar", 64, 8, 1, 0, 1),
     "tree_r64_fp16_hier_max": ("ar", 64, 8, 1, 1, 1),

@@ -153,13 +153,15 @@ bool overlap(uintptr_t a, size_t an, uintptr_t b, size_t bn) {
 // path accesses whole elements.
 enum Kind { kAR, kRS, kAG };
 vr_result_t check_buffers(const void* const* send, void* const* recv, int R, size_t sendBytes,
-                          size_t recvBytes, Kind kind, size_t E) {
+                          size_t recvBytes, Kind kind, size_t E, bool nullRecvOk = false) {
   if (!send || !recv) return VR_ERR_INVALID_ARGUMENT;
   for (int r = 0; r < R; ++r) {
-    if ((sendBytes && !send[r]) || (recvBytes && !recv[r])) return VR_ERR_INVALID_ARGUMENT;
+    if ((sendBytes && !send[r]) || (recvBytes && !recv[r] && !nullRecvOk))
+      return VR_ERR_INVALID_ARGUMENT;
     if (((uintptr_t)send[r] | (uintptr_t)recv[r]) % E) return VR_ERR_INVALID_ARGUMENT;
   }
   for (int r = 0; r < R; ++r) {
+    if (!recv[r]) continue;  // nothing received (only where nullRecvOk)
     const uintptr_t s = (uintptr_t)send[r], d = (uintptr_t)recv[r];
     bool inPlace = false;
     if (kind == kAR) inPlace = d == s;
@@ -168,7 +170,8 @@ vr_result_t check_buffers(const void* const* send, void* const* recv, int R, siz
     if (!inPlace && overlap(s, sendBytes, d, recvBytes)) return VR_ERR_INVALID_ARGUMENT;
     for (int q = 0; q < R; ++q) {
       if (q == r) continue;
-      if (overlap(d, recvBytes, (uintptr_t)recv[q], recvBytes)) return VR_ERR_INVALID_ARGUMENT;
+      if (recv[q] && overlap(d, recvBytes, (uintptr_t)recv[q], recvBytes))
+        return VR_ERR_INVALID_ARGUMENT;
       if (overlap(d, recvBytes, (uintptr_t)send[q], sendBytes)) return VR_ERR_INVALID_ARGUMENT;
     }
   }
@@ -545,8 +548,8 @@ vr_result_t vr_allreduce_host(const void* const* sendbufs, void* const* recvbufs
       !valid_common(R, dtype, nChannels, chunkBytes))
     return VR_ERR_INVALID_ARGUMENT;
   const size_t E = elem_size(dtype);
-  // the host side: distinct buffers, in place allowed
-  vr_result_t e = check_buffers(sendbufs, recvbufs, R, count * E, count * E, kAR, E);
+  // the host side: distinct buffers, in place allowed, NULL receive buffers skipped
+  vr_result_t e = check_buffers(sendbufs, recvbufs, R, count * E, count * E, kAR, E, true);
   if (e != VR_SUCCESS) return e;
   // the device side: the workspace, folded in place
   KArgs a;
@@ -559,7 +562,7 @@ vr_result_t vr_allreduce_host(const void* const* sendbufs, void* const* recvbufs
   if ((e = device_info(&di, &device)) != VR_SUCCESS) return e;
   for (int r = 0; r < R; ++r)
     if (!is_device_memory(workbufs[r], device) || !is_host_memory(sendbufs[r]) ||
-        !is_host_memory(recvbufs[r]))
+        (recvbufs[r] && !is_host_memory(recvbufs[r])))
       return VR_ERR_INVALID_ARGUMENT;
   const bool vec = aligned16(const_cast<const void* const*>(workbufs), R, 0);
   const int forced = forced_path();
@@ -595,7 +598,8 @@ vr_result_t vr_allreduce_host(const void* const* sendbufs, void* const* recvbufs
         cudaStreamWaitEvent(hp->out, hp->folded, 0) != cudaSuccess)
       return VR_ERR_CUDA;
     for (int r = 0; r < R; ++r)
-      if (cudaMemcpyAsync((char*)recvbufs[r] + off, (const char*)workbufs[r] + off, bytes,
+      if (recvbufs[r] &&
+          cudaMemcpyAsync((char*)recvbufs[r] + off, (const char*)workbufs[r] + off, bytes,
                           cudaMemcpyDeviceToHost, hp->out) != cudaSuccess)
         return VR_ERR_CUDA;
   }

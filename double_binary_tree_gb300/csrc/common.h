@@ -1,12 +1,21 @@
 // Internal types shared by the host planner and the kernels.
 #pragma once
 
+#ifdef __CUDACC_RTC__  // run-time compilation (jit.cc): no C library headers
+typedef unsigned char uint8_t;
+typedef unsigned short uint16_t;
+typedef unsigned int uint32_t;
+typedef unsigned long long uint64_t;
+typedef long long int64_t;
+#else
 #include <stdint.h>
+#endif
 
 #include "../../include/vr.h"
 
 namespace vr {
 
+constexpr int kWarpSize = 32;
 constexpr int kMaxRanks = VR_MAX_RANKS;
 constexpr int kMaxChannels = VR_MAX_CHANNELS;
 constexpr int kGrainBytes = 16;      // channel ranges are cut in 16-byte grains

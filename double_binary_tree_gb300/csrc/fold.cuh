@@ -18,14 +18,17 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#ifndef __CUDACC_RTC__  // run-time compilation (jit.cc) has no host headers
 #include <cuda_runtime.h>
 #include <stdint.h>
-
-#include <type_traits>
+#endif
 
 #include "common.h"
 
 namespace vr {
+
+template <bool C, class A, class B> struct Select { typedef A type; };
+template <class A, class B> struct Select<false, A, B> { typedef B type; };
 
 constexpr int kBatch = 8;  // rank loads issued together before they are folded
 
@@ -74,7 +77,7 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 // A unit is one 16-byte vector (NV = Ty<T>::U elements) or one element.
 template <typename T, int NV> struct Unit {
   typedef typename Ty<T>::Bits Bits;
-  typedef typename std::conditional<NV == 1, Bits, uint4>::type Raw;
+  typedef typename Select<NV == 1, Bits, uint4>::type Raw;
 
   static __device__ __forceinline__ void store(char* p, Raw v) {
     if constexpr (NV == 1) *reinterpret_cast<Bits*>(p) = v;

@@ -29,7 +29,6 @@
 
 namespace vr {
 
-constexpr int kWarpSize = 32;
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

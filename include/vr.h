@@ -37,7 +37,9 @@
 #ifndef VR_H
 #define VR_H
 
+#ifndef __CUDACC_RTC__
 #include <stddef.h>
+#endif
 
 #ifdef __cplusplus
 extern "C" {
@@ -197,6 +199,9 @@ vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, 
  *     the copies to overlap (pageable memory works, serialised); in place
  *     (recvbufs[r] == sendbufs[r]) allowed.  They must stay valid, and
  *     sendbufs unchanged, until `stream` has passed this call.
+ *     recvbufs[r] may be NULL: rank r's result is then not copied out and
+ *     stays in workbufs[r] only (every rank's result is the same vector, so
+ *     a caller that needs one copy on the host names one receive buffer).
  *   workbufs[r]: device memory of the current device, count elements each,
  *     owned by the caller; overwritten.
  *   stream: nothing is copied in before the caller's earlier work on it is

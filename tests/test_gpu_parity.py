@@ -526,3 +526,21 @@ def test_allreduce_host_orders_with_the_stream():
     assert bool((back == 10.0).all())
     for r in range(R):
         assert bool((recv[r] == 10.0).all())
+
+
+def test_allreduce_host_null_receive_buffers():
+    """Only rank 0's result is copied out; every rank's result stays in the
+    workspace, all equal to the oracle."""
+    R, count = 8, (1 << 20) + 3
+    inp = workloads.generate(R, count, BF16, "normal", 23)
+    _, want = expect_allreduce(inp, BF16, SUM, TREE, 4, 1 << 16)
+    send = [t.clone().pin_memory() for t in inp]
+    out0 = torch.full_like(inp[0], 7).pin_memory()
+    work = [torch.empty(count, dtype=inp[0].dtype, device="cuda") for _ in range(R)]
+    st = torch.cuda.current_stream()
+    vr.vr_allreduce_host(send, [out0] + [None] * (R - 1), R, count, BF16, SUM, TREE, 4, 1 << 16,
+                         1, work, 1 << 18, st)
+    st.synchronize()
+    assert_status_ok()
+    assert_bits_equal([workloads.raw_numpy(out0)], want[:1], "rank 0 copied out")
+    assert_bits_equal([bits(w) for w in work], want, "workspace")
