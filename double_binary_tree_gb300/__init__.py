@@ -64,6 +64,8 @@ _SIGNATURES = {
     "vr_predict_us": (I, [I, I, I, S, P(vr_cost_model_t), P(ctypes.c_double)]),
     "vr_select_algo": (I, [I, I, S, P(vr_cost_model_t), P(I)]),
     "vr_set_cost_model": (I, [P(vr_cost_model_t)]),
+    "vr_jit_status": (I, [P(I), P(ctypes.c_longlong), P(ctypes.c_longlong)]),
+    "vr_jit_compile_dtree": (I, [I, I, I, I, I, P(S), ctypes.c_char_p, S]),
     "vr_stream_status": (I, [VP]),
     "vr_launch_count": (ctypes.c_ulonglong, []),
     "vr_debug_stall_next": (I, [ctypes.c_longlong]),
@@ -274,6 +276,26 @@ def vr_set_cost_model(model=None):
     m = _model(model)
     _check(_L().vr_set_cost_model(ctypes.byref(m) if m is not None else None),
            "vr_set_cost_model")
+
+
+def vr_jit_status():
+    """(enabled, kernel sets compiled, failed) of the run-time specialised trees."""
+    en, comp, fail = ctypes.c_int(), ctypes.c_longlong(), ctypes.c_longlong()
+    _check(_L().vr_jit_status(ctypes.byref(en), ctypes.byref(comp), ctypes.byref(fail)),
+           "vr_jit_status")
+    return bool(en.value), comp.value, fail.value
+
+
+def vr_jit_compile_dtree(nNodes, localRanks, dtype, op, smArch=103):
+    """Compile-only: CUBIN bytes of the specialised kernels of the double
+    binary tree of (nNodes, localRanks); raises VrError with the log."""
+    size = ctypes.c_size_t()
+    log = ctypes.create_string_buffer(8192)
+    code = _L().vr_jit_compile_dtree(nNodes, localRanks, dtype, op, smArch, ctypes.byref(size),
+                                     log, len(log))
+    if code != 0:
+        raise VrError(code, "vr_jit_compile_dtree: " + log.value.decode(errors="replace")[:2000])
+    return size.value
 
 
 def vr_stream_status(stream=None):

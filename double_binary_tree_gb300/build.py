@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libvr.so")
 SOURCES = ["topology.cc", "api.cc", "kernels_f32.cu", "kernels_f16.cu", "kernels_bf16.cu",
-           "kernels_copy.cu", "kernels_ablation.cu", "noalloc.cu"]
+           "kernels_copy.cu", "kernels_ablation.cu", "noalloc.cu", "jit.cc"]
 HEADERS = ["common.h", "host.h", "fold.cuh", "kernels.cuh", "staged.cuh", "ablation.cuh", "gather.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -81,7 +81,7 @@ def build(force=False, verbose=False, ptxas_info=False):
     if failed:
         raise RuntimeError("nvcc failed\n" + "\n".join(failed))
     tmp = LIB + ".tmp"
-    link = [nvcc, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static"]
+    link = [nvcc, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static", "-ldl"]
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout.decode(errors="replace"))

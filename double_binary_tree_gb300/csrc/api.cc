@@ -116,15 +116,9 @@ vr_result_t tree_programs(int nNodes, int L, std::array<FoldProg, 2>* out) {
   auto key = std::make_pair(nNodes, L);
   auto it = g_progs.find(key);
   if (it == g_progs.end()) {
-    const int R = nNodes * L;
-    vr_tree_t trees[2 * kMaxRanks];
-    vr_result_t e = build_dtree(nNodes, L, 2, trees);  // channel 0: tree 0, channel 1: tree 1
-    if (e != VR_SUCCESS) return e;
     std::array<FoldProg, 2> p;
-    for (int t = 0; t < 2; ++t) {
-      e = compile_fold(trees + t * R, R, &p[t]);
-      if (e != VR_SUCCESS) return e;
-    }
+    const vr_result_t e = dtree_programs(nNodes, L, p.data());
+    if (e != VR_SUCCESS) return e;
     it = g_progs.emplace(key, p).first;
   }
   *out = it->second;
@@ -218,10 +212,12 @@ const void* pick_staged(int dtype, int mode, int op, int stack = 0) {
 // for 3 CTAs per SM (1.2-1.5x faster from 16 MiB per rank; slower for 16-bit
 // types, which keep the general kernel).  VR_SMALL_RANKS=0, read per call,
 // turns it off for tuning.
+bool use_small(int dtype, int mode, bool vec, int stack, int R) {
+  return dtype == VR_FLOAT32 && vec && R <= 4 && stack <= 4 && mode != kReduceScatter &&
+         env_uint("VR_SMALL_RANKS", 1) != 0;
+}
 const void* pick_kernel(int dtype, int mode, int op, bool vec, int stack = 0, int R = 64) {
-  const bool small = dtype == VR_FLOAT32 && vec && R <= 4 && stack <= 4 &&
-                     mode != kReduceScatter &&
-                     env_uint("VR_SMALL_RANKS", 1) != 0;
+  const bool small = use_small(dtype, mode, vec, stack, R);
   switch (dtype) {
     case VR_FLOAT32: return kernel_ptr_f32(mode, op, vec, stack, small);
     case VR_FLOAT16: return kernel_ptr_f16(mode, op, vec, stack, small);
@@ -259,9 +255,16 @@ vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream,
 // warps are too few to hide the latency of the tree's data-dependent fold
 // and of ReduceScatter's 64-rank folds, and with few ranks its stages hold
 // too few bytes in flight.  Everything else runs on the register path.
+// Measured on GB300: from 16 MiB per rank the staged kernel beats the
+// register path for the ring of 8-32 ranks and, with its fold specialised at
+// run time (jit.cc), for the tree of 8-64 ranks (the interpreting staged tree
+// is 2-3x slower than the register path).
 bool use_staged(int mode, int R, size_t bytesPerRank) {
   const size_t minBytes = env_uint("VR_STAGED_MIN_BYTES", 16u << 20);
-  return mode == kRingAllReduce && R >= 8 && R <= 32 && bytesPerRank >= minBytes;
+  if (R < 8 || bytesPerRank < minBytes) return false;
+  if (mode == kRingAllReduce) return R <= 32;
+  if (mode == kTreeAllReduce) return jit_enabled();
+  return false;
 }
 
 // Per-rank tile bytes of the staged kernel (bulk copies below 2 KB lose
@@ -352,15 +355,25 @@ vr_result_t launch_allreduce_range(KArgs& a, int dtype, int mode, int op, int st
   const long long E = (long long)elem_size(dtype);
   a.lo = lo;
   a.hi = hi;
+  // Trees on 16-byte units: the kernels specialised for this call's programs
+  // when they can be had (jit.cc), else the interpreting ones.
+  // (The specialised register-path kernel measured slower than the
+  // interpreting one at 64 ranks: above 32 only the staged one is used.)
+  const void* special = nullptr;
+  if (mode == kTreeAllReduce && vec && (staged || a.R <= 32) && jit_enabled() &&
+      jit_tree_kernel(dtype, op, stack, use_small(dtype, mode, vec, stack, a.R), staged, a.prog,
+                      a.nProgs, &special) != VR_SUCCESS)
+    special = nullptr;
   if (staged) {
     a.unitLo = lo * E / 16;
     a.unitsAll = (hi * E + 15) / 16;
     a.unitsFull = hi * E / 16;
-    return launch_staged(pick_staged(dtype, mode, op, stack), a, mode, stream);
+    return launch_staged(special ? special : pick_staged(dtype, mode, op, stack), a, mode,
+                         stream);
   }
   const long long NV = vec ? kGrainBytes / E : 1;
-  return launch(pick_kernel(dtype, mode, op, vec, stack, a.R), a, (hi + NV - 1) / NV - lo / NV,
-                stream);
+  return launch(special ? special : pick_kernel(dtype, mode, op, vec, stack, a.R), a,
+                (hi + NV - 1) / NV - lo / NV, stream);
 }
 
 // Per device: the two copy streams and three events of vr_allreduce_host,
@@ -694,8 +707,11 @@ vr_result_t vr_allreduce_trees(const void* const* sendbufs, void* const* recvbuf
     a.chanProg[c] = (uint8_t)found;
   }
   const bool vec = aligned16(sendbufs, R, 0) && aligned16(recvbufs, R, 0);
-  return launch_allreduce_range(a, dtype, kTreeAllReduce, op, stack, vec,
-                                vec && forced_path() == 2, 0, (long long)count, stream);
+  const int forced = forced_path();
+  const bool staged =
+      vec && forced != 1 && (forced == 2 || use_staged(kTreeAllReduce, R, count * E));
+  return launch_allreduce_range(a, dtype, kTreeAllReduce, op, stack, vec, staged, 0,
+                                (long long)count, stream);
 }
 
 vr_result_t vr_reduce_scatter(const void* const* sendbufs, void* const* recvbufs, int R,
@@ -869,6 +885,20 @@ const char* vr_get_error_string(vr_result_t result) {
     case VR_ERR_INTERNAL: return "internal error";
     default: return "unknown result";
   }
+}
+
+vr_result_t vr_jit_status(int* enabled, long long* compiled, long long* failed) {
+  if (!enabled || !compiled || !failed) return VR_ERR_INVALID_ARGUMENT;
+  *enabled = jit_enabled() ? 1 : 0;
+  jit_counts(compiled, failed);
+  return VR_SUCCESS;
+}
+
+vr_result_t vr_jit_compile_dtree(int nNodes, int localRanks, vr_dtype_t dtype, vr_op_t op,
+                                 int smArch, size_t* cubinBytes, char* log, size_t logBytes) {
+  if (!cubinBytes || !elem_size(dtype) || (op != VR_SUM && op != VR_MAX) || smArch < 90)
+    return VR_ERR_INVALID_ARGUMENT;
+  return jit_compile_dtree(nNodes, localRanks, dtype, op, smArch, cubinBytes, log, logBytes);
 }
 
 void vr_finalize(void) {

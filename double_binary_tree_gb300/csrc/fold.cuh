@@ -385,6 +385,27 @@ __device__ __forceinline__ typename Unit<T, NV>::Raw tree_fold(const Src& src, c
   return Ln::encode(top);
 }
 
+#ifdef VR_JIT_TREE
+// Defined by the run-time compiled source (jit.cc): the straight-line fold of
+// program t of the call's programs.
+template <typename T, int OP, int NV, class Src>
+__device__ __forceinline__ typename Unit<T, NV>::Raw jit_tree_fold(const Src& src, int t);
+#endif
+
+// The tree fold of program t: interpreted from its stream, or in a kernel
+// compiled at run time for this call's programs (VR_JIT_TREE), the same
+// steps as straight-line code -- the same operations in the same order.
+template <typename T, int OP, int NV, int S, class Src, int B = kBatch>
+__device__ __forceinline__ typename Unit<T, NV>::Raw tree_fold_t(const Src& src,
+                                                                const FoldProg* progs, int t,
+                                                                int R) {
+#ifdef VR_JIT_TREE
+  return jit_tree_fold<T, OP, NV, Src>(src, t);
+#else
+  return tree_fold<T, OP, NV, S, Src, B>(src, progs[t], R);
+#endif
+}
+
 // --------------------------------------------------------- partition math
 // Where element e sits: its channel range [lo, hi) and, for the ring, its
 // block [lo, hi) inside the loop with block number j.  Channels hold 16-byte

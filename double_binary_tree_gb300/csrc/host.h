@@ -15,6 +15,17 @@ vr_result_t build_dtree_ex(int nNodes, int L, int nCh, int pattern, const int* o
                            vr_tree_t* out);
 bool valid_tree(const vr_tree_t* tree, int R);
 vr_result_t compile_fold(const vr_tree_t* tree, int R, FoldProg* prog);
+vr_result_t dtree_programs(int nNodes, int L, FoldProg out[2]);
+
+// Tree kernel specialised at run time for a call's fold programs (jit.cc):
+// the shared-memory-staged one when `staged`, else the register-path one
+// (16-byte units; the few-rank variant when `small`).
+bool jit_enabled();
+vr_result_t jit_tree_kernel(int dtype, int op, int stack, bool small, bool staged,
+                            const FoldProg* progs, int nProgs, const void** out);
+void jit_counts(long long* compiled, long long* failed);
+vr_result_t jit_compile_dtree(int nNodes, int L, int dtype, int op, int arch,
+                              size_t* cubinBytes, char* log, size_t logBytes);
 
 // Kernel entry points, one getter per element type: `mode` is a Mode,
 // `vec` selects the 16-byte vector path (all buffers and block offsets

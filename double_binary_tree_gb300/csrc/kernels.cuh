@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(kBlock, SMALL ? kMinBlocksSmall
       const GlobalSrc src{s_src, e0 * E};
       typename Unit<T, NV>::Raw o;
       if constexpr (MODE == kTreeAllReduce)
-        o = tree_fold<T, OP, NV, S, GlobalSrc, B>(src, s_prog[cur.t], R);
+        o = tree_fold_t<T, OP, NV, S, GlobalSrc, B>(src, s_prog, cur.t, R);
       else
         o = ring_fold<T, OP, NV, GlobalSrc, B>(src, R, cur.j);
       for (int r = 0; r < R; ++r) Unit<T, NV>::store(s_dst[r] + e0 * E, o);

@@ -230,4 +230,15 @@ vr_result_t compile_fold(const vr_tree_t* tr, int R, FoldProg* p) {
   return VR_SUCCESS;
 }
 
+// The two fold programs of the double binary tree of (nNodes, localRanks):
+// tree 0 and tree 1 as channel 0 and channel 1 of vr_build_dtree see them.
+vr_result_t dtree_programs(int nNodes, int L, FoldProg out[2]) {
+  if (nNodes < 1 || L < 1 || nNodes * L > kMaxRanks) return VR_ERR_INVALID_ARGUMENT;
+  const int R = nNodes * L;
+  vr_tree_t trees[2 * kMaxRanks];
+  vr_result_t e = build_dtree(nNodes, L, 2, trees);
+  for (int t = 0; e == VR_SUCCESS && t < 2; ++t) e = compile_fold(trees + t * R, R, &out[t]);
+  return e;
+}
+
 }  // namespace vr

@@ -160,10 +160,12 @@ vr_result_t vr_ring_block(size_t count, vr_dtype_t dtype, int R, int nChannels,
  * chunkBytes (a positive multiple of 16) is the per-rank chunk C of a ring
  * loop and the chunk of a tree channel.
  * In place: sendbufs[r] == recvbufs[r] is allowed.
- * Buffers: any alignment.  16-byte aligned buffers run 16-byte units: the
- * ring with 8..32 ranks and at least 16 MiB per rank on a kernel that stages
- * each tile of all R ranks in shared memory with bulk asynchronous copies,
- * everything else on a kernel that loads the ranks' units into registers.  The
+ * Buffers: any alignment.  16-byte aligned buffers run 16-byte units: from
+ * 16 MiB per rank the ring with 8..32 ranks and the tree with 8..64 ranks run
+ * on a kernel that stages each tile of all R ranks in shared memory with bulk
+ * asynchronous copies (the tree's fold specialised at run time, see
+ * vr_jit_status), everything else on a kernel that loads the ranks' units
+ * into registers.  The
  * environment variable VR_KERNEL_PATH=staged|register (read on every call)
  * forces one of the two for testing and tuning; results are identical.
  * Unaligned buffers run element units on the register kernel.
@@ -351,6 +353,32 @@ vr_result_t vr_select_algo(int R, int localRanks, size_t bytesPerRank,
  * built-in one), e.g. one fitted to other hardware.  Errors:
  * VR_ERR_INVALID_ARGUMENT for negative or non-finite entries. */
 vr_result_t vr_set_cost_model(const vr_cost_model_t* model);
+
+/* ------------------------------------------ run-time specialised trees
+ * Tree AllReduce on 16-byte aligned buffers runs kernels compiled at run time
+ * (NVRTC, opened with dlopen) for the call's trees: the fold program of each
+ * tree ([Course13] "每种 rank 的操作", post-order) becomes straight-line code
+ * instead of an interpreted control stream, with the same operations in the
+ * same order, so results are unchanged.  Kernels are cached per architecture,
+ * element type, op and set of trees; the first call with new trees compiles
+ * them (about a second).  Without NVRTC, without the kernel sources beside
+ * the library, or with the environment variable VR_JIT=0 (read per call),
+ * the built-in interpreting kernels run. */
+
+/* Whether specialised trees are in use, and how many kernel sets were
+ * compiled and failed to compile or load so far.  Errors:
+ * VR_ERR_INVALID_ARGUMENT for a NULL output. */
+vr_result_t vr_jit_status(int* enabled, long long* compiled, long long* failed);
+
+/* Compiles, without loading or touching a device, the specialised kernels of
+ * vr_build_dtree(nNodes, localRanks, 2)'s two trees for sm_<smArch>a (e.g.
+ * 103) and returns the CUBIN size; the compiler log, if any, goes to `log`
+ * (logBytes, NUL-terminated, may be NULL / 0).  Errors:
+ * VR_ERR_INVALID_ARGUMENT for bad sizes, dtype, op or smArch < 90;
+ * VR_ERR_UNSUPPORTED when NVRTC or the kernel sources are not found;
+ * VR_ERR_INTERNAL when the compilation fails. */
+vr_result_t vr_jit_compile_dtree(int nNodes, int localRanks, vr_dtype_t dtype, vr_op_t op,
+                                 int smArch, size_t* cubinBytes, char* log, size_t logBytes);
 
 /* ------------------------------------------------------------- status */
 

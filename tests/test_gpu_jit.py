@@ -1,0 +1,74 @@
+"""Tree kernels specialised at run time (the straight-line folds compiled with
+NVRTC) against the interpreting kernels and the oracle: both bit-exact on
+the same inputs, on the register and the staged path."""
+
+import os
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+import workloads  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU runs deselect these
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import double_binary_tree_gb300 as vr  # noqa: E402
+
+TREE = vr.VR_ALGO_TREE
+
+
+def _run(inp, dtype, op, nch, cb, L, jit, path):
+    R, count = len(inp), inp[0].numel()
+    old = {k: os.environ.get(k) for k in ("VR_JIT", "VR_KERNEL_PATH")}
+    os.environ["VR_JIT"] = "1" if jit else "0"
+    os.environ["VR_KERNEL_PATH"] = path
+    try:
+        src = [t.cuda() for t in inp]
+        dst = [torch.empty_like(s) for s in src]
+        vr.vr_allreduce_ex(src, dst, R, count, dtype, op, TREE, nch, cb, L,
+                           torch.cuda.current_stream())
+        assert vr.vr_stream_status(torch.cuda.current_stream()) == 0
+        return [workloads.raw_numpy(d.cpu()) for d in dst]
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+def test_specialisation_is_available():
+    enabled, _, failed = vr.vr_jit_status()
+    assert enabled, "NVRTC or the kernel sources beside the library were not found"
+    assert failed == 0
+
+
+@pytest.mark.parametrize("path", ["register", "staged"])
+@pytest.mark.parametrize("nodes,L,dtype,op,count,nch", [
+    (2, 1, vr.VR_FLOAT32, vr.VR_SUM, 10007, 2),
+    (3, 1, vr.VR_BFLOAT16, vr.VR_SUM, 30011, 3),
+    (7, 1, vr.VR_FLOAT16, vr.VR_MAX, 65539, 2),
+    (8, 1, vr.VR_FLOAT32, vr.VR_MAX, 100003, 12),
+    (16, 1, vr.VR_BFLOAT16, vr.VR_SUM, 20011, 4),
+    (2, 4, vr.VR_FLOAT16, vr.VR_SUM, 9001, 5),
+    (8, 8, vr.VR_BFLOAT16, vr.VR_SUM, 12345, 12),
+])
+def test_specialised_equals_interpreted_equals_oracle(nodes, L, dtype, op, count, nch, path):
+    R = nodes * L
+    inp = workloads.generate(R, count, dtype, "normal", 300 + R)
+    want = oracle.allreduce([workloads.raw_numpy(t) for t in inp], dtype, op, TREE, nch, 1024,
+                            local_ranks=L)
+    _, compiled0, _ = vr.vr_jit_status()
+    got_jit = _run(inp, dtype, op, nch, 1024, L, True, path)
+    _, compiled1, failed = vr.vr_jit_status()
+    got_int = _run(inp, dtype, op, nch, 1024, L, False, path)
+    assert failed == 0
+    assert compiled1 >= compiled0
+    for r in range(R):
+        assert np.array_equal(got_jit[r], want[r]), "specialised rank %d" % r
+        assert np.array_equal(got_int[r], want[r]), "interpreted rank %d" % r

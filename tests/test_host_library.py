@@ -365,3 +365,25 @@ def test_allreduce_host_argument_errors():
     # count == 0 enqueues nothing
     h(FAKE[:4], FAKE_R[:4], 4, 0, F32, SUM, RING, 1, 16, 1, W[:4], 0)
     assert vr.vr_launch_count() == before
+
+
+# ------------------------------------------------ run-time specialised trees
+@pytest.mark.parametrize("nodes,L,dtype,op", [(1, 8, vr.VR_FLOAT32, vr.VR_SUM),
+                                              (7, 1, vr.VR_BFLOAT16, vr.VR_MAX),
+                                              (2, 4, vr.VR_FLOAT16, vr.VR_SUM)])
+def test_specialised_tree_kernels_compile_for_sm103a(nodes, L, dtype, op):
+    """The generated straight-line folds compile (NVRTC, no device) with the
+    kernel sources beside the library."""
+    enabled, _, _ = vr.vr_jit_status()
+    if not enabled:
+        pytest.skip("NVRTC or the kernel sources not found")
+    assert vr.vr_jit_compile_dtree(nodes, L, dtype, op, 103) > 0
+
+
+def test_specialised_tree_argument_errors():
+    INV = vr.VR_ERR_INVALID_ARGUMENT
+    assert _err(vr.vr_jit_compile_dtree, 1, 8, 7, vr.VR_SUM, 103) == INV
+    assert _err(vr.vr_jit_compile_dtree, 1, 8, vr.VR_FLOAT32, 5, 103) == INV
+    assert _err(vr.vr_jit_compile_dtree, 1, 8, vr.VR_FLOAT32, vr.VR_SUM, 80) == INV
+    assert _err(vr.vr_jit_compile_dtree, 0, 8, vr.VR_FLOAT32, vr.VR_SUM, 103) == INV
+    assert _err(vr.vr_jit_compile_dtree, 9, 8, vr.VR_FLOAT32, vr.VR_SUM, 103) == INV
