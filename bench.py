@@ -27,7 +27,8 @@ job value is the sum of the work over the max time across ranks.
 the same workload, metric and unit, each step a bounded sample.
 
 --sweep prints the ring vs tree sweep (R=4, 8 B .. 256 MiB per rank, fp32,
-12 channels, 512 KiB chunks) as JSON lines instead.
+12 channels, 512 KiB chunks) as JSON lines instead, then the alpha-beta
+model fitted to it (vr_fit_cost_model) and its crossover.
 """
 
 import argparse
@@ -543,6 +544,7 @@ def sweep(args):
     g = torch.Generator(device=dev)
     g.manual_seed(3)
     size = 8
+    rows = []
     while size <= 256 * 1024 * 1024:
         count = size // 4
         nbytes = ar_bytes(R, count, 0)
@@ -564,8 +566,24 @@ def sweep(args):
         row["winner"] = "tie" if hi / lo - 1 < 0.05 else (
             "ring" if row["ring_us"] < row["tree_us"] else "tree")
         print(json.dumps(row), flush=True)
+        rows.append(row)
         del bufs
         size *= 2
+    # The pages' alpha-beta model fitted to these times (the library's own
+    # relative least squares), its crossover, and how well it predicts.
+    n = len(rows)
+    sizes = [r["bytes_per_rank"] for r in rows]
+    fit = vr.vr_fit_cost_model([R] * n, [1] * n, sizes, [r["ring_us"] for r in rows],
+                               [r["tree_us"] for r in rows])
+    err = {}
+    for algo, name in ((0, "ring"), (1, "tree")):
+        rel = [vr.vr_predict_us(algo, R, 1, r["bytes_per_rank"], fit) / r[name + "_us"] - 1
+               for r in rows if r["bytes_per_rank"] >= (1 << 20)]
+        err[name] = round(max(abs(x) for x in rel), 4)
+    print(json.dumps({"fit": {"alpha_us": {"ring": fit[0][0], "tree": fit[0][1]},
+                              "us_per_byte": {"ring": fit[1][0], "tree": fit[1][1]}},
+                      "crossover_bytes_per_rank": vr.vr_crossover_bytes(R, 1, fit),
+                      "max_rel_error_from_1mib": err}), flush=True)
 
 
 def main():

@@ -64,6 +64,9 @@ _SIGNATURES = {
     "vr_predict_us": (I, [I, I, I, S, P(vr_cost_model_t), P(ctypes.c_double)]),
     "vr_select_algo": (I, [I, I, S, P(vr_cost_model_t), P(I)]),
     "vr_set_cost_model": (I, [P(vr_cost_model_t)]),
+    "vr_fit_cost_model": (I, [I, P(I), P(I), P(S), P(ctypes.c_double), P(ctypes.c_double),
+                              P(vr_cost_model_t)]),
+    "vr_crossover_bytes": (I, [I, I, P(vr_cost_model_t), P(ctypes.c_double)]),
     "vr_jit_status": (I, [P(I), P(ctypes.c_longlong), P(ctypes.c_longlong)]),
     "vr_jit_compile_dtree": (I, [I, I, I, I, I, P(S), ctypes.c_char_p, S]),
     "vr_stream_status": (I, [VP]),
@@ -270,6 +273,27 @@ def vr_select_algo(R, localRanks, bytesPerRank, model=None):
                                ctypes.byref(m) if m is not None else None, ctypes.byref(out)),
            "vr_select_algo")
     return out.value
+
+
+def vr_fit_cost_model(R, localRanks, bytesPerRank, ringUs, treeUs):
+    """Sequences of equal length; returns ((alpha_ring, alpha_tree),
+    (per_byte_ring, per_byte_tree))."""
+    n = len(R)
+    D = ctypes.c_double
+    out = vr_cost_model_t()
+    _check(_L().vr_fit_cost_model(n, (I * n)(*R), (I * n)(*localRanks), (S * n)(*bytesPerRank),
+                                  (D * n)(*ringUs), (D * n)(*treeUs), ctypes.byref(out)),
+           "vr_fit_cost_model")
+    return (tuple(out.alphaUs), tuple(out.usPerByte))
+
+
+def vr_crossover_bytes(R, localRanks, model=None):
+    """Bytes per rank where ring and tree predictions meet, or None."""
+    out = ctypes.c_double()
+    m = _model(model)
+    _check(_L().vr_crossover_bytes(R, localRanks, ctypes.byref(m) if m is not None else None,
+                                   ctypes.byref(out)), "vr_crossover_bytes")
+    return None if out.value < 0 else out.value
 
 
 def vr_set_cost_model(model=None):

@@ -657,6 +657,62 @@ vr_result_t vr_select_algo(int R, int localRanks, size_t bytesPerRank,
   return VR_SUCCESS;
 }
 
+vr_result_t vr_fit_cost_model(int n, const int* R, const int* localRanks,
+                              const size_t* bytesPerRank, const double* ringUs,
+                              const double* treeUs, vr_cost_model_t* out) {
+  if (n < 2 || !R || !localRanks || !bytesPerRank || !ringUs || !treeUs || !out)
+    return VR_ERR_INVALID_ARGUMENT;
+  // Each sample's prediction is alpha * stages + perByte * traffic, linear in
+  // the two unknowns: the model with alpha = 1, perByte = 0 gives `stages`,
+  // the one with alpha = 0, perByte = 1 gives `traffic`.
+  const vr_cost_model_t unitA = {{1.0, 1.0}, {0.0, 0.0}};
+  const vr_cost_model_t unitB = {{0.0, 0.0}, {1.0, 1.0}};
+  vr_cost_model_t m;
+  for (int alg = 0; alg < 2; ++alg) {
+    const double* t = alg == 0 ? ringUs : treeUs;
+    double ss = 0, sb = 0, bb = 0, s1 = 0, b1 = 0;
+    int used = 0;
+    for (int i = 0; i < n; ++i) {
+      if (!(t[i] > 0)) continue;
+      double st = 0, tr = 0;
+      vr_result_t e = vr_predict_us((vr_algo_t)alg, R[i], localRanks[i], bytesPerRank[i], &unitA,
+                                    &st);
+      if (e == VR_SUCCESS)
+        e = vr_predict_us((vr_algo_t)alg, R[i], localRanks[i], bytesPerRank[i], &unitB, &tr);
+      if (e != VR_SUCCESS) return e;
+      // relative error: divide the row and its target (the time) by the time
+      const double x = st / t[i], y = tr / t[i];
+      ss += x * x; sb += x * y; bb += y * y; s1 += x; b1 += y;
+      ++used;
+    }
+    const double det = ss * bb - sb * sb;
+    if (used < 2 || !(std::fabs(det) > 1e-300 * (ss * bb + 1e-300)) || !std::isfinite(det))
+      return VR_ERR_INVALID_ARGUMENT;
+    m.alphaUs[alg] = (s1 * bb - b1 * sb) / det;
+    m.usPerByte[alg] = (ss * b1 - sb * s1) / det;
+  }
+  *out = m;
+  return VR_SUCCESS;
+}
+
+vr_result_t vr_crossover_bytes(int R, int localRanks, const vr_cost_model_t* model,
+                               double* bytes) {
+  if (!bytes) return VR_ERR_INVALID_ARGUMENT;
+  // Both predictions are lines in the message size M: evaluate each at M = 0
+  // and M = 1 GiB (far apart, so the slopes lose no precision) and intersect.
+  const size_t far = (size_t)1 << 30;
+  double r0 = 0, r1 = 0, t0 = 0, t1 = 0;
+  vr_result_t e = vr_predict_us(VR_ALGO_RING, R, localRanks, 0, model, &r0);
+  if (e == VR_SUCCESS) e = vr_predict_us(VR_ALGO_RING, R, localRanks, far, model, &r1);
+  if (e == VR_SUCCESS) e = vr_predict_us(VR_ALGO_TREE, R, localRanks, 0, model, &t0);
+  if (e == VR_SUCCESS) e = vr_predict_us(VR_ALGO_TREE, R, localRanks, far, model, &t1);
+  if (e != VR_SUCCESS) return e;
+  const double slope = ((r1 - r0) - (t1 - t0)) / (double)far;
+  const double m = slope != 0 ? (t0 - r0) / slope : -1.0;
+  *bytes = m > 0 && std::isfinite(m) ? m : -1.0;
+  return VR_SUCCESS;
+}
+
 vr_result_t vr_set_cost_model(const vr_cost_model_t* model) {
   if (model)
     for (int i = 0; i < 2; ++i)

@@ -349,6 +349,27 @@ vr_result_t vr_predict_us(vr_algo_t algo, int R, int localRanks, size_t bytesPer
 vr_result_t vr_select_algo(int R, int localRanks, size_t bytesPerRank,
                            const vr_cost_model_t* model, vr_algo_t* algo);
 
+/* Fits the model to measured AllReduce times: sample i ran R[i] ranks in
+ * nodes of localRanks[i], bytesPerRank[i] each, in ringUs[i] and treeUs[i]
+ * microseconds (a value <= 0 leaves that algorithm's sample out).  For each
+ * algorithm, (alphaUs, usPerByte) minimises the sum of squared relative
+ * errors (predicted / measured - 1)^2, so that short and long messages count
+ * alike -- the pages give the model's form, not its constants.  On noisy data
+ * a fitted parameter can come out negative (vr_set_cost_model refuses it).
+ * Errors: VR_ERR_INVALID_ARGUMENT for n < 2, NULL arrays, a bad R /
+ * localRanks, or fewer than two usable samples (or a singular system) for an
+ * algorithm. */
+vr_result_t vr_fit_cost_model(int n, const int* R, const int* localRanks,
+                              const size_t* bytesPerRank, const double* ringUs,
+                              const double* treeUs, vr_cost_model_t* out);
+
+/* The message size per rank at which the ring and tree predictions are equal
+ * under `model` (NULL: the current model), from the closed form of the two
+ * lines; *bytes = -1 when they do not cross at a positive size.  Errors as
+ * vr_predict_us. */
+vr_result_t vr_crossover_bytes(int R, int localRanks, const vr_cost_model_t* model,
+                               double* bytes);
+
 /* Installs `model` as the current model for this process (NULL restores the
  * built-in one), e.g. one fitted to other hardware.  Errors:
  * VR_ERR_INVALID_ARGUMENT for negative or non-finite entries. */

@@ -387,3 +387,68 @@ def test_specialised_tree_argument_errors():
     assert _err(vr.vr_jit_compile_dtree, 1, 8, vr.VR_FLOAT32, vr.VR_SUM, 80) == INV
     assert _err(vr.vr_jit_compile_dtree, 0, 8, vr.VR_FLOAT32, vr.VR_SUM, 103) == INV
     assert _err(vr.vr_jit_compile_dtree, 9, 8, vr.VR_FLOAT32, vr.VR_SUM, 103) == INV
+
+
+@pytest.mark.parametrize("R,L", [(4, 1), (8, 1), (16, 4), (64, 8)])
+@pytest.mark.parametrize("model", [None, OTHER])
+def test_crossover_matches_oracle(R, L, model):
+    (a0, a1), (b0, b1) = model or BUILTIN
+    want = ocost.crossover(R, _oracle_depth(R, L), (a0, b0), (a1, b1))
+    got = vr.vr_crossover_bytes(R, L, model)
+    if want is None:
+        assert got is None
+    else:
+        assert got == pytest.approx(want, rel=1e-9)
+
+
+def _samples(rng):
+    Rs, Ls, Ms = [], [], []
+    for R, L in ((4, 1), (8, 1), (16, 4), (64, 8), (7, 1)):
+        for M in (8, 4096, 1 << 16, 1 << 20, 1 << 24, 1 << 28):
+            Rs.append(R); Ls.append(L); Ms.append(int(M * (1 + rng.random())))
+    return Rs, Ls, Ms
+
+
+def test_fit_recovers_a_planted_model():
+    rng = np.random.default_rng(5)
+    Rs, Ls, Ms = _samples(rng)
+    (a0, a1), (b0, b1) = (0.7, 1.9), (1.3e-6, 7.5e-7)
+    ring = [ocost.t_ring(R, M, a0, b0) for R, M in zip(Rs, Ms)]
+    tree = [ocost.t_tree(_oracle_depth(R, L), M, a1, b1) for R, L, M in zip(Rs, Ls, Ms)]
+    (fa0, fa1), (fb0, fb1) = vr.vr_fit_cost_model(Rs, Ls, Ms, ring, tree)
+    assert (fa0, fa1) == pytest.approx((a0, a1), rel=1e-9)
+    assert (fb0, fb1) == pytest.approx((b0, b1), rel=1e-9)
+
+
+def test_fit_minimises_relative_squared_error():
+    """Noisy times: the fit equals the least-squares solution of the rows
+    (stages, traffic) / t against 1, from numpy; samples <= 0 are left out."""
+    rng = np.random.default_rng(6)
+    Rs, Ls, Ms = _samples(rng)
+    ring = [ocost.t_ring(R, M, 0.6, 1.2e-6) * (1 + 0.2 * rng.standard_normal())
+            for R, M in zip(Rs, Ms)]
+    tree = [ocost.t_tree(_oracle_depth(R, L), M, 0.8, 9e-7) * (1 + 0.2 * rng.standard_normal())
+            for R, L, M in zip(Rs, Ls, Ms)]
+    tree[3] = 0.0                              # left out
+    got = vr.vr_fit_cost_model(Rs, Ls, Ms, ring, tree)
+    for alg, t in ((0, ring), (1, tree)):
+        rows, rhs = [], []
+        for R, L, M, ti in zip(Rs, Ls, Ms, t):
+            if ti <= 0:
+                continue
+            s, b = (ocost.ring_terms(R, M) if alg == 0 else
+                    ocost.tree_terms(_oracle_depth(R, L), M))
+            rows.append([s / ti, b / ti])
+            rhs.append(1.0)
+        sol = np.linalg.lstsq(np.array(rows), np.array(rhs), rcond=None)[0]
+        assert got[0][alg] == pytest.approx(sol[0], rel=1e-7)
+        assert got[1][alg] == pytest.approx(sol[1], rel=1e-7)
+
+
+def test_fit_argument_errors():
+    with pytest.raises(vr.VrError):
+        vr.vr_fit_cost_model([8], [1], [1024], [1.0], [1.0])           # n < 2
+    with pytest.raises(vr.VrError):
+        vr.vr_fit_cost_model([8, 8], [1, 1], [1024, 1024], [1.0, 2.0], [1.0, 0.0])  # 1 tree sample
+    with pytest.raises(vr.VrError):
+        vr.vr_fit_cost_model([8, 6], [1, 4], [1024, 2048], [1.0, 2.0], [1.0, 2.0])  # 6 % 4
