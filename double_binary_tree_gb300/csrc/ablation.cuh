@@ -38,8 +38,8 @@ __global__ void __launch_bounds__(kBlock, kMinBlocksTree) tree_up_kernel(const _
   const int R = a.R;
   const long long count = a.count;
   const long long units = (count + NV - 1) / NV;
-  const long long ub = units * blockIdx.x / gridDim.x;
-  const long long ue = units * (blockIdx.x + 1) / gridDim.x;
+  const long long ub = udiv(units * blockIdx.x, gridDim.x);
+  const long long ue = udiv(units * (blockIdx.x + 1), gridDim.x);
   Cursor cur{0, -1, 0, 0, 0, 0, 0};
   for (long long u = ub + threadIdx.x; u < ue; u += blockDim.x) {
     const long long e0 = u * NV;
@@ -71,8 +71,8 @@ __global__ void __launch_bounds__(kBlock) tree_down_kernel(const __grid_constant
   const int R = a.R;
   const long long count = a.count;
   const long long units = (count + NV - 1) / NV;
-  const long long ub = units * blockIdx.x / gridDim.x;
-  const long long ue = units * (blockIdx.x + 1) / gridDim.x;
+  const long long ub = udiv(units * blockIdx.x, gridDim.x);
+  const long long ue = udiv(units * (blockIdx.x + 1), gridDim.x);
   Cursor cur{0, -1, 0, 0, 0, 0, 0};
   for (long long u = ub + threadIdx.x; u < ue; u += blockDim.x) {
     const long long e0 = u * NV;
@@ -125,8 +125,8 @@ __global__ void __launch_bounds__(kBlock)
   char* fifo = static_cast<char*>(a.scratch);
   const long long count = a.count;
   const long long units = (count + NV - 1) / NV;
-  const long long ub = units * blockIdx.x / gridDim.x;
-  const long long ue = units * (blockIdx.x + 1) / gridDim.x;
+  const long long ub = udiv(units * blockIdx.x, gridDim.x);
+  const long long ue = udiv(units * (blockIdx.x + 1), gridDim.x);
   Cursor cur{0, -1, 0, 0, 0, 0, 0};
   for (long long u = ub + threadIdx.x; u < ue; u += blockDim.x) {
     const long long e0 = u * NV;
@@ -185,8 +185,8 @@ __global__ void __launch_bounds__(kBlock) copy_ranks_kernel(const __grid_constan
   const long long bytes = a.count;  // per rank
   const long long per = (bytes + NB - 1) / NB;
   const long long units = per * R;
-  const long long ub = units * blockIdx.x / gridDim.x;
-  const long long ue = units * (blockIdx.x + 1) / gridDim.x;
+  const long long ub = udiv(units * blockIdx.x, gridDim.x);
+  const long long ue = udiv(units * (blockIdx.x + 1), gridDim.x);
   for (long long u = ub + threadIdx.x; u < ue; u += blockDim.x) {
     const int r = (int)(u / per);
     if (s_src[r] == s_dst[r]) continue;

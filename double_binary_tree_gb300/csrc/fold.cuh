@@ -420,6 +420,13 @@ struct Cursor {
   int m;
 };
 
+// a / b for 0 <= a, 0 < b: 32-bit division when both fit (any message under
+// 4 Gi elements per rank), the much longer 64-bit sequence otherwise.
+__device__ __forceinline__ long long udiv(long long a, long long b) {
+  return ((unsigned long long)(a | b) >> 32) == 0 ? (long long)((unsigned)a / (unsigned)b)
+                                                  : a / b;
+}
+
 template <int U>
 __device__ __forceinline__ void locate_channel(const KArgs& a, long long e, int& k,
                                                long long& cs, long long& ce) {
@@ -427,10 +434,10 @@ __device__ __forceinline__ void locate_channel(const KArgs& a, long long e, int&
   const long long big = a.gm * (a.gq + 1);
   long long gs;
   if (g < big) {
-    k = (int)(g / (a.gq + 1));
+    k = (int)udiv(g, a.gq + 1);
     gs = (long long)k * (a.gq + 1);
   } else {
-    k = (int)(a.gm + (g - big) / a.gq);
+    k = (int)(a.gm + udiv(g - big, a.gq));
     gs = big + (long long)(k - a.gm) * a.gq;
   }
   const long long len = a.gq + (k < a.gm ? 1 : 0);
@@ -452,17 +459,17 @@ __device__ __forceinline__ void locate(const KArgs& a, long long e, Cursor& c) {
     const long long R = a.R;
     const long long LC = R * a.chunk;
     const long long off = e - cs;
-    const long long ls = (off / LC) * LC;
+    const long long ls = udiv(off, LC) * LC;
     const long long L = min(LC, (ce - cs) - ls);
     const long long w = off - ls;
-    const long long q = L / R, m = L % R;
+    const long long q = udiv(L, R), m = L - q * R;
     long long j, bs, bl;
     if (w < m * (q + 1)) {
-      j = w / (q + 1);
+      j = udiv(w, q + 1);
       bs = j * (q + 1);
       bl = q + 1;
     } else {
-      j = m + (w - m * (q + 1)) / q;
+      j = m + udiv(w - m * (q + 1), q);
       bs = m * (q + 1) + (j - m) * q;
       bl = q;
     }

@@ -61,12 +61,12 @@ __global__ void __launch_bounds__(kWarpSize) allgather_tma_kernel(const __grid_c
 
   const long long bytes = a.count;
   const long long perRank = (bytes + kGatherTile - 1) / kGatherTile;
-  const long long tb = a.tiles * blockIdx.x / gridDim.x;
-  const long long te = a.tiles * (blockIdx.x + 1) / gridDim.x;
+  const long long tb = udiv(a.tiles * blockIdx.x, gridDim.x);
+  const long long te = udiv(a.tiles * (blockIdx.x + 1), gridDim.x);
   for (long long i = 0; tb + i < te; ++i) {
     const int s = (int)(i % kGatherStages);
     const long long t = tb + i;
-    const int r = (int)(t / perRank);
+    const int r = (int)udiv(t, perRank);
     const long long off = (t - (long long)r * perRank) * kGatherTile;
     const unsigned n = (unsigned)min((long long)kGatherTile, bytes - off);
     const uint32_t buf = smem_addr(stage[s]);

@@ -68,8 +68,8 @@ __global__ void __launch_bounds__(kBlock, SMALL ? kMinBlocksSmall
   const long long count = a.hi;  // end of this launch's range of the message
   const long long u0 = a.lo / NV;
   const long long units = (count + NV - 1) / NV - u0;
-  const long long ub = u0 + units * blockIdx.x / gridDim.x;
-  const long long ue = u0 + units * (blockIdx.x + 1) / gridDim.x;
+  const long long ub = u0 + udiv(units * blockIdx.x, gridDim.x);
+  const long long ue = u0 + udiv(units * (blockIdx.x + 1), gridDim.x);
   Cursor cur{0, -1, 0, 0, 0, 0, 0};
   for (long long u = ub + threadIdx.x; u < ue; u += blockDim.x) {
     const long long e0 = u * NV;
@@ -116,8 +116,8 @@ __global__ void __launch_bounds__(kBlock, kMinBlocksRing)
   const long long rc = a.count;
   const long long per = (rc + NV - 1) / NV;
   const long long units = per * R;
-  const long long ub = units * blockIdx.x / gridDim.x;
-  const long long ue = units * (blockIdx.x + 1) / gridDim.x;
+  const long long ub = udiv(units * blockIdx.x, gridDim.x);
+  const long long ue = udiv(units * (blockIdx.x + 1), gridDim.x);
   for (long long u = ub + threadIdx.x; u < ue; u += blockDim.x) {
     const int b = (int)(u / per);
     const long long p0 = (u - (long long)b * per) * NV;
@@ -149,8 +149,8 @@ __global__ void __launch_bounds__(kBlock) allgather_kernel(const __grid_constant
   const long long bytes = a.count;
   const long long per = (bytes + NB - 1) / NB;
   const long long units = per * R;
-  const long long ub = units * blockIdx.x / gridDim.x;
-  const long long ue = units * (blockIdx.x + 1) / gridDim.x;
+  const long long ub = udiv(units * blockIdx.x, gridDim.x);
+  const long long ue = udiv(units * (blockIdx.x + 1), gridDim.x);
   for (long long u = ub + threadIdx.x; u < ue; u += blockDim.x) {
     const int r = (int)(u / per);
     const long long off = (u - (long long)r * per) * NB;

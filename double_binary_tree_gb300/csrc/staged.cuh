@@ -164,8 +164,8 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
   }
   __syncthreads();
 
-  const long long tb = a.tiles * blockIdx.x / gridDim.x;
-  const long long te = a.tiles * (blockIdx.x + 1) / gridDim.x;
+  const long long tb = udiv(a.tiles * blockIdx.x, gridDim.x);
+  const long long te = udiv(a.tiles * (blockIdx.x + 1), gridDim.x);
   const long long n = te - tb;
 
   if (warp == 0) {
