@@ -32,9 +32,10 @@ std::map<std::pair<int, int>, std::array<FoldProg, 2>> g_progs;  // (nNodes, loc
 std::map<std::pair<const void*, int>, int> g_smemSet;            // (kernel, device) -> bytes
 std::atomic<long long> g_stallNext{-1};                          // test hook
 
-// The alpha-beta cost model: built-in constants fitted on GB300 (4 ranks,
-// 8 B .. 256 MiB per rank), replaceable through vr_set_cost_model.
-const vr_cost_model_t kBuiltinModel = {{0.58989, 0.79715}, {1.17824e-6, 8.81738e-7}};
+// The alpha-beta cost model: built-in constants fitted on GB300 with
+// vr_fit_cost_model to the measured times of 4 ranks, 8 B .. 256 MiB per rank
+// (bench.py --sweep); replaceable through vr_set_cost_model.
+const vr_cost_model_t kBuiltinModel = {{0.698237, 0.626768}, {9.11290e-7, 6.66176e-7}};
 vr_cost_model_t g_model = kBuiltinModel;
 
 // Exact depth (edges from the root to the deepest leaf) of one tree.
