@@ -69,6 +69,7 @@ _SIGNATURES = {
     "vr_crossover_bytes": (I, [I, I, P(vr_cost_model_t), P(ctypes.c_double)]),
     "vr_jit_status": (I, [P(I), P(ctypes.c_longlong), P(ctypes.c_longlong)]),
     "vr_jit_compile_dtree": (I, [I, I, I, I, I, P(S), ctypes.c_char_p, S]),
+    "vr_jit_compile_ring": (I, [I, I, I, I, P(S), ctypes.c_char_p, S]),
     "vr_stream_status": (I, [VP]),
     "vr_launch_count": (ctypes.c_ulonglong, []),
     "vr_debug_stall_next": (I, [ctypes.c_longlong]),
@@ -319,6 +320,16 @@ def vr_jit_compile_dtree(nNodes, localRanks, dtype, op, smArch=103):
                                      log, len(log))
     if code != 0:
         raise VrError(code, "vr_jit_compile_dtree: " + log.value.decode(errors="replace")[:2000])
+    return size.value
+
+
+def vr_jit_compile_ring(R, dtype, op, smArch=103):
+    """Compile-only: CUBIN bytes of the specialised ring kernels for R ranks."""
+    size = ctypes.c_size_t()
+    log = ctypes.create_string_buffer(8192)
+    code = _L().vr_jit_compile_ring(R, dtype, op, smArch, ctypes.byref(size), log, len(log))
+    if code != 0:
+        raise VrError(code, "vr_jit_compile_ring: " + log.value.decode(errors="replace")[:2000])
     return size.value
 
 

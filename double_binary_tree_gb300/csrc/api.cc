@@ -365,6 +365,15 @@ vr_result_t launch_allreduce_range(KArgs& a, int dtype, int mode, int op, int st
       jit_tree_kernel(dtype, op, stack, use_small(dtype, mode, vec, stack, a.R), staged, a.prog,
                       a.nProgs, &special) != VR_SUCCESS)
     special = nullptr;
+  // The ring specialised for R ranks: measured 6-12% faster on the register
+  // path for 3-16 ranks, neutral on the staged one (VR_JIT_RING=1 also takes
+  // it there, 0 turns it off).
+  const unsigned jr = env_uint("VR_JIT_RING", 2);
+  if (mode == kRingAllReduce && vec && a.R >= 3 && a.R <= 16 && jr != 0 &&
+      (!staged || jr == 1) && jit_enabled() &&
+      jit_ring_kernel(dtype, op, a.R, use_small(dtype, mode, vec, stack, a.R), staged,
+                      &special) != VR_SUCCESS)
+    special = nullptr;
   if (staged) {
     a.unitLo = lo * E / 16;
     a.unitsAll = (hi * E + 15) / 16;
@@ -956,6 +965,13 @@ vr_result_t vr_jit_compile_dtree(int nNodes, int localRanks, vr_dtype_t dtype, v
   if (!cubinBytes || !elem_size(dtype) || (op != VR_SUM && op != VR_MAX) || smArch < 90)
     return VR_ERR_INVALID_ARGUMENT;
   return jit_compile_dtree(nNodes, localRanks, dtype, op, smArch, cubinBytes, log, logBytes);
+}
+
+vr_result_t vr_jit_compile_ring(int R, vr_dtype_t dtype, vr_op_t op, int smArch,
+                                size_t* cubinBytes, char* log, size_t logBytes) {
+  if (!cubinBytes || !elem_size(dtype) || (op != VR_SUM && op != VR_MAX) || smArch < 90)
+    return VR_ERR_INVALID_ARGUMENT;
+  return jit_compile_ring(R, dtype, op, smArch, cubinBytes, log, logBytes);
 }
 
 void vr_finalize(void) {

@@ -406,6 +406,25 @@ __device__ __forceinline__ typename Unit<T, NV>::Raw tree_fold_t(const Src& src,
 #endif
 }
 
+#ifdef VR_JIT_RING
+// Defined by the run-time compiled source (jit.cc) for one rank count: the
+// ranks' units loaded in rank order, folded in the rotation of block j.
+template <typename T, int OP, int NV, class Src>
+__device__ __forceinline__ typename Unit<T, NV>::Raw jit_ring_fold(const Src& src, int j);
+#endif
+
+// The ring fold of block j (ranks j, j+1, ..., j-1): the loop above, or in a
+// kernel compiled at run time for the call's rank count (VR_JIT_RING), the
+// same folds with the loads' ranks fixed at compile time.
+template <typename T, int OP, int NV, class Src, int B = kBatch>
+__device__ __forceinline__ typename Unit<T, NV>::Raw ring_fold_t(const Src& src, int R, int j) {
+#ifdef VR_JIT_RING
+  return jit_ring_fold<T, OP, NV, Src>(src, j);
+#else
+  return ring_fold<T, OP, NV, Src, B>(src, R, j);
+#endif
+}
+
 // --------------------------------------------------------- partition math
 // Where element e sits: its channel range [lo, hi) and, for the ring, its
 // block [lo, hi) inside the loop with block number j.  Channels hold 16-byte

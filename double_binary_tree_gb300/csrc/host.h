@@ -23,9 +23,13 @@ vr_result_t dtree_programs(int nNodes, int L, FoldProg out[2]);
 bool jit_enabled();
 vr_result_t jit_tree_kernel(int dtype, int op, int stack, bool small, bool staged,
                             const FoldProg* progs, int nProgs, const void** out);
+// The ring AllReduce kernel specialised for R ranks (the same variants).
+vr_result_t jit_ring_kernel(int dtype, int op, int R, bool small, bool staged, const void** out);
 void jit_counts(long long* compiled, long long* failed);
 vr_result_t jit_compile_dtree(int nNodes, int L, int dtype, int op, int arch,
                               size_t* cubinBytes, char* log, size_t logBytes);
+vr_result_t jit_compile_ring(int R, int dtype, int op, int arch, size_t* cubinBytes, char* log,
+                             size_t logBytes);
 
 // Kernel entry points, one getter per element type: `mode` is a Mode,
 // `vec` selects the 16-byte vector path (all buffers and block offsets

@@ -189,6 +189,37 @@ bool generate(const FoldProg* progs, int nProgs, std::string* src) {
   return true;
 }
 
+// The ring fold of one rank count R: the R units loaded in rank order
+// (static ranks: the pointer table is read once, not per load), then block
+// j's rotation j, j+1, ..., j-1 folded left to right from them -- the
+// interpreter's folds, one straight-line case per j.
+bool generate_ring(int R, std::string* src) {
+  if (R < 1 || R > kMaxRanks) return false;
+  std::string s =
+      "#define VR_JIT_RING 1\n"
+      "#include \"kernels.cuh\"\n"
+      "#include \"staged.cuh\"\n"
+      "namespace vr {\n"
+      "#define VR_J_FOLD(v) { typename Ln::L x_[Ln::N]; Ln::decode(v, x_); "
+      "_Pragma(\"unroll\") for (int e_ = 0; e_ < Ln::N; ++e_) acc[e_] = Ln::op(acc[e_], x_[e_]); }\n"
+      "template <typename T, int OP, int NV, class Src>\n"
+      "__device__ __forceinline__ typename Unit<T, NV>::Raw jit_ring_fold(const Src& src, int j) {\n"
+      "  typedef Lanes<T, OP, NV> Ln;\n";
+  for (int r = 0; r < R; ++r)
+    s += "  const typename Unit<T, NV>::Raw v" + std::to_string(r) + " = load_unit<T, NV>(src, " +
+         std::to_string(r) + ");\n";
+  s += "  typename Ln::L acc[Ln::N];\n  switch (j) {\n";
+  for (int j = 0; j < R; ++j) {
+    s += j == 0 ? "  default:\n  case 0:\n" : "  case " + std::to_string(j) + ":\n";
+    s += "    Ln::decode(v" + std::to_string(j) + ", acc);\n";
+    for (int k = 1; k < R; ++k) s += "    VR_J_FOLD(v" + std::to_string((j + k) % R) + ")\n";
+    s += "    break;\n";
+  }
+  s += "  }\n  return Ln::encode(acc);\n}\n}  // namespace vr\n";
+  *src = s;
+  return true;
+}
+
 // ------------------------------------------------------------------ cache
 struct Entry {
   bool ok = false;
@@ -210,20 +241,24 @@ std::string cache_key(int arch, int dtype, int op, int stack, bool small, const 
 
 // Compiles the register-path and staged tree kernels of `progs` for sm_<arch>a
 // into a CUBIN.  Returns the lowered names in `names`.
-bool compile(int arch, int dtype, int op, int stack, bool small, int kind, const FoldProg* progs,
-             int nProgs, std::string* cubin, std::string* name, std::string* log) {
+// mode: kTreeAllReduce (progs, nProgs, stack) or kRingAllReduce (R).
+bool compile(int arch, int dtype, int op, int mode, int stack, bool small, int kind,
+             const FoldProg* progs, int nProgs, int R, std::string* cubin, std::string* name,
+             std::string* log) {
   const Nvrtc& n = nvrtc();
   const std::string dir = source_dir();
   const char* T = type_name(dtype);
   if (!n.ok || dir.empty() || !T || (op != VR_SUM && op != VR_MAX)) return false;
   std::string src;
-  if (!generate(progs, nProgs, &src)) return false;
+  if (mode == kTreeAllReduce ? !generate(progs, nProgs, &src) : !generate_ring(R, &src))
+    return false;
   const int S = stack <= 4 ? 4 : 8;
+  const std::string M = std::to_string(mode);
   const std::string expr =
-      kind == 0 ? std::string("vr::allreduce_kernel<") + T + ", " + std::to_string(op) +
-                      ", 1, true, " + std::to_string(S) + (small ? ", true>" : ", false>")
-                : std::string("vr::staged_kernel<") + T + ", " + std::to_string(op) + ", 1, " +
-                      std::to_string(S) + ">";
+      kind == 0 ? std::string("vr::allreduce_kernel<") + T + ", " + std::to_string(op) + ", " +
+                      M + ", true, " + std::to_string(S) + (small ? ", true>" : ", false>")
+                : std::string("vr::staged_kernel<") + T + ", " + std::to_string(op) + ", " + M +
+                      ", " + std::to_string(S) + ">";
   nvrtcProgram prog;
   if (n.create(&prog, src.c_str(), "vr_jit_tree.cu", 0, nullptr, nullptr) != NVRTC_SUCCESS)
     return false;
@@ -263,24 +298,19 @@ bool jit_enabled() {
   return nvrtc().ok && !source_dir().empty();
 }
 
-vr_result_t jit_tree_kernel(int dtype, int op, int stack, bool small, bool staged,
-                            const FoldProg* progs, int nProgs, const void** out) {
-  int device = 0, major = 0, minor = 0;
-  if (cudaGetDevice(&device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess)
-    return VR_ERR_CUDA;
-  const int arch = major * 10 + minor;
-  const int kind = staged ? 1 : 0;
-  const std::string key =
-      std::to_string(kind) + "/" + cache_key(arch, dtype, op, stack, small && !staged, progs, nProgs);
+namespace {
+
+// The compiled kernel for `key`, compiling and loading it on first use.
+vr_result_t cached_kernel(const std::string& key, int dtype, int op, int mode, int stack,
+                          bool small, bool staged, const FoldProg* progs, int nProgs, int R,
+                          int arch, const void** out) {
   std::lock_guard<std::mutex> g(g_jitMu);
   auto it = g_cache.find(key);
   if (it == g_cache.end()) {
     Entry e;
     std::string cubin, name;
-    if (compile(arch, dtype, op, stack, small && !staged, kind, progs, nProgs, &cubin, &name,
-                nullptr) &&
+    if (compile(arch, dtype, op, mode, stack, small, staged ? 1 : 0, progs, nProgs, R, &cubin,
+                &name, nullptr) &&
         cudaLibraryLoadData(&e.lib, cubin.data(), nullptr, nullptr, 0, nullptr, nullptr, 0) ==
             cudaSuccess)
       e.ok = cudaLibraryGetKernel(&e.kernel, e.lib, name.c_str()) == cudaSuccess;
@@ -291,6 +321,43 @@ vr_result_t jit_tree_kernel(int dtype, int op, int stack, bool small, bool stage
   if (!it->second.ok) return VR_ERR_UNSUPPORTED;
   *out = reinterpret_cast<const void*>(it->second.kernel);
   return VR_SUCCESS;
+}
+
+vr_result_t device_arch(int* arch) {
+  int device = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess)
+    return VR_ERR_CUDA;
+  *arch = major * 10 + minor;
+  return VR_SUCCESS;
+}
+
+}  // namespace
+
+vr_result_t jit_tree_kernel(int dtype, int op, int stack, bool small, bool staged,
+                            const FoldProg* progs, int nProgs, const void** out) {
+  int arch = 0;
+  const vr_result_t e = device_arch(&arch);
+  if (e != VR_SUCCESS) return e;
+  small = small && !staged;
+  const std::string key = std::string(staged ? "t1/" : "t0/") +
+                          cache_key(arch, dtype, op, stack, small, progs, nProgs);
+  return cached_kernel(key, dtype, op, kTreeAllReduce, stack, small, staged, progs, nProgs, 0,
+                       arch, out);
+}
+
+vr_result_t jit_ring_kernel(int dtype, int op, int R, bool small, bool staged,
+                            const void** out) {
+  int arch = 0;
+  const vr_result_t e = device_arch(&arch);
+  if (e != VR_SUCCESS) return e;
+  small = small && !staged;
+  const std::string key = std::string(staged ? "r1/" : "r0/") + std::to_string(arch) + "/" +
+                          std::to_string(dtype) + "/" + std::to_string(op) + "/" +
+                          std::to_string(R) + (small ? "/s" : "/g");
+  return cached_kernel(key, dtype, op, kRingAllReduce, 0, small, staged, nullptr, 0, R, arch,
+                       out);
 }
 
 void jit_counts(long long* compiled, long long* failed) {
@@ -309,13 +376,36 @@ vr_result_t jit_compile_dtree(int nNodes, int L, int dtype, int op, int arch,
   const int stack = p[0].depth > p[1].depth ? p[0].depth : p[1].depth;
   if (!nvrtc().ok || source_dir().empty()) return VR_ERR_UNSUPPORTED;
   std::string cubin, name, text;
-  const bool ok = compile(arch, dtype, op, stack, false, 0, p, 2, &cubin, &name, &text);
+  const bool ok = compile(arch, dtype, op, kTreeAllReduce, stack, false, 0, p, 2, 0, &cubin,
+                          &name, &text);
   if (log && logBytes) {
     std::strncpy(log, text.c_str(), logBytes - 1);
     log[logBytes - 1] = 0;
   }
   if (!ok) return VR_ERR_INTERNAL;
   *cubinBytes = cubin.size();
+  return VR_SUCCESS;
+}
+
+// Compile-only check of the ring fold of R ranks (both kernel kinds).
+vr_result_t jit_compile_ring(int R, int dtype, int op, int arch, size_t* cubinBytes, char* log,
+                             size_t logBytes) {
+  if (R < 1 || R > kMaxRanks) return VR_ERR_INVALID_ARGUMENT;
+  if (!nvrtc().ok || source_dir().empty()) return VR_ERR_UNSUPPORTED;
+  std::string text;
+  *cubinBytes = 0;
+  for (int kind = 0; kind < 2; ++kind) {
+    std::string cubin, name;
+    if (!compile(arch, dtype, op, kRingAllReduce, 0, false, kind, nullptr, 0, R, &cubin, &name,
+                 &text)) {
+      if (log && logBytes) {
+        std::strncpy(log, text.c_str(), logBytes - 1);
+        log[logBytes - 1] = 0;
+      }
+      return VR_ERR_INTERNAL;
+    }
+    *cubinBytes += cubin.size();
+  }
   return VR_SUCCESS;
 }
 

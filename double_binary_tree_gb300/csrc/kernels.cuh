@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kBlock, SMALL ? kMinBlocksSmall
       if constexpr (MODE == kTreeAllReduce)
         o = tree_fold_t<T, OP, NV, S, GlobalSrc, B>(src, s_prog, cur.t, R);
       else
-        o = ring_fold<T, OP, NV, GlobalSrc, B>(src, R, cur.j);
+        o = ring_fold_t<T, OP, NV, GlobalSrc, B>(src, R, cur.j);
       for (int r = 0; r < R; ++r) Unit<T, NV>::store(s_dst[r] + e0 * E, o);
     } else if (MODE == kRingAllReduce && VEC && n == NV && e0 + NV <= cur.loopEnd &&
                e0 + NV <= cur.hi + cur.q + (cur.j + 1 < cur.m ? 1 : 0)) {

@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
             const SharedSrc src{base + 16 * lu, TB};
             typename Unit<T, U>::Raw o;
             if constexpr (MODE == kTreeAllReduce) o = tree_fold_t<T, OP, U, S>(src, s_prog, cur.t, R);
-            else o = ring_fold<T, OP, U>(src, R, cur.j);
+            else o = ring_fold_t<T, OP, U>(src, R, cur.j);
             for (int r = 0; r < R; ++r) Unit<T, U>::store(s_dst[r] + e0 * E, o);
           } else if (MODE == kRingAllReduce && e0 + U <= cur.loopEnd &&
                      e0 + U <= cur.hi + cur.q + (cur.j + 1 < cur.m ? 1 : 0)) {

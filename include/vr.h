@@ -401,6 +401,18 @@ vr_result_t vr_jit_status(int* enabled, long long* compiled, long long* failed);
 vr_result_t vr_jit_compile_dtree(int nNodes, int localRanks, vr_dtype_t dtype, vr_op_t op,
                                  int smArch, size_t* cubinBytes, char* log, size_t logBytes);
 
+/* The same for the ring fold of R ranks (register-path and staged kernels):
+ * the R ranks' units loaded in rank order, block j's rotation folded from
+ * them ([Interview] "手撕代码": block j starts at rank j), one straight-line
+ * case per j.  Register-path ring kernels of 16-byte aligned buffers with
+ * 3 <= R <= 16 use it (measured 6-12% faster; neutral on the staged kernel,
+ * which keeps the loop); the environment variable VR_JIT_RING=0 (read per
+ * call) turns it off, VR_JIT_RING=1 also applies it to the staged kernel.
+ * Errors as
+ * vr_jit_compile_dtree (R outside [1, VR_MAX_RANKS]: invalid). */
+vr_result_t vr_jit_compile_ring(int R, vr_dtype_t dtype, vr_op_t op, int smArch,
+                                size_t* cubinBytes, char* log, size_t logBytes);
+
 /* ------------------------------------------------------------- status */
 
 /* Synchronises `stream`, then returns and clears the current device's status

@@ -72,3 +72,38 @@ def test_specialised_equals_interpreted_equals_oracle(nodes, L, dtype, op, count
     for r in range(R):
         assert np.array_equal(got_jit[r], want[r]), "specialised rank %d" % r
         assert np.array_equal(got_int[r], want[r]), "interpreted rank %d" % r
+
+
+@pytest.mark.parametrize("path", ["register", "staged"])
+@pytest.mark.parametrize("R,dtype,op,count,nch,cb", [
+    (2, vr.VR_FLOAT32, vr.VR_SUM, 10007, 2, 64),
+    (3, vr.VR_BFLOAT16, vr.VR_MAX, 30011, 3, 48),
+    (4, vr.VR_FLOAT32, vr.VR_SUM, 65539, 12, 1024),
+    (7, vr.VR_FLOAT16, vr.VR_SUM, 100003, 5, 160),
+    (8, vr.VR_FLOAT32, vr.VR_SUM, 262147, 12, 4096),
+    (16, vr.VR_BFLOAT16, vr.VR_SUM, 40009, 4, 256),
+])
+def test_specialised_ring_equals_oracle(R, dtype, op, count, nch, cb, path):
+    """Ring folds specialised for R ranks (VR_JIT_RING=1) against the oracle:
+    blocks cut units (small chunks), so the split and element paths run too."""
+    inp = workloads.generate(R, count, dtype, "normal", 400 + R)
+    want = oracle.allreduce([workloads.raw_numpy(t) for t in inp], dtype, op,
+                            vr.VR_ALGO_RING, nch, cb)
+    old = {k: os.environ.get(k) for k in ("VR_JIT_RING", "VR_KERNEL_PATH")}
+    os.environ.update(VR_JIT_RING="1", VR_KERNEL_PATH=path)
+    try:
+        src = [t.cuda() for t in inp]
+        dst = [torch.empty_like(s) for s in src]
+        vr.vr_allreduce(src, dst, R, count, dtype, op, vr.VR_ALGO_RING, nch, cb,
+                        torch.cuda.current_stream())
+        assert vr.vr_stream_status(torch.cuda.current_stream()) == 0
+        got = [workloads.raw_numpy(d.cpu()) for d in dst]
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    assert vr.vr_jit_status()[2] == 0
+    for r in range(R):
+        assert np.array_equal(got[r], want[r]), "rank %d" % r

@@ -452,3 +452,12 @@ def test_fit_argument_errors():
         vr.vr_fit_cost_model([8, 8], [1, 1], [1024, 1024], [1.0, 2.0], [1.0, 0.0])  # 1 tree sample
     with pytest.raises(vr.VrError):
         vr.vr_fit_cost_model([8, 6], [1, 4], [1024, 2048], [1.0, 2.0], [1.0, 2.0])  # 6 % 4
+
+
+def test_specialised_ring_kernels_compile_for_sm103a():
+    enabled, _, _ = vr.vr_jit_status()
+    if not enabled:
+        pytest.skip("NVRTC or the kernel sources not found")
+    assert vr.vr_jit_compile_ring(4, vr.VR_FLOAT32, vr.VR_SUM, 103) > 0
+    with pytest.raises(vr.VrError):
+        vr.vr_jit_compile_ring(0, vr.VR_FLOAT32, vr.VR_SUM, 103)
