@@ -832,14 +832,30 @@ vr_result_t vr_allgather(const void* const* sendbufs, void* const* recvbufs, int
     DeviceInfo di;
     int device = 0;
     if ((e = device_info(&di, &device)) != VR_SUCCESS) return e;
-    const long long tile = gather_tile_bytes();
+    // geometry: tuning overrides VR_AG_TILE / VR_AG_STAGES / VR_AG_CTAS
+    const int tile = (int)env_uint("VR_AG_TILE", (unsigned)gather_tile_bytes());
+    const int stages = (int)env_uint("VR_AG_STAGES", (unsigned)gather_stages());
+    const int ctas = (int)std::max(1u, env_uint("VR_AG_CTAS", (unsigned)gather_ctas_per_sm()));
+    const void* fn = kernel_ptr_allgather_tma(tile, stages);
+    if (!fn) return VR_ERR_INVALID_ARGUMENT;
+    const size_t smem = (size_t)tile * stages;
+    {
+      std::lock_guard<std::mutex> g(g_mu);
+      int& set = g_smemSet[std::make_pair(fn, device)];
+      if (set < (int)smem) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+          return VR_ERR_CUDA;
+        set = (int)smem;
+      }
+    }
     a.tiles = (long long)R * (((long long)bytes + tile - 1) / tile);
     a.status = di.status;
     a.timeoutNs = wait_timeout_ns();
-    const long long grid = std::min<long long>(a.tiles, (long long)di.sms * gather_ctas_per_sm());
+    const long long grid = std::min<long long>(a.tiles, (long long)di.sms * ctas);
     void* args[] = {&a};
-    if (cudaLaunchKernel(kernel_ptr_allgather_tma(), dim3((unsigned)grid), dim3(32), args, 0,
-                         (cudaStream_t)stream) != cudaSuccess)
+    if (cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(32), args, smem, (cudaStream_t)stream) !=
+        cudaSuccess)
       return VR_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return VR_SUCCESS;

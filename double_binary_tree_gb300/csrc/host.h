@@ -41,8 +41,9 @@ const void* kernel_ptr_f16(int mode, int op, bool vec, int stack, bool small);
 const void* kernel_ptr_bf16(int mode, int op, bool vec, int stack, bool small);
 const void* kernel_ptr_allgather(bool vec);
 // TMA AllGather (16-byte aligned buffers): one warp per CTA.
-const void* kernel_ptr_allgather_tma();
+const void* kernel_ptr_allgather_tma(int tile, int stages);
 int gather_tile_bytes();
+int gather_stages();
 int gather_ctas_per_sm();
 const void* staged_kernel_ptr_f32(int mode, int op, int stack);
 const void* staged_kernel_ptr_f16(int mode, int op, int stack);

@@ -13,8 +13,16 @@ const void* kernel_ptr_allgather(bool vec) {
   return vec ? (const void*)allgather_kernel<true> : (const void*)allgather_kernel<false>;
 }
 
-const void* kernel_ptr_allgather_tma() { return (const void*)allgather_tma_kernel; }
+// TMA AllGather variants: (tile bytes, stages); nullptr for other pairs.
+const void* kernel_ptr_allgather_tma(int tile, int stages) {
+#define VR_AG(T, S) \
+  if (tile == T && stages == S) return (const void*)allgather_tma_kernel<T, S>;
+  VR_AG(8192, 4) VR_AG(8192, 8) VR_AG(16384, 4) VR_AG(16384, 6) VR_AG(32768, 3) VR_AG(4096, 8)
+#undef VR_AG
+  return nullptr;
+}
 int gather_tile_bytes() { return (int)kGatherTile; }
+int gather_stages() { return kGatherStages; }
 int gather_ctas_per_sm() { return kGatherCtasPerSm; }
 
 cudaError_t read_and_clear_status(unsigned* value) {
