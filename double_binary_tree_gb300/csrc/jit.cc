@@ -106,12 +106,17 @@ const Nvrtc& nvrtc() {
   return lib;
 }
 
-// The directory of the kernel sources: csrc/ beside this library.
-std::string source_dir() {
-  Dl_info info;
-  if (!dladdr(reinterpret_cast<void*>(&source_dir), &info) || !info.dli_fname) return "";
-  const std::string d = dir_of(info.dli_fname) + "/csrc";
-  return file_exists(d + "/kernels.cuh") ? d : std::string();
+// The directory of the kernel sources: csrc/ beside this library (looked up
+// once).
+const std::string& source_dir() {
+  static const std::string dir = [] {
+    Dl_info info;
+    if (!dladdr(reinterpret_cast<void*>(&source_dir), &info) || !info.dli_fname)
+      return std::string();
+    const std::string d = dir_of(info.dli_fname) + "/csrc";
+    return file_exists(d + "/kernels.cuh") ? d : std::string();
+  }();
+  return dir;
 }
 
 // ------------------------------------------------------------- generation
