@@ -155,19 +155,39 @@ vr_result_t check_buffers(const void* const* send, void* const* recv, int R, siz
       return VR_ERR_INVALID_ARGUMENT;
     if (((uintptr_t)send[r] | (uintptr_t)recv[r]) % E) return VR_ERR_INVALID_ARGUMENT;
   }
-  for (int r = 0; r < R; ++r) {
-    if (!recv[r]) continue;  // nothing received (only where nullRecvOk)
-    const uintptr_t s = (uintptr_t)send[r], d = (uintptr_t)recv[r];
-    bool inPlace = false;
-    if (kind == kAR) inPlace = d == s;
-    if (kind == kRS) inPlace = d == s + (uintptr_t)r * recvBytes;
-    if (kind == kAG) inPlace = s == d + (uintptr_t)r * sendBytes;
-    if (!inPlace && overlap(s, sendBytes, d, recvBytes)) return VR_ERR_INVALID_ARGUMENT;
-    for (int q = 0; q < R; ++q) {
-      if (q == r) continue;
-      if (recv[q] && overlap(d, recvBytes, (uintptr_t)recv[q], recvBytes))
-        return VR_ERR_INVALID_ARGUMENT;
-      if (overlap(d, recvBytes, (uintptr_t)send[q], sendBytes)) return VR_ERR_INVALID_ARGUMENT;
+  if (!recvBytes) return VR_SUCCESS;
+  // Receive buffers (all recvBytes long) sorted by address must be pairwise
+  // disjoint: each one ends before the next begins.
+  struct Iv {
+    uintptr_t lo;
+    int r;
+  };
+  Iv rv[kMaxRanks];
+  int n = 0;
+  for (int r = 0; r < R; ++r)
+    if (recv[r]) rv[n++] = Iv{(uintptr_t)recv[r], r};  // NULL: nothing received
+  std::sort(rv, rv + n, [](const Iv& x, const Iv& y) { return x.lo < y.lo; });
+  for (int i = 1; i < n; ++i)
+    if (rv[i].lo - rv[i - 1].lo < recvBytes) return VR_ERR_INVALID_ARGUMENT;
+  if (!sendBytes) return VR_SUCCESS;
+  // A send buffer may touch no receive buffer but its own rank's, and that
+  // one only in the collective's in-place position.  The receive buffers
+  // that overlap send[q] are consecutive in address order (equal lengths,
+  // disjoint): the first one ending after send[q] begins, and those after it
+  // that begin before send[q] ends.
+  for (int q = 0; q < R; ++q) {
+    const uintptr_t s = (uintptr_t)send[q];
+    int i = (int)(std::lower_bound(rv, rv + n, s,
+                                   [&](const Iv& x, uintptr_t v) { return x.lo + recvBytes <= v; }) -
+                  rv);
+    for (; i < n && rv[i].lo < s + sendBytes; ++i) {
+      if (rv[i].r != q) return VR_ERR_INVALID_ARGUMENT;
+      const uintptr_t d = rv[i].lo;
+      bool inPlace = false;
+      if (kind == kAR) inPlace = d == s;
+      if (kind == kRS) inPlace = d == s + (uintptr_t)q * recvBytes;
+      if (kind == kAG) inPlace = s == d + (uintptr_t)q * sendBytes;
+      if (!inPlace) return VR_ERR_INVALID_ARGUMENT;
     }
   }
   return VR_SUCCESS;

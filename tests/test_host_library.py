@@ -461,3 +461,68 @@ def test_specialised_ring_kernels_compile_for_sm103a():
     assert vr.vr_jit_compile_ring(4, vr.VR_FLOAT32, vr.VR_SUM, 103) > 0
     with pytest.raises(vr.VrError):
         vr.vr_jit_compile_ring(0, vr.VR_FLOAT32, vr.VR_SUM, 103)
+
+
+def _brute_force_ok(kind, send, recv, sb, rb):
+    """The buffer rules of include/vr.h, pair by pair."""
+    def ov(a, an, b, bn):
+        return an and bn and a < b + bn and b < a + an
+    R = len(send)
+    for r in range(R):
+        for q in range(R):
+            if q != r and (ov(recv[r], rb, recv[q], rb) or ov(recv[r], rb, send[q], sb)):
+                return False
+        inplace = {"ar": recv[r] == send[r], "rs": recv[r] == send[r] + r * rb,
+                   "ag": send[r] == recv[r] + r * sb}[kind]
+        if not inplace and ov(send[r], sb, recv[r], rb):
+            return False
+    return True
+
+
+@pytest.mark.parametrize("kind", ["ar", "rs", "ag"])
+def test_buffer_rules_match_brute_force(kind):
+    """Random layouts in a small address space (so that overlaps are common):
+    the library accepts exactly what the pairwise rules accept.  Accepted
+    calls go on to look for a device and fail there with another code."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        # accepted layouts hold fake pointers: they must never reach a launch
+        pytest.skip("runs only where no device can be reached")
+    rng = np.random.default_rng({"ar": 1, "rs": 2, "ag": 3}[kind])
+    INV = vr.VR_ERR_INVALID_ARGUMENT
+    E, base = 4, 1 << 24
+    seen = {True: 0, False: 0}
+    for trial in range(3000):
+        R = int(rng.integers(1, 9))
+        n = int(rng.integers(1, 5))                  # count per rank / per block
+        sb, rb = {"ar": (n * E, n * E), "rs": (R * n * E, n * E), "ag": (n * E, R * n * E)}[kind]
+        span = 4 * R * max(sb, rb)
+        send = [base + E * int(rng.integers(0, span // E)) for _ in range(R)]
+        recv = [base + E * int(rng.integers(0, span // E)) for _ in range(R)]
+        if rng.random() < 0.3:                       # plant in-place positions
+            for r in range(R):
+                if rng.random() < 0.7:
+                    if kind == "ar":
+                        recv[r] = send[r]
+                    elif kind == "rs":
+                        recv[r] = send[r] + r * rb
+                    else:
+                        send[r] = recv[r] + r * sb
+        want = _brute_force_ok(kind, send, recv, sb, rb)
+        if kind == "ar":
+            fn = lambda: vr.vr_allreduce_ex(send, recv, R, n, vr.VR_FLOAT32, vr.VR_SUM,  # noqa: E731
+                                            vr.VR_ALGO_RING, 1, 16, 1)
+        elif kind == "rs":
+            fn = lambda: vr.vr_reduce_scatter(send, recv, R, n, vr.VR_FLOAT32, vr.VR_SUM,  # noqa: E731
+                                              vr.VR_ALGO_RING, 1, 16)
+        else:
+            fn = lambda: vr.vr_allgather(send, recv, R, n, vr.VR_FLOAT32,  # noqa: E731
+                                         vr.VR_ALGO_RING, 1, 16)
+        try:
+            fn()
+            code = 0
+        except vr.VrError as e:
+            code = e.code
+        assert (code != INV) == want, (trial, R, n, send, recv)
+        seen[want] += 1
+    assert seen[True] > 100 and seen[False] > 100
