@@ -26,13 +26,40 @@
  *     ([Internals] "API 返回只意味着提交边界，不意味着数据已经可读").  Read the
  *     result only after synchronising the stream or through a stream-ordered
  *     dependency.
- *   - The library allocates no device memory.  The only library-owned device
- *     state is one status word per device (a __device__ variable).
+ *   - The library allocates no device buffers at run time.  Its own device
+ *     state is static: one status word per device and the 8 MiB FIFO of
+ *     vr_allreduce_ring_stepwise_noalloc (__device__ variables), plus the code
+ *     of kernels compiled at run time (vr_jit_status) and, once
+ *     vr_allreduce_host has run on a device, two streams and four events
+ *     there.  vr_finalize releases what is not static.
  *   - Reductions accumulate in fp32 for every dtype and narrow to the element
  *     type once, round-to-nearest-even.  Sum is IEEE fp32 addition in the
  *     schedule's order; Max returns the larger value, with +0 above -0.
  *   - Results are deterministic: the same call on the same inputs gives the
  *     same bits, and every rank's output is bit-identical.
+ *
+ * Environment overrides, for tests and tuning (read on every call unless
+ * noted; no override changes a result, only which kernel computes it):
+ *   VR_KERNEL_PATH=staged|register  force the shared-memory-staged or the
+ *                                   register-path AllReduce kernel
+ *   VR_JIT=0                        interpreting tree / ring folds only
+ *   VR_JIT_RING=0|1                 ring folds specialised: never / also on
+ *                                   the staged kernel
+ *   VR_SMALL_RANKS=0                no few-rank register-path variant
+ *   VR_STAGED_MIN_BYTES=n           staged kernel from n bytes per rank
+ *                                   (default 16 MiB)
+ *   VR_STAGED_TILE_BYTES, VR_STAGED_STAGES, VR_STAGED_MIN_STAGES
+ *                                   staged geometry: bytes per rank per
+ *                                   tile, most stages, fewest stages
+ *   VR_AG_TILE, VR_AG_STAGES, VR_AG_CTAS
+ *                                   TMA AllGather geometry (pairs of tile
+ *                                   and stages that are compiled: 8192/4,
+ *                                   8192/8, 16384/4, 16384/6, 32768/3,
+ *                                   4096/8; others are INVALID_ARGUMENT)
+ *   VR_WAIT_TIMEOUT_NS=n            (read once) limit of every bounded wait
+ *                                   (default 1 s)
+ *   VR_VALIDATE_POINTERS=1          (read once) check that every buffer is
+ *                                   reachable from the current device
  */
 #ifndef VR_H
 #define VR_H
