@@ -247,6 +247,26 @@ const void* pick_kernel(int dtype, int mode, int op, bool vec, int stack = 0, in
   }
 }
 
+// Launches `fn`; with programmatic stream serialisation (VR_PDL, read per
+// call) the kernel may start while the previous kernel on the stream drains
+// -- every kernel here waits for it (pdl_wait) before touching global memory.
+cudaError_t launch_kernel(const void* fn, dim3 grid, dim3 block, void** args, size_t smem,
+                          void* stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  if (env_uint("VR_PDL", 0)) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream,
                    void** extra = nullptr, int nExtra = 0) {
   if (!fn) return VR_ERR_INTERNAL;
@@ -263,8 +283,7 @@ vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream,
   const int grid = (int)std::max(1LL, std::min(resident, wanted));
   void* args[4] = {&a, nullptr, nullptr, nullptr};
   for (int i = 0; i < nExtra && i < 3; ++i) args[1 + i] = extra[i];
-  if (cudaLaunchKernel(fn, dim3(grid), dim3(kBlockThreads), args, 0, (cudaStream_t)stream) !=
-      cudaSuccess)
+  if (launch_kernel(fn, dim3(grid), dim3(kBlockThreads), args, 0, stream) != cudaSuccess)
     return VR_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return VR_SUCCESS;
@@ -342,8 +361,8 @@ vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
   a.injectStall = g_stallNext.exchange(-1);
   const int grid = (int)std::max(1LL, std::min<long long>(di.sms, a.tiles));
   void* args[] = {&a};
-  if (cudaLaunchKernel(fn, dim3(grid), dim3(32 * (a.consumers + 1)), args, smem,
-                       (cudaStream_t)stream) != cudaSuccess)
+  if (launch_kernel(fn, dim3(grid), dim3(32 * (a.consumers + 1)), args, smem, stream) !=
+      cudaSuccess)
     return VR_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return VR_SUCCESS;
@@ -874,8 +893,7 @@ vr_result_t vr_allgather(const void* const* sendbufs, void* const* recvbufs, int
     a.timeoutNs = wait_timeout_ns();
     const long long grid = std::min<long long>(a.tiles, (long long)di.sms * ctas);
     void* args[] = {&a};
-    if (cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(32), args, smem, (cudaStream_t)stream) !=
-        cudaSuccess)
+    if (launch_kernel(fn, dim3((unsigned)grid), dim3(32), args, smem, stream) != cudaSuccess)
       return VR_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return VR_SUCCESS;

@@ -27,6 +27,18 @@
 
 namespace vr {
 
+// Programmatic dependent launch.  A kernel launched with programmatic
+// stream serialisation may start while the previous kernel on its stream is
+// still running: pdl_launch lets the next kernel start early in the same
+// way, pdl_wait blocks until the previous kernel has finished and its memory
+// is visible.  Every kernel here calls pdl_wait after its prologue and
+// before touching global memory, so stream order is kept; for a kernel
+// launched without the attribute both are no-ops.
+__device__ __forceinline__ void pdl_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 template <bool C, class A, class B> struct Select { typedef A type; };
 template <class A, class B> struct Select<false, A, B> { typedef B type; };
 

@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(kWarpSize) allgather_tma_kernel(const __grid_c
   __shared__ char* s_dst[kMaxRanks];
   const int lane = threadIdx.x;
   const int R = a.R;
+  pdl_launch();
   for (int i = lane; i < R; i += kWarpSize) {
     s_src[i] = static_cast<const char*>(a.src[i]);
     s_dst[i] = static_cast<char*>(a.dst[i]);
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(kWarpSize) allgather_tma_kernel(const __grid_c
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncwarp();
+  pdl_wait();  // the previous kernel on the stream is done
 
   const long long bytes = a.count;
   const long long perRank = (bytes + TILE - 1) / TILE;

@@ -30,9 +30,13 @@ constexpr int kMinBlocksSmall = 3;
 
 // Rank pointers (and tree programs) copied to shared memory: they are indexed
 // by a runtime rank.
+// (Also the programmatic-launch handshake: the next kernel may start now,
+// and nothing below this call touches global memory before the previous
+// kernel is done.)
 template <int MODE>
 __device__ __forceinline__ void stage_args(const KArgs& a, const char** s_src, char** s_dst,
                                            FoldProg* s_prog) {
+  pdl_launch();
   for (int i = threadIdx.x; i < a.R; i += blockDim.x) {
     s_src[i] = static_cast<const char*>(a.src[i]);
     s_dst[i] = static_cast<char*>(a.dst[i]);
@@ -44,6 +48,7 @@ __device__ __forceinline__ void stage_args(const KArgs& a, const char** s_src, c
     for (int i = threadIdx.x; i < words; i += blockDim.x) to[i] = from[i];
   }
   __syncthreads();
+  pdl_wait();
 }
 
 // AllReduce, ring or tree.  VEC: 16-byte units (aligned buffers), else one

@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
   const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kStagedMaxStages);
 
   const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
+  pdl_launch();
   for (int i = threadIdx.x; i < R; i += blockDim.x) {
     s_src[i] = static_cast<const char*>(a.src[i]);
     s_dst[i] = static_cast<char*>(a.dst[i]);
@@ -163,6 +164,7 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
+  pdl_wait();  // the previous kernel on the stream is done
 
   const long long tb = udiv(a.tiles * blockIdx.x, gridDim.x);
   const long long te = udiv(a.tiles * (blockIdx.x + 1), gridDim.x);
