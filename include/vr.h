@@ -46,6 +46,11 @@
  *   VR_JIT_RING=0|1                 ring folds specialised: never / also on
  *                                   the staged kernel
  *   VR_SMALL_RANKS=0                no few-rank register-path variant
+ *   VR_PDL=0                        launch without programmatic stream
+ *                                   serialisation (by default a kernel may
+ *                                   start while the previous one on the
+ *                                   stream drains; it waits for it before
+ *                                   touching memory)
  *   VR_STAGED_MIN_BYTES=n           staged kernel from n bytes per rank
  *                                   (default 16 MiB)
  *   VR_STAGED_TILE_BYTES, VR_STAGED_STAGES, VR_STAGED_MIN_STAGES
