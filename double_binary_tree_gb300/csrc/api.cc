@@ -597,7 +597,12 @@ vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, 
                                  chunkBytes, localRanks, a, mode, stack);
   if (e != VR_SUCCESS || count == 0) return e;
   const size_t E = elem_size(dtype);
-  const bool vec = aligned16(sendbufs, R, 0) && aligned16(recvbufs, R, 0);
+  // Ring blocks shorter than a 16-byte unit (a channel of fewer grains than
+  // ranks) cut every unit several times, and the vector path folds such a
+  // unit element by element in one thread: the element kernel, one element
+  // per thread, is faster there (same order, same bits).
+  const bool tinyBlocks = mode == kRingAllReduce && a.gq < R;
+  const bool vec = aligned16(sendbufs, R, 0) && aligned16(recvbufs, R, 0) && !tinyBlocks;
   const int forced = forced_path();
   const bool staged = vec && forced != 1 && (forced == 2 || use_staged(mode, R, count * E));
   return launch_allreduce_range(a, dtype, mode, op, stack, vec, staged, 0, (long long)count,

@@ -544,3 +544,23 @@ def test_allreduce_host_null_receive_buffers():
     assert_status_ok()
     assert_bits_equal([workloads.raw_numpy(out0)], want[:1], "rank 0 copied out")
     assert_bits_equal([bits(w) for w in work], want, "workspace")
+
+
+# --------------------------------------------- back-to-back dependent calls
+@pytest.mark.parametrize("algo", [RING, TREE])
+@pytest.mark.parametrize("R,count,dtype", [(8, 1 << 22, F32), (4, 65539, BF16), (16, 300007, F16)])
+def test_in_place_chain_without_sync(algo, R, count, dtype, path):
+    """Three in-place AllReduces enqueued back to back with no host sync: each
+    reads what the previous one wrote (launches overlap, so every kernel must
+    wait for its predecessor before touching memory)."""
+    inp = workloads.generate(R, count, dtype, "uniform", 500 + R)
+    raws = [workloads.raw_numpy(t) for t in inp]
+    want = raws
+    for _ in range(3):
+        want = oracle.allreduce(want, dtype, SUM, algo, 12, 1 << 19)
+    bufs = [t.cuda() for t in inp]
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        vr.vr_allreduce(bufs, bufs, R, count, dtype, SUM, algo, 12, 1 << 19, st)
+    assert_status_ok()
+    assert_bits_equal([bits(b) for b in bufs], want, "chain")
