@@ -1,5 +1,5 @@
-// The C ABI of include/vr.h: argument checks, host planning and one kernel
-// launch per collective call.
+// The C ABI of include/vr.h: argument checks, host planning and the kernel
+// launches of each collective call (one for the fused collectives).
 #include <algorithm>
 #include <array>
 #include <atomic>
@@ -695,10 +695,21 @@ vr_result_t vr_predict_us(vr_algo_t algo, int R, int localRanks, size_t bytesPer
     *us = 2.0 * (N - 1) * m.alphaUs[0] + (2.0 * (N - 1) / N * M) * m.usPerByte[0];
     return VR_SUCCESS;
   }
-  vr_tree_t trees[2 * kMaxRanks];
-  vr_result_t e = build_dtree(R / localRanks, localRanks, 2, trees);
-  if (e != VR_SUCCESS) return e;
-  const int D = std::max(exact_depth(trees, R), exact_depth(trees + R, R));
+  int D = 0;
+  {
+    static std::map<std::pair<int, int>, int> depths;  // (R, localRanks) -> D
+    std::lock_guard<std::mutex> g(g_mu);
+    auto it = depths.find(std::make_pair(R, localRanks));
+    if (it == depths.end()) {
+      vr_tree_t trees[2 * kMaxRanks];
+      const vr_result_t e = build_dtree(R / localRanks, localRanks, 2, trees);
+      if (e != VR_SUCCESS) return e;
+      it = depths.emplace(std::make_pair(R, localRanks),
+                          std::max(exact_depth(trees, R), exact_depth(trees + R, R)))
+               .first;
+    }
+    D = it->second;
+  }
   *us = 2.0 * D * m.alphaUs[1] + (2.0 * M) * m.usPerByte[1];
   return VR_SUCCESS;
 }
