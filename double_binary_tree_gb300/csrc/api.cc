@@ -283,10 +283,19 @@ vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream,
   a.status = di.status;
   const long long resident = (long long)di.sms * blocks_per_sm(fn, device);
   const long long wanted = (units + kBlockThreads - 1) / kBlockThreads;
-  const int grid = (int)std::max(1LL, std::min(resident, wanted));
+  // Fewer units than 256-thread CTAs to cover every SM: smaller CTAs (a
+  // warp multiple), so that the work spreads over all SMs instead of
+  // queueing on a few (each SM's load bandwidth bounds a small call).
+  int block = kBlockThreads;
+  if (wanted < di.sms && env_uint("VR_SPREAD", 1)) {
+    const long long perSm = (units + di.sms - 1) / di.sms;
+    block = (int)std::min<long long>(kBlockThreads, std::max<long long>(32, (perSm + 31) / 32 * 32));
+  }
+  const long long grid =
+      std::max(1LL, std::min(resident, (units + block - 1) / block));
   void* args[4] = {&a, nullptr, nullptr, nullptr};
   for (int i = 0; i < nExtra && i < 3; ++i) args[1 + i] = extra[i];
-  if (launch_kernel(fn, dim3(grid), dim3(kBlockThreads), args, 0, stream) != cudaSuccess)
+  if (launch_kernel(fn, dim3((unsigned)grid), dim3(block), args, 0, stream) != cudaSuccess)
     return VR_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return VR_SUCCESS;
@@ -364,8 +373,9 @@ vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
   a.injectStall = g_stallNext.exchange(-1);
   const int grid = (int)std::max(1LL, std::min<long long>(di.sms, a.tiles));
   void* args[] = {&a};
-  if (launch_kernel(fn, dim3(grid), dim3(32 * (a.consumers + 1)), args, smem, stream) !=
-      cudaSuccess)
+  // (Overlapped launch measured neutral to 5% slower above 32 ranks.)
+  if (launch_kernel(fn, dim3(grid), dim3(32 * (a.consumers + 1)), args, smem, stream,
+                    a.R <= 32) != cudaSuccess)
     return VR_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return VR_SUCCESS;
@@ -597,11 +607,13 @@ vr_result_t vr_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, 
                                  chunkBytes, localRanks, a, mode, stack);
   if (e != VR_SUCCESS || count == 0) return e;
   const size_t E = elem_size(dtype);
-  // Ring blocks shorter than a 16-byte unit (a channel of fewer grains than
-  // ranks) cut every unit several times, and the vector path folds such a
-  // unit element by element in one thread: the element kernel, one element
-  // per thread, is faster there (same order, same bits).
-  const bool tinyBlocks = mode == kRingAllReduce && a.gq < R;
+  // Small rings run the element kernel, one element per thread (same order,
+  // same bits).  A latency-bound call lasts as long as its slowest thread,
+  // and in the vector path that is a thread whose unit a ring block boundary
+  // cuts (folded out of line, element by element when blocks are shorter
+  // than a unit).  Measured on GB300: faster up to 64 Ki elements per rank
+  // (R = 4 fp32, R = 8 bf16), slower from 128 Ki.
+  const bool tinyBlocks = mode == kRingAllReduce && (a.gq < R || count <= 65536);
   const bool vec = aligned16(sendbufs, R, 0) && aligned16(recvbufs, R, 0) && !tinyBlocks;
   const int forced = forced_path();
   const bool staged = vec && forced != 1 && (forced == 2 || use_staged(mode, R, count * E));
