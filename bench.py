@@ -480,6 +480,7 @@ PROFILE_CASES = {
     "tree_r8_bf16": ("ar", 8, 1, 2, 0, 1),
     "tree_r8_fp32": ("ar", 8, 1, 0, 0, 1),
     "ring_r4_fp32": ("ar", 4, 1, 0, 0, 0),
+    "tree_r4_fp32": ("ar", 4, 1, 0, 0, 1),
     "tree_r7_bf16": ("ar", 7, 1, 2, 0, 1),
     "tree_r64_fp16_hier": ("ar", 64, 8, 1, 0, 1),
     "tree_r64_fp16_hier_max": ("ar", 64, 8, 1, 1, 1),
