@@ -396,6 +396,15 @@ void fill_partition(KArgs& a, size_t count, size_t E, int nCh, size_t chunkBytes
   a.nCh = nCh;
   a.lo = 0;
   a.hi = (long long)count;
+  // reciprocals of the cursor's divisors (a.R is set by the caller)
+  auto recip = [](long long d) -> unsigned long long {
+    return d > 1 ? ~0ull / (unsigned long long)d + 1 : 0ull;
+  };
+  a.mGq1 = recip(a.gq + 1);
+  a.mGq = recip(a.gq);
+  a.mLC = recip((long long)a.R * a.chunk);
+  a.mR = recip(a.R);
+  a.mC = recip(a.chunk);
 }
 
 // The AllReduce kernel over the elements [lo, hi) of the message `a`

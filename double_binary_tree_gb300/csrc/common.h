@@ -54,6 +54,10 @@ struct KArgs {
   long long grains;     // AllReduce: 16-byte grains of the message
   long long gq, gm;     // grains / nChannels, grains % nChannels
   long long chunk;      // C, elements per rank per ring loop block
+  // 64-bit reciprocals of the partition's divisors (gq + 1, gq, R * chunk, R,
+  // chunk): n / d = high 64 bits of M * n for 32-bit n and d, M =
+  // floor((2^64 - 1) / d) + 1 (0 for d = 1, which divides trivially).
+  unsigned long long mGq1, mGq, mLC, mR, mC;
   long long lo, hi;     // AllReduce: the elements [lo, hi) this launch folds, a piece of the
                         // count-element message whose partition the fields above describe
                         // (lo at a 16-byte boundary); [0, count) for a whole message

@@ -458,6 +458,15 @@ __device__ __forceinline__ long long udiv(long long a, long long b) {
                                                   : a / b;
 }
 
+// n / d with d's reciprocal M (KArgs): one high multiply when both fit in
+// 32 bits (exact there: Lemire, Kaser and Kurz, "Faster remainder by direct
+// computation", 2019), a 64-bit division otherwise.
+__device__ __forceinline__ long long div_by(long long n, long long d, unsigned long long M) {
+  if (((unsigned long long)(n | d) >> 32) == 0)
+    return d == 1 ? n : (long long)__umul64hi(M, (unsigned long long)n);
+  return n / d;
+}
+
 template <int U>
 __device__ __forceinline__ void locate_channel(const KArgs& a, long long e, int& k,
                                                long long& cs, long long& ce) {
@@ -465,10 +474,10 @@ __device__ __forceinline__ void locate_channel(const KArgs& a, long long e, int&
   const long long big = a.gm * (a.gq + 1);
   long long gs;
   if (g < big) {
-    k = (int)udiv(g, a.gq + 1);
+    k = (int)div_by(g, a.gq + 1, a.mGq1);
     gs = (long long)k * (a.gq + 1);
   } else {
-    k = (int)(a.gm + udiv(g - big, a.gq));
+    k = (int)(a.gm + div_by(g - big, a.gq, a.mGq));
     gs = big + (long long)(k - a.gm) * a.gq;
   }
   const long long len = a.gq + (k < a.gm ? 1 : 0);
@@ -490,17 +499,19 @@ __device__ __forceinline__ void locate(const KArgs& a, long long e, Cursor& c) {
     const long long R = a.R;
     const long long LC = R * a.chunk;
     const long long off = e - cs;
-    const long long ls = udiv(off, LC) * LC;
+    const long long ls = div_by(off, LC, a.mLC) * LC;
     const long long L = min(LC, (ce - cs) - ls);
     const long long w = off - ls;
-    const long long q = udiv(L, R), m = L - q * R;
+    const long long q = div_by(L, R, a.mR), m = L - q * R;
     long long j, bs, bl;
     if (w < m * (q + 1)) {
       j = udiv(w, q + 1);
       bs = j * (q + 1);
       bl = q + 1;
     } else {
-      j = m + udiv(w - m * (q + 1), q);
+      // a full loop has blocks of exactly `chunk` elements
+      const long long rest = w - m * (q + 1);
+      j = m + (q == a.chunk ? div_by(rest, q, a.mC) : udiv(rest, q));
       bs = m * (q + 1) + (j - m) * q;
       bl = q;
     }
