@@ -4,8 +4,9 @@
  * R "virtual ranks" are R device buffers in one GPU's memory.  The library
  * computes what an AllReduce (ReduceScatter, AllGather) over R ranks
  * computes, following the ring and double-binary-tree schedules, and writes
- * every rank's result buffer.  Each collective call is one kernel launch on
- * the caller's stream; nothing crosses a GPU or process boundary.
+ * every rank's result buffer.  Each fused collective call is one kernel
+ * launch on the caller's stream (the host-buffer and non-fused variants
+ * enqueue several); nothing crosses a GPU or process boundary.
  *
  * Sources (web pages), cited below as [tag] "section":
  *   [Course13]  "NCCL 专家课程 13：Tree、双树、层次化连接与真实交叉区间" (blog.cptz.space)
