@@ -319,9 +319,25 @@ bool use_staged(int mode, int R, size_t bytesPerRank) {
   return false;
 }
 
+// ReduceScatter: one store per unit leaves the staged consumers little work
+// per tile, so their per-tile overhead shows unless tiles are large (64 KB
+// stages, see staged_tile_bytes).  Measured on GB300 from 16 MiB sent per
+// rank, fp32: 20% (8 ranks) to 37% (2 ranks) faster than the register path.
+// Above 8 ranks such tiles do not fit three stages, and for 16-bit types the
+// consumers' widening work makes the staged kernel slower (R = 8 bf16: 128
+// against 101 us): both stay on the register path.
+bool use_staged_rs(int R, int dtype, size_t sendBytesPerRank) {
+  return dtype == VR_FLOAT32 && R >= 2 && R <= 8 &&
+         sendBytesPerRank >= env_uint("VR_STAGED_MIN_BYTES", 16u << 20);
+}
+
 // Per-rank tile bytes of the staged kernel (bulk copies below 2 KB lose
-// throughput; 4 KB measured best for 9..16 ranks).
-unsigned staged_tile_bytes(int R) { return R > 8 && R <= 16 ? 4096u : 2048u; }
+// throughput; 4 KB measured best for 9..16 ranks; ReduceScatter: 64 KB stages
+// up to 16 KB per rank).
+unsigned staged_tile_bytes(int R, int mode) {
+  if (mode == kReduceScatter) return std::min(16384u, (65536u / (unsigned)R) & ~15u);
+  return R > 8 && R <= 16 ? 4096u : 2048u;
+}
 
 // Staged geometry: tiles of tileUnits 16-byte units per rank; as many stages
 // (at most 16) as fit in the opt-in shared memory; up to 7 consumer warps.
@@ -343,7 +359,7 @@ vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
   unsigned tb = env_uint("VR_STAGED_TILE_BYTES", 0);
   int minStages = (int)env_uint("VR_STAGED_MIN_STAGES", 3);
   if (!tb) {
-    tb = staged_tile_bytes(a.R);
+    tb = staged_tile_bytes(a.R, mode);
     while (tb > 512 && (long long)a.R * tb * minStages > room) tb >>= 1;
   }
   a.tileBytes = tb;
@@ -878,7 +894,7 @@ vr_result_t vr_reduce_scatter(const void* const* sendbufs, void* const* recvbufs
   a.chunk = (long long)(chunkBytes / E);
   const bool vec = aligned16(sendbufs, R, recvcount * E) && aligned16(recvbufs, R, 0);
   const int forced = forced_path();
-  if (vec && forced != 1 && (forced == 2 || use_staged(kReduceScatter, R, recvcount * E * R))) {
+  if (vec && forced != 1 && (forced == 2 || use_staged_rs(R, dtype, recvcount * E * R))) {
     a.unitsFull = (long long)(recvcount * E / 16);
     a.unitsAll = a.unitsFull;
     return launch_staged(pick_staged(dtype, kReduceScatter, op), a, kReduceScatter, stream);
