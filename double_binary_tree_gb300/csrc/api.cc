@@ -35,7 +35,7 @@ std::atomic<long long> g_stallNext{-1};                          // test hook
 // The alpha-beta cost model: built-in constants fitted on GB300 with
 // vr_fit_cost_model to the measured times of 4 ranks, 8 B .. 256 MiB per rank
 // (bench.py --sweep); replaceable through vr_set_cost_model.
-const vr_cost_model_t kBuiltinModel = {{0.358003, 0.489089}, {9.47561e-7, 6.56306e-7}};
+const vr_cost_model_t kBuiltinModel = {{0.344664, 0.486336}, {9.44218e-7, 6.54488e-7}};
 vr_cost_model_t g_model = kBuiltinModel;
 
 // Exact depth (edges from the root to the deepest leaf) of one tree.
