@@ -42,11 +42,14 @@
  * Environment overrides, for tests and tuning (read on every call unless
  * noted; no override changes a result, only which kernel computes it):
  *   VR_KERNEL_PATH=staged|register  force the shared-memory-staged or the
- *                                   register-path AllReduce kernel
+ *                                   register-path AllReduce / ReduceScatter
+ *                                   kernel (aligned buffers)
  *   VR_JIT=0                        interpreting tree / ring folds only
  *   VR_JIT_RING=0|1                 ring folds specialised: never / also on
  *                                   the staged kernel
  *   VR_SMALL_RANKS=0                no few-rank register-path variant
+ *   VR_SPREAD=0                     256-thread CTAs even when a small call
+ *                                   would leave SMs idle
  *   VR_PDL=0                        launch without programmatic stream
  *                                   serialisation (by default a kernel may
  *                                   start while the previous one on the
