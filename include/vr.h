@@ -201,10 +201,10 @@ vr_result_t vr_ring_block(size_t count, vr_dtype_t dtype, int R, int nChannels,
  * on a kernel that stages each tile of all R ranks in shared memory with bulk
  * asynchronous copies (the tree's fold specialised at run time, see
  * vr_jit_status), everything else on a kernel that loads the ranks' units
- * into registers.  The
- * environment variable VR_KERNEL_PATH=staged|register (read on every call)
- * forces one of the two for testing and tuning; results are identical.
- * Unaligned buffers run element units on the register kernel.
+ * into registers (rings of at most 64 Ki elements per rank: one element per
+ * thread).  The environment variable VR_KERNEL_PATH=staged|register (read on
+ * every call) forces one of the two for testing and tuning; results are
+ * identical.  Unaligned buffers run element units on the register kernel.
  * Errors (nothing enqueued): VR_ERR_INVALID_ARGUMENT for R outside
  * [1, VR_MAX_RANKS], NULL arrays, a NULL buffer with count > 0, a buffer not
  * aligned to the element size, a bad enum, bad nChannels or chunkBytes, or a
@@ -278,7 +278,9 @@ vr_result_t vr_allreduce_trees(const void* const* sendbufs, void* const* recvbuf
  * b+1, b+2, ..., b (mod R).  Only VR_ALGO_RING: tree implements AllReduce
  * only ([CodeNotes] "通讯时如何选择Channel"), so VR_ALGO_TREE returns
  * VR_ERR_UNSUPPORTED.  In place: recvbufs[r] == sendbufs[r] + r*recvcount
- * (in elements).  Other errors as vr_allreduce. */
+ * (in elements).  fp32 with 2..8 ranks from 16 MiB sent per rank runs the
+ * shared-memory-staged kernel (64 KB stages), everything else the register
+ * kernel.  Other errors as vr_allreduce. */
 vr_result_t vr_reduce_scatter(const void* const* sendbufs, void* const* recvbufs, int R,
                               size_t recvcount, vr_dtype_t dtype, vr_op_t op,
                               vr_algo_t algo, int nChannels, size_t chunkBytes,
