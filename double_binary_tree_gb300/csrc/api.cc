@@ -308,13 +308,13 @@ vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream,
 // and of ReduceScatter's 64-rank folds, and with few ranks its stages hold
 // too few bytes in flight.  Everything else runs on the register path.
 // Measured on GB300: from 16 MiB per rank the staged kernel beats the
-// register path for the ring of 8-32 ranks and, with its fold specialised at
+// register path for the ring of 8-64 ranks and, with its fold specialised at
 // run time (jit.cc), for the tree of 8-64 ranks (the interpreting staged tree
 // is 2-3x slower than the register path).
 bool use_staged(int mode, int R, size_t bytesPerRank) {
   const size_t minBytes = env_uint("VR_STAGED_MIN_BYTES", 16u << 20);
   if (R < 8 || bytesPerRank < minBytes) return false;
-  if (mode == kRingAllReduce) return R <= 32;
+  if (mode == kRingAllReduce) return true;
   if (mode == kTreeAllReduce) return jit_enabled();
   return false;
 }
@@ -357,10 +357,14 @@ vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
   // at least kMinStages stages in the opt-in shared memory.
   const int room = di.smemOptin - kStagedHeader;
   unsigned tb = env_uint("VR_STAGED_TILE_BYTES", 0);
-  int minStages = (int)env_uint("VR_STAGED_MIN_STAGES", 3);
+  // Above 32 ranks two stages with larger tiles (more consumer warps) beat
+  // three smaller ones: measured 2.5% (tree) to 20% (ring) faster at 64.
+  int minStages = (int)env_uint("VR_STAGED_MIN_STAGES", a.R > 32 ? 2 : 3);
   if (!tb) {
     tb = staged_tile_bytes(a.R, mode);
-    while (tb > 512 && (long long)a.R * tb * minStages > room) tb >>= 1;
+    if (a.R > 32 && mode != kReduceScatter)  // the largest 512-byte multiple that fits
+      tb = std::max(512u, ((unsigned)(room / (minStages * a.R))) & ~511u);
+    while (tb > 512 && (long long)a.R * tb * minStages > room) tb -= 512;
   }
   a.tileBytes = tb;
   a.tileUnits = (int)(tb / 16);

@@ -197,7 +197,7 @@ vr_result_t vr_ring_block(size_t count, vr_dtype_t dtype, int R, int nChannels,
  * loop and the chunk of a tree channel.
  * In place: sendbufs[r] == recvbufs[r] is allowed.
  * Buffers: any alignment.  16-byte aligned buffers run 16-byte units: from
- * 16 MiB per rank the ring with 8..32 ranks and the tree with 8..64 ranks run
+ * 16 MiB per rank the ring and the tree with 8..64 ranks run
  * on a kernel that stages each tile of all R ranks in shared memory with bulk
  * asynchronous copies (the tree's fold specialised at run time, see
  * vr_jit_status), everything else on a kernel that loads the ranks' units
