@@ -301,13 +301,10 @@ vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream,
   return VR_SUCCESS;
 }
 
-// Which kernel family serves an aligned collective.  Measured on GB300
-// (ring and tree, R = 2..64, 1..128 MiB per rank): the staged kernel wins
-// for the ring with 8..32 ranks and at least 16 MiB per rank; its consumer
-// warps are too few to hide the latency of the tree's data-dependent fold
-// and of ReduceScatter's 64-rank folds, and with few ranks its stages hold
-// too few bytes in flight.  Everything else runs on the register path.
-// Measured on GB300: from 16 MiB per rank the staged kernel beats the
+// Which kernel family serves an aligned AllReduce.  With few ranks the
+// staged kernel's stages hold too few bytes in flight, and below 16 MiB per
+// rank its pipeline does not fill.  Measured on GB300: from 16 MiB per rank
+// the staged kernel beats the
 // register path for the ring of 8-64 ranks and, with its fold specialised at
 // run time (jit.cc), for the tree of 8-64 ranks (the interpreting staged tree
 // is 2-3x slower than the register path).
