@@ -564,3 +564,43 @@ def test_in_place_chain_without_sync(algo, R, count, dtype, path):
         vr.vr_allreduce(bufs, bufs, R, count, dtype, SUM, algo, 12, 1 << 19, st)
     assert_status_ok()
     assert_bits_equal([bits(b) for b in bufs], want, "chain")
+
+
+# ------------------------------------------------------------- maximum size
+@pytest.mark.parametrize("algo", [RING, TREE])
+def test_more_than_2_pow_32_elements_per_rank(algo, path):
+    """R=2 x (2^32 + 37) bf16 per rank (8 GiB each; 32 GiB in all): element
+    indices and byte offsets past 32 bits.  Inputs are small integers, so
+    every result is an exact sum: checked for every element in chunks, and
+    bit-exact against the oracle at sampled elements (the first ones, around
+    2^31 and 2^32, the ragged tail)."""
+    free, _ = torch.cuda.mem_get_info()
+    if free < (40 << 30):
+        pytest.skip("needs 40 GiB of free device memory")
+    R, count, nch, cb = 2, (1 << 32) + 37, 12, 1 << 19
+    g = torch.Generator(device="cuda")
+    g.manual_seed(600)
+    src = [torch.empty(count, dtype=torch.bfloat16, device="cuda").random_(-8, 9, generator=g)
+           for _ in range(R)]
+    dst = [torch.empty_like(s) for s in src]
+    vr.vr_allreduce(src, dst, R, count, BF16, SUM, algo, nch, cb, torch.cuda.current_stream())
+    assert_status_ok()
+    step = 1 << 28
+    for lo in range(0, count, step):
+        hi = min(count, lo + step)
+        want = (src[0][lo:hi].float() + src[1][lo:hi].float()).to(torch.bfloat16)
+        for d in dst:
+            assert torch.equal(d[lo:hi].view(torch.int16), want.view(torch.int16)), lo
+    idx = sorted(set([0, 1, 7, 8, 9, (1 << 31) - 1, 1 << 31, (1 << 31) + 5, (1 << 32) - 8,
+                      (1 << 32) - 1, 1 << 32, (1 << 32) + 1, count - 1]
+                     + [int(x) for x in np.random.default_rng(1).integers(0, count, 40)]))
+    it = torch.tensor(idx, device="cuda")
+    vals = [workloads.raw_numpy(s[it].cpu()) for s in src]
+    got = workloads.raw_numpy(dst[1][it].cpu())
+    for n, e in enumerate(idx):
+        v = [numerics.to_f32(np.array([vals[r][n]]), BF16)[0] for r in range(R)]
+        from oracle import sample
+        f = sample.allreduce_element(v, e, count, BF16, SUM, algo, nch, cb)
+        assert numerics.from_f32(np.array([f], dtype=np.float32), BF16)[0] == got[n], e
+    del src, dst
+    torch.cuda.empty_cache()
