@@ -820,6 +820,7 @@ vr_result_t vr_allgather(const void* const* sendbufs, void* const* recvbufs, int
     a.tiles = (long long)R * (((long long)bytes + tile - 1) / tile);
     a.status = di.status;
     a.timeoutNs = wait_timeout_ns();
+    a.injectStall = g_stallNext.exchange(-1);
     const long long grid = std::min<long long>(a.tiles, (long long)di.sms * ctas);
     void* args[] = {&a};
     if (launch_kernel(fn, dim3((unsigned)grid), dim3(32), args, smem, stream, false) !=

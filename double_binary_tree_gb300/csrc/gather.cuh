@@ -83,7 +83,10 @@ __global__ void __launch_bounds__(kWarpSize) allgather_tma_kernel(const __grid_c
     __syncwarp();
     if (lane == 0) {
       mbar_arrive_expect_tx(smem_addr(&full[s]), n);
-      bulk_load(buf, s_src[r] + off, n, smem_addr(&full[s]));
+      // test hook: CTA 0 never loads its tile a.injectStall, so that wait
+      // runs out (the failure path, without any fault)
+      if (!(blockIdx.x == 0 && i == a.injectStall))
+        bulk_load(buf, s_src[r] + off, n, smem_addr(&full[s]));
     }
     const bool ok = __any_sync(~0u, wait_phase(smem_addr(&full[s]),
                                                (unsigned)((i / NS) & 1),

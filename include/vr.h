@@ -466,7 +466,8 @@ unsigned long long vr_launch_count(void);
 
 /* Test hook for the device-side failure path.  The next collective call
  * that runs a shared-memory-staged kernel (16-byte aligned AllReduce or
- * ReduceScatter) makes its first CTA skip the loads of its tile number
+ * ReduceScatter) or the TMA AllGather makes its first CTA skip the loads of
+ * its tile number
  * `tile`, so the wait for that tile runs out after the bounded-wait limit
  * (1 s, or VR_WAIT_TIMEOUT_NS nanoseconds from the environment at first
  * use): that call's results are incomplete and vr_stream_status reports

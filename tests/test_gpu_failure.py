@@ -1,7 +1,8 @@
 """Device-side failure detection without a GPU fault.
 
-The staged kernels bound every wait.  The library's test hook makes the
-first CTA of the next staged call skip the loads of one tile, so the wait for
+The staged kernels and the TMA AllGather bound every wait.  The library's
+test hook makes the first CTA of the next such call skip the loads of one
+tile, so the wait for
 that tile runs out: the call must report VR_ERR_TIMEOUT through
 vr_stream_status within about the wait limit (1 s), leave the context usable,
 and the next call must be bit-exact again.  Nothing here traps, faults or
@@ -77,3 +78,22 @@ def test_stall_request_is_consumed_once_and_cancellable():
     assert all(bool((d == 4).all()) for d in dst)
     with pytest.raises(vr.VrError):
         vr.vr_debug_stall_next(-2)
+
+
+def test_allgather_stalled_tile_times_out_and_recovers():
+    """The TMA AllGather's waits are bounded too: CTA 0 skips the load of its
+    first tile, the call reports VR_ERR_TIMEOUT, and the next call is exact."""
+    R, sc = 4, 1 << 20
+    src = [torch.full((sc,), float(r + 1), device="cuda") for r in range(R)]
+    dst = [torch.zeros(R * sc, device="cuda") for _ in range(R)]
+    stream = torch.cuda.current_stream()
+    vr.vr_debug_stall_next(0)
+    t0 = time.time()
+    vr.vr_allgather(src, dst, R, sc, vr.VR_FLOAT32, vr.VR_ALGO_RING, 12, 512 * 1024, stream)
+    assert vr.vr_stream_status(stream) == vr.VR_ERR_TIMEOUT
+    assert time.time() - t0 < 30
+    vr.vr_allgather(src, dst, R, sc, vr.VR_FLOAT32, vr.VR_ALGO_RING, 12, 512 * 1024, stream)
+    assert vr.vr_stream_status(stream) == 0
+    want = torch.cat(src)
+    for d in dst:
+        assert torch.equal(d, want)
