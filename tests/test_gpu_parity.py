@@ -604,3 +604,38 @@ def test_more_than_2_pow_32_elements_per_rank(algo, path):
         assert numerics.from_f32(np.array([f], dtype=np.float32), BF16)[0] == got[n], e
     del src, dst
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------- the sweep configuration, sampled
+@pytest.mark.parametrize("algo", [RING, TREE])
+@pytest.mark.parametrize("size", [8, 4096, 1 << 20, 64 << 20, 256 << 20])
+def test_sweep_configuration(size, algo):
+    """R=4 fp32, 12 channels, 512 KiB chunks, uniform [-1, 1) drawn on the
+    device as the sweep does: bit-exact to the oracle (every element up to
+    64 MiB per rank, 2000 sampled elements above) and every element within
+    the fp64 bound."""
+    R, count, nch, cb = 4, size // 4, 12, 512 * 1024
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    src = [torch.rand(count, generator=g, device="cuda") * 2 - 1 for _ in range(R)]
+    dst = [torch.empty_like(s) for s in src]
+    vr.vr_allreduce(src, dst, R, count, F32, SUM, algo, nch, cb, torch.cuda.current_stream())
+    assert_status_ok()
+    raws = [workloads.raw_numpy(s.cpu()) for s in src]
+    got = bits(dst[2])
+    if size <= (64 << 20):
+        want = oracle.allreduce(raws, F32, SUM, algo, nch, cb)
+        assert_bits_equal([bits(d) for d in dst], want, "sweep %d" % size)
+    else:
+        from oracle import sample
+        for d in dst[:2]:
+            assert torch.equal(d.view(torch.int32), dst[2].view(torch.int32))
+        idx = np.unique(np.concatenate([np.arange(8), np.arange(count - 8, count),
+                                        np.random.default_rng(size).integers(0, count, 1984)]))
+        for e in idx:
+            f = sample.allreduce_element([r[e] for r in raws], int(e), count, F32, SUM, algo,
+                                         nch, cb)
+            assert np.float32(f).view(np.uint32) == got[e].view(np.uint32), e
+    s = oracle.fp64_sum(raws, F32)
+    a = sum(np.abs(x.astype(np.float64)) for x in raws)
+    check_against_fp64(got, s, a, R, F32)
