@@ -3,21 +3,39 @@ on the CPU (monkeypatch, undone after the test), makes at least one pin of
 tests/test_oracle_pins.py fail.  A mutation that every pin let through would
 mean a mistake of that kind could hide in the oracle."""
 
+import inspect
+import textwrap
+
 import numpy as np
 import pytest
 
-from oracle import costmodel, numerics, partition, sample, topology
+import oracle
+from oracle import api, costmodel, numerics, partition, sample, schedules, topology
 from tests import test_oracle_pins as pins
 
 
 def _caught(checks):
-    """True when at least one check raises AssertionError."""
+    """True when at least one check fails: an assertion, or an error raised
+    by the mutated oracle (a tree that no longer reaches every rank, an index
+    out of range)."""
     for check in checks:
         try:
             check()
-        except AssertionError:
+        except Exception:
             return True
     return False
+
+
+def _rewrite(monkeypatch, module, name, old, new):
+    """Install, for the test's duration, module.name with the one occurrence
+    of ``old`` in its source replaced by ``new``."""
+    src = textwrap.dedent(inspect.getsource(getattr(module, name)))
+    assert src.count(old) == 1, (name, old)
+    ns = dict(vars(module))
+    exec(compile(src.replace(old, new), module.__file__, "exec"), ns)
+    if getattr(oracle, name, None) is getattr(module, name):   # re-exported by the package
+        monkeypatch.setattr(oracle, name, ns[name])
+    monkeypatch.setattr(module, name, ns[name])
 
 
 def test_btree_children_swapped(monkeypatch, golden):
@@ -123,6 +141,115 @@ def test_tree_traffic_halved(monkeypatch):
         return 2 * D, 1.0 * M
     monkeypatch.setattr(costmodel, "tree_terms", tree_terms)
     assert _caught([pins.test_cost_model_step_counts_and_traffic])
+
+
+# ------------------------------------------ one expression of the oracle changed
+# (module, function, original text, mutated text, the pins expected to catch it)
+REWRITES = [
+    ("ring sends to the left neighbour", schedules, "ring_allreduce_loop",
+     "dst = (r + 1) % R", "dst = (r - 1) % R",
+     ["test_ring_trace_figure1"]),
+    ("ring all-gather forwards the block one step early", schedules, "ring_allreduce_loop",
+     "(r + 1 - s) % R, held[r][(r + 1 - s) % R]", "(r - s) % R, held[r][(r - s) % R]",
+     ["test_ring_trace_figure1", "test_brute_force_exact_small_integers"]),
+    ("ReduceScatter uses the AllReduce block labels", schedules, "ring_reduce_scatter",
+     "(r - s - 1) % R, held[r][(r - s - 1) % R]", "(r - s) % R, held[r][(r - s) % R]",
+     ["test_reduce_scatter_blocks_and_order", "test_each_rank_contributes_once"]),
+    ("AllGather forwards the block it received last step", schedules, "ring_allgather",
+     "(r - s) % R, held[r][(r - s) % R]", "(r - s + 1) % R, held[r][(r - s + 1) % R]",
+     ["test_allgather_is_concatenation"]),
+    ("tree reduce leaves out the local input", schedules, "tree_allreduce_chunk",
+     "acc = xs[v][start:start + length].copy()", "acc = np.zeros(length, np.float32)",
+     ["test_each_rank_contributes_once", "test_two_rank_example"]),
+    ("tree broadcast forwards the child's own partial", schedules, "tree_allreduce_chunk",
+     "result[c] = result[v].copy()", "result[c] = partial[c].copy()",
+     ["test_each_rank_contributes_once", "test_brute_force_exact_small_integers"]),
+    ("tree folds children in reverse slot order", schedules, "tree_allreduce_chunk",
+     "for c in tree[v].down:\n                if c != -1:\n                    acc",
+     "for c in reversed(tree[v].down):\n                if c != -1:\n                    acc",
+     ["test_tree_local_first_then_children_in_slot_order"]),
+    ("first tree takes the smaller half of the channels", topology, "channel_tree_index",
+     "(n_channels + 1) // 2", "n_channels // 2",
+     ["test_channel_to_tree_split"]),
+    ("tree halves swapped", topology, "channel_tree_index",
+     "return 0 if channel", "return 1 if channel",
+     ["test_channel_to_tree_split"]),
+    ("children one level too far", topology, "btree",
+     "low = b >> 1", "low = b",
+     ["test_dtree4_figure", "test_hand_derived_trees_r8_r7", "test_tree_invariants"]),
+    ("parent falls back to setting the next bit only", topology, "btree",
+     "up = r ^ b\n", "up = r | (b << 1)\n",
+     ["test_dtree4_figure", "test_hand_derived_trees_r8_r7", "test_tree_invariants"]),
+    ("ring loop of one chunk instead of R", partition, "ring_blocks",
+     "step = R * chunk_elems", "step = chunk_elems",
+     ["test_partition_small_ring_case"]),
+    ("channels split in elements, not 16-byte grains", partition, "channel_ranges",
+     "grains = -(-count // U)", "grains, U = count, 1",
+     ["test_partition_covers_message"]),
+    ("fp16 narrowing rounds ties away from zero", numerics, "f32_to_f16_bits",
+     "(rem > half) | ((rem == half) & ((q & 1) == 1))", "rem >= half",
+     ["test_f16_rne_matches_numpy_and_torch"]),
+    ("fp16 narrowing ignores the subnormal range", numerics, "f32_to_f16_bits",
+     "d = np.maximum(13, 126 - e_eff)", "d = np.full_like(e_eff, 13)",
+     ["test_f16_rne_matches_numpy_and_torch"]),
+    ("fp16 widening with exponent bias 16", numerics, "f16_bits_to_f32",
+     "(np.maximum(e, 1) - 25)", "(np.maximum(e, 1) - 26)",
+     ["test_f16_rne_matches_numpy_and_torch"]),
+    ("fp64 sum accumulated in fp32", api, "fp64_sum",
+     "acc += x.astype(np.float64)", "acc = (acc.astype(np.float32) + x).astype(np.float64)",
+     ["test_fp64_sum_exact_where_fp64_is"]),
+    ("fp64 max starts from zero", api, "fp64_max",
+     "-np.inf", "0.0",
+     ["test_brute_force_exact_small_integers", "test_fp64_sum_exact_where_fp64_is"]),
+    ("sampler: element at a channel's end counted in the channel", sample, "channel_of",
+     "cs <= e < cs + cn", "cs < e <= cs + cn",
+     ["test_sampler_matches_literal_simulation"]),
+    ("sampler: tree children folded in reverse", sample, "tree_fold",
+     "for c in tree[v].down:", "for c in reversed(tree[v].down):",
+     ["test_sampler_matches_literal_simulation"]),
+    ("crossover of the wrong sign", costmodel, "crossover",
+     "m = num / den", "m = -num / den",
+     ["test_cost_model_crossover_matches_search"]),
+    ("tree cost model counts one pass of the tree", costmodel, "tree_terms",
+     "return 2 * D, 2.0 * M", "return D, 2.0 * M",
+     ["test_cost_model_step_counts_and_traffic"]),
+]
+
+
+def _pin_checks(names, golden):
+    """The named pins as zero-argument checks, over every parameter value of
+    their own ``parametrize`` marks (the golden fixture passed in)."""
+    import itertools
+    checks = []
+    for name in names:
+        fn = getattr(pins, name)
+        grid = {"golden": [golden]}
+        for mark in getattr(fn, "pytestmark", []):
+            if mark.name == "parametrize":
+                grid[mark.args[0]] = list(mark.args[1])
+        params = list(inspect.signature(fn).parameters)
+        for combo in itertools.product(*[grid[p] for p in params]):
+            checks.append(lambda fn=fn, kw=dict(zip(params, combo)): fn(**kw))
+    return checks
+
+
+@pytest.mark.parametrize("what,module,name,old,new,catchers", REWRITES,
+                         ids=[r[0] for r in REWRITES])
+def test_rewrite_is_caught(monkeypatch, golden, what, module, name, old, new, catchers):
+    _rewrite(monkeypatch, module, name, old, new)
+    assert _caught(_pin_checks(catchers, golden)), what
+
+
+@pytest.mark.parametrize("what,module,name,old,new,catchers", REWRITES,
+                         ids=[r[0] for r in REWRITES])
+def test_unchanged_rewrite_keeps_pins_green(monkeypatch, golden, what, module, name, old, new,
+                                            catchers):
+    """The rewrite machinery itself (recompiling the function from its source
+    in a copy of its module's namespace) changes nothing: with the text put
+    back unchanged, the same pins pass."""
+    _rewrite(monkeypatch, module, name, old, old)
+    for check in _pin_checks(catchers, golden):
+        check()
 
 
 @pytest.mark.parametrize("name", ["test_btree_root_and_parent_types", "test_partition_covers_message",

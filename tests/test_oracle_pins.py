@@ -263,12 +263,15 @@ def test_chain_fold_order():
 
 def test_tree_local_first_then_children_in_slot_order():
     # Reading: a rank folds its local input first, then its children's partials
-    # in down[] order.  Tree 0 of 4 nodes is 0 -> 2 -> {1, 3}.  By hand:
-    # P(2) = (x2 + x1) + x3 = (2**24 + 1 -> 2**24) + 1 -> 2**24, P(0) = 0 + P(2).
-    # Folding the children first would give (1 + 1) + 2**24 = 2**24 + 2.
-    xs = [np.array([v], np.float32) for v in (0.0, 1.0, 2.0 ** 24, 1.0)]
+    # in down[] order.  Tree 0 of 4 nodes is 0 -> 2 -> {1, 3}; x = (0, 1,
+    # 2**24 + 2, -1).  Above 2**24 fp32 steps by 2 and ties go to the even
+    # significand.  By hand, P(2) = (x2 + x1) + x3:
+    # 2**24 + 3 -> 2**24 + 4, then 2**24 + 3 -> 2**24 + 4; P(0) = 0 + P(2).
+    # Children in reverse slot order, (x2 + x3) + x1: 2**24 + 1 -> 2**24, then
+    # 2**24 + 1 -> 2**24.  Children first, (x1 + x3) + x2: 2**24 + 2.
+    xs = [np.array([v], np.float32) for v in (0.0, 1.0, 2.0 ** 24 + 2, -1.0)]
     out = oracle.allreduce(xs, F32, SUM, TREE, 1, 16)
-    assert [o[0] for o in out] == [2.0 ** 24] * 4
+    assert [o[0] for o in out] == [2.0 ** 24 + 4] * 4
 
 
 def test_ring_fold_starts_at_block_owner():
@@ -423,6 +426,29 @@ def test_within_fp64_bounds(dtype, algo):
         a = sum(np.abs(numerics.to_f32(x, dtype).astype(np.float64)) for x in raws)
         for o in out:
             check_against_fp64(numerics.to_f32(o, dtype), s, a, R, dtype)
+
+
+def test_fp64_sum_exact_where_fp64_is():
+    # By hand: 2**24 + 1 - 2**24 is 1 (fp32 partials would round it to 0).
+    xs = [np.array([v], np.float32) for v in (2.0 ** 24, 1.0, -2.0 ** 24)]
+    assert oracle.fp64_sum(xs, F32).tolist() == [1.0]
+    # fp32 values with exponents in [-10, 10]: the grid is 2**-33 and up to 64
+    # of them sum below 2**17, so every partial fits in 53 bits and the fp64
+    # sum in any order is the exact sum, which math.fsum returns.
+    import math
+    rng = np.random.default_rng(12)
+    for R in (2, 7, 64):
+        m = rng.uniform(1, 2, (R, 40)) * np.exp2(rng.integers(-10, 11, (R, 40)))
+        f = (m * rng.choice([-1.0, 1.0], (R, 40))).astype(np.float32)
+        got = oracle.fp64_sum([f[r] for r in range(R)], F32)
+        want = [math.fsum(float(v) for v in f[:, e]) for e in range(40)]
+        assert got.tolist() == want
+    # widened 16-bit inputs: Max is the plain maximum of the decoded values
+    for dtype in (F16, BF16):
+        raws = [numerics.from_f32(rng.standard_normal(40).astype(np.float32), dtype)
+                for _ in range(5)]
+        dec = [numerics.to_f32(x, dtype).astype(np.float64) for x in raws]
+        assert oracle.fp64_max(raws, dtype).tolist() == [max(v[e] for v in dec) for e in range(40)]
 
 
 @pytest.mark.parametrize("algo", [RING, TREE])
