@@ -180,6 +180,30 @@ REWRITES = [
     ("parent falls back to setting the next bit only", topology, "btree",
      "up = r ^ b\n", "up = r | (b << 1)\n",
      ["test_dtree4_figure", "test_hand_derived_trees_r8_r7", "test_tree_invariants"]),
+    ("odd double tree shifted the other way", topology, "dtree",
+     "btree(n, (r - 1 + n) % n)", "btree(n, (r + 1) % n)",
+     ["test_probe_table", "test_odd_overlap_at_node0", "test_tree_invariants"]),
+    ("parent head hangs under the other child head", topology, "build_dtree",
+     "(ttc0 if ptype == 0 else ttc1)[u]", "(ttc1 if ptype == 0 else ttc0)[u]",
+     ["test_split_tree_two_by_two_by_hand", "test_balanced_tree_four_by_two_by_hand"]),
+    ("second child node attached to the child0 head", topology, "build_dtree",
+     "_set_down(per_rank[ttc1[k]], ttp[d1])", "_set_down(per_rank[ttc0[k]], ttp[d1])",
+     ["test_balanced_tree_four_by_two_by_hand"]),
+    ("intra order ignored", topology, "build_dtree",
+     "k * L + order[i]", "k * L + i",
+     ["test_active_trees_table"]),
+    ("SPLIT_TREE with the BALANCED_TREE heads", topology, "head_indices",
+     "return 0, 1, 1", "return 0, 1, 0",
+     ["test_split_tree_two_by_two_by_hand"]),
+    ("BALANCED_TREE with its child heads swapped", topology, "head_indices",
+     "return 0, 1, 0", "return 0, 0, 1",
+     ["test_balanced_tree_four_by_two_by_hand"]),
+    ("per-hop rounding left out", api, "allreduce",
+     "hop = lambda x: numerics.to_f32(numerics.from_f32(x, dtype), dtype)", "hop = lambda x: x",
+     ["test_hop_rounding_bf16_by_hand"]),
+    ("bf16 widened with a 15-bit shift", numerics, "bf16_bits_to_f32",
+     "<< np.uint32(16)", "<< np.uint32(15)",
+     ["test_bf16_rne_matches_torch"]),
     ("ring loop of one chunk instead of R", partition, "ring_blocks",
      "step = R * chunk_elems", "step = chunk_elems",
      ["test_partition_small_ring_case"]),
