@@ -361,20 +361,29 @@ def test_hier_16mib_fp16_tree_full_size(hier, op):
                               oracle.fp64_max(raws, F16))
 
 
-def test_hier_16mib_fp16_ring_full_size(hier):
+@pytest.mark.parametrize("op", [SUM, MAX])
+def test_hier_16mib_fp16_ring_full_size(hier, op, path):
     w = hier
     R, count, nch, cb = w["R"], w["count"], w["n_channels"], w["chunk_bytes"]
     src = [t.cuda() for t in w["inputs"]]
     dst = [torch.empty_like(s) for s in src]
-    vr.vr_allreduce(src, dst, R, count, F16, SUM, RING, nch, cb, None)
+    vr.vr_allreduce(src, dst, R, count, F16, op, RING, nch, cb, None)
     assert_status_ok()
     for d in dst[1:]:
         assert torch.equal(d.view(torch.int16), dst[0].view(torch.int16))
     raws = [workloads.raw_numpy(t) for t in w["inputs"]]
     xs = [numerics.to_f32(x, F16) for x in raws]
     got = bits(dst[0])
-    cs, cn, want = _channel_slice_sim(xs, count, 2, R, nch, cb // 2, 3, SUM)
-    assert np.array_equal(got[cs:cs + cn], numerics.from_f32(want, F16))
+    if op == MAX:                             # no rounding: every element exact
+        assert np.array_equal(numerics.to_f32(got, F16).astype(np.float64),
+                              oracle.fp64_max(raws, F16))
+        return
+    for k in (0, 3, nch - 1):                 # whole channels, first and last
+        cs, cn, want = _channel_slice_sim(xs, count, 2, R, nch, cb // 2, k, SUM)
+        assert np.array_equal(got[cs:cs + cn], numerics.from_f32(want, F16)), k
+    s64 = oracle.fp64_sum(raws, F16)
+    a = sum(np.abs(x.astype(np.float64)) for x in xs)
+    check_against_fp64(numerics.to_f32(got, F16), s64, a, R, F16)
 
 
 def test_hier_16mib_reduce_scatter_and_allgather(hier):
@@ -608,7 +617,7 @@ def test_more_than_2_pow_32_elements_per_rank(algo, path):
 
 # ------------------------------------------- the sweep configuration, sampled
 @pytest.mark.parametrize("algo", [RING, TREE])
-@pytest.mark.parametrize("size", [8, 4096, 1 << 20, 64 << 20, 256 << 20])
+@pytest.mark.parametrize("size", [8 << k for k in range(26)])
 def test_sweep_configuration(size, algo):
     """R=4 fp32, 12 channels, 512 KiB chunks, uniform [-1, 1) drawn on the
     device as the sweep does: bit-exact to the oracle (every element up to
