@@ -485,6 +485,7 @@ PROFILE_CASES = {
     "tree_r64_fp16_hier": ("ar", 64, 8, 1, 0, 1),
     "tree_r64_fp16_hier_max": ("ar", 64, 8, 1, 1, 1),
     "ring_r64_fp16": ("ar", 64, 1, 1, 0, 0),
+    "ring_r64_fp16_max": ("ar", 64, 1, 1, 1, 0),
     "rs_r64_fp16": ("rs", 64, 1, 1, 0, 0),
     "rs_r8_fp32": ("rs", 8, 1, 0, 0, 0),
     "ag_r64_fp16": ("ag", 64, 1, 1, 0, 0),

@@ -164,13 +164,23 @@ __device__ __forceinline__ unsigned key32(unsigned b) {
 __device__ __forceinline__ unsigned unkey32(unsigned k) {
   return k ^ (~(unsigned)((int)k >> 31) | 0x80000000u);
 }
+// 0xFFFF in every 16-bit lane whose top bit is set, else 0: a byte permute
+// that replicates the sign of bytes 1 and 3 (selector nibbles 8 | byte).
+__device__ __forceinline__ unsigned lane_signs16x2(unsigned w) {
+  unsigned m;
+  asm("prmt.b32 %0, %1, %2, 0xBB99;" : "=r"(m) : "r"(w), "r"(0u));
+  return m;
+}
 __device__ __forceinline__ unsigned key16x2(unsigned w) {
-  const unsigned neg = ((w >> 15) & 0x00010001u) * 0xFFFFu;  // 0xFFFF in negative lanes
-  return w ^ (neg | 0x80008000u);
+  return w ^ (lane_signs16x2(w) | 0x80008000u);  // negative lanes: all bits flipped
 }
 __device__ __forceinline__ unsigned unkey16x2(unsigned k) {
-  const unsigned pos = ((k >> 15) & 0x00010001u) * 0xFFFFu;  // 0xFFFF in lanes >= +0
-  return k ^ (~pos | 0x80008000u);
+  return k ^ (~lane_signs16x2(k) | 0x80008000u);  // lanes >= +0 have the top bit set
+}
+__device__ __forceinline__ unsigned max_u16x2(unsigned a, unsigned b) {
+  unsigned d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 // The fold's working lanes for one unit: fp32 values for Sum, integer keys
@@ -212,7 +222,7 @@ template <typename T, int NV> struct Lanes<T, VR_MAX, NV, false> {
   }
   static __device__ __forceinline__ L op(L a, L b) {
     if constexpr (kWide) return max(a, b);
-    else return __vmaxu2(a, b);
+    else return max_u16x2(a, b);
   }
 };
 

@@ -6,6 +6,7 @@ output buffer is surrounded by canary bytes that must survive the call.
 Inputs come from workloads.py only; no expected value comes from the GPU.
 """
 
+import itertools
 import os
 
 import numpy as np
@@ -200,6 +201,38 @@ def test_max_signed_zero_total_order(path):
         for g, w in zip(got, want):
             assert g.view(np.uint32).tolist() == w.view(np.uint32).tolist()
         assert np.signbit(got[0]).tolist() == [False, False, True, True, False]
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+def test_max_every_16bit_value(dtype, path):
+    """Max on 16-bit keys, exhaustively: every non-NaN bit pattern of the type
+    meets others in both halves of a 32-bit word, and every ordered triple of
+    +-0, +-smallest subnormal, +-largest finite and +-inf meets in both
+    halves too.  Three ranks; bit-exact to the oracle, and equal to the plain
+    maximum of the decoded values."""
+    allbits = np.arange(65536, dtype=np.uint16)
+    keep = allbits[~np.isnan(numerics.to_f32(allbits, dtype))]
+    rng = np.random.default_rng(21)
+    one = numerics.from_f32(np.array([1.0], np.float32), dtype)[0]
+    sub = np.uint16(1)                                   # smallest subnormal
+    big = np.uint16(0x7BFF if dtype == F16 else 0x7F7F)  # largest finite
+    inf = np.uint16(0x7C00 if dtype == F16 else 0x7F80)
+    special = np.array([0, 0x8000, sub, sub | 0x8000, big, big | 0x8000, inf, inf | 0x8000],
+                       np.uint16)
+    trip = np.array(list(itertools.product(special, repeat=3)), np.uint16).T   # 3 x 512
+    cols = []
+    for r in range(3):
+        a = np.concatenate([keep, rng.permutation(keep), np.roll(keep, r + 1)])
+        cols.append(np.concatenate([a, trip[r], [one], trip[r]]))    # triples in both lanes
+    inp = [torch.from_numpy(c.view(np.int16).copy()).view(TDT[dtype]) for c in cols]
+    assert inp[0].numel() > 65536                        # the ring's vector kernels
+    for algo in (RING, TREE):
+        raws, want = expect_allreduce(inp, dtype, MAX, algo, 12, 4096)
+        got = run_allreduce(inp, dtype, MAX, algo, 12, 4096)
+        assert_bits_equal(got, want, "algo %d" % algo)
+        dec = np.maximum.reduce([numerics.to_f32(x, dtype) for x in raws])
+        zero = dec == 0
+        assert np.array_equal(numerics.to_f32(got[0], dtype)[~zero], dec[~zero])
 
 
 @pytest.mark.parametrize("algo", [RING, TREE])
