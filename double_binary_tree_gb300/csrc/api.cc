@@ -47,7 +47,7 @@ unsigned long long wait_timeout_ns() {
   return ns;
 }
 
-// Temporary comparison switch (read on every call): VR_KERNEL_PATH=register
+// Test and tuning override (read on every call): VR_KERNEL_PATH=register
 // or =staged forces aligned AllReduce / ReduceScatter onto one kernel family.
 int forced_path() {
   const char* v = std::getenv("VR_KERNEL_PATH");
