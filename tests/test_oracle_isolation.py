@@ -1,15 +1,19 @@
-"""The oracle is test infrastructure: the product path never reaches it.
+"""The oracle is test infrastructure: the product path never reaches it,
+and it has no fallback of any kind.
 
 Static and import-time checks, no GPU: the package's sources never name the
 oracle, importing the package loads no oracle module, and the only places
 outside tests/ that import it are the bench's CPU baseline and reference
-arm and the smoke check.
+arm and the smoke check.  Without an up-to-date libvr.so every entry point
+raises.
 """
 
 import ast
 import os
 import subprocess
 import sys
+
+import pytest
 
 from tests.conftest import ROOT
 
@@ -76,3 +80,24 @@ def test_oracle_imported_only_where_allowed():
             assert fn in allowed, "%s:%d imports the oracle in %s" % (name, line, fn)
     with open(os.path.join(ROOT, "workloads.py"), encoding="utf-8") as fh:
         assert not _oracle_imports(ast.parse(fh.read()))
+
+
+# ------------------------------------------------------------ no fallback
+def test_missing_library_raises(monkeypatch):
+    """Without libvr.so every entry point raises: there is no other path."""
+    import double_binary_tree_gb300 as vr
+    monkeypatch.setattr(vr, "_lib", None)
+    monkeypatch.setattr(vr, "LIB", os.path.join(ROOT, "no_such_dir", "libvr.so"))
+    with pytest.raises(ImportError, match="not built"):
+        vr.vr_build_ring(4, 2)
+    with pytest.raises(ImportError, match="not built"):
+        vr.vr_get_error_string(0)
+
+
+def test_stale_library_raises(monkeypatch):
+    """A library older than its sources (or built elsewhere) is not loaded."""
+    import double_binary_tree_gb300 as vr
+    monkeypatch.setattr(vr, "_lib", None)
+    monkeypatch.setattr(vr, "is_fresh", lambda: False)
+    with pytest.raises(ImportError, match="older than its sources"):
+        vr.vr_build_ring(4, 2)
