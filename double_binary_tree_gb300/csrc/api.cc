@@ -407,6 +407,38 @@ void fill_partition(KArgs& a, size_t count, size_t E, int nCh, size_t chunkBytes
   a.mC = recip(a.chunk);
 }
 
+// A register-path call is a few rounds per thread, each R loads of one unit
+// waited for together (a DRAM round trip), over a persistent grid of every
+// resident thread.  While a tree call takes at most three rounds it is
+// bound by those round trips, and when the specialised kernel compiled for
+// four CTAs per SM (at most 64 registers) takes a whole round off every
+// thread, that kernel is used.  Measured on GB300 (R = 4, 7, 8; fp32 and
+// bf16): 9-17% faster at 2 MiB per rank, 2-8% at 4 MiB; 2-5% slower from
+// 6 MiB (four rounds or more), and 4-21% slower for every ring, which keep
+// their kernels.  VR_JIT_OCC=0 never switches, =4 always does (rings too).
+const void* more_resident(const void* special, long long units, int dtype, int op, int mode,
+                          int stack, const KArgs& a) {
+  const unsigned occ = env_uint("VR_JIT_OCC", 1);
+  if (occ == 0 || (occ != 4 && mode != kTreeAllReduce)) return special;
+  DeviceInfo di;
+  int device = 0;
+  if (device_info(&di, &device) != VR_SUCCESS) return special;
+  const int now = blocks_per_sm(special, device);
+  if (now >= 4) return special;
+  const long long perBlock = (long long)kBlockThreads * di.sms;
+  const long long roundsNow = (units + perBlock * now - 1) / (perBlock * now);
+  const long long roundsFour = (units + perBlock * 4 - 1) / (perBlock * 4);
+  if (occ != 4 && (roundsNow > 3 || roundsFour >= roundsNow)) return special;
+  const bool small = use_small(dtype, mode, true, stack, a.R);
+  const void* four = nullptr;
+  const vr_result_t e =
+      mode == kTreeAllReduce
+          ? jit_tree_kernel(dtype, op, stack, small, false, a.prog, a.nProgs, &four, 4)
+          : jit_ring_kernel(dtype, op, a.R, small, false, &four, 4);
+  if (e != VR_SUCCESS || blocks_per_sm(four, device) < 4) return special;
+  return four;
+}
+
 // The AllReduce kernel over the elements [lo, hi) of the message `a`
 // describes (lo at a 16-byte boundary): the staged kernel, or the register
 // kernel (16-byte units when `vec`, else elements).  Every element's fold
@@ -443,8 +475,10 @@ vr_result_t launch_allreduce_range(KArgs& a, int dtype, int mode, int op, int st
                          stream);
   }
   const long long NV = vec ? kGrainBytes / E : 1;
-  return launch(special ? special : pick_kernel(dtype, mode, op, vec, stack, a.R), a,
-                (hi + NV - 1) / NV - lo / NV, stream);
+  const long long units = (hi + NV - 1) / NV - lo / NV;
+  if (special) special = more_resident(special, units, dtype, op, mode, stack, a);
+  return launch(special ? special : pick_kernel(dtype, mode, op, vec, stack, a.R), a, units,
+                stream);
 }
 
 // Per device: the two copy streams and three events of vr_allreduce_host,

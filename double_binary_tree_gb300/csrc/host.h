@@ -19,12 +19,15 @@ vr_result_t dtree_programs(int nNodes, int L, FoldProg out[2]);
 
 // Tree kernel specialised at run time for a call's fold programs (jit.cc):
 // the shared-memory-staged one when `staged`, else the register-path one
-// (16-byte units; the few-rank variant when `small`).
+// (16-byte units; the few-rank variant when `small`; compiled for at least
+// `minBlocks` resident CTAs per SM when it is above 0).
 bool jit_enabled();
 vr_result_t jit_tree_kernel(int dtype, int op, int stack, bool small, bool staged,
-                            const FoldProg* progs, int nProgs, const void** out);
+                            const FoldProg* progs, int nProgs, const void** out,
+                            int minBlocks = 0);
 // The ring AllReduce kernel specialised for R ranks (the same variants).
-vr_result_t jit_ring_kernel(int dtype, int op, int R, bool small, bool staged, const void** out);
+vr_result_t jit_ring_kernel(int dtype, int op, int R, bool small, bool staged, const void** out,
+                            int minBlocks = 0);
 void jit_counts(long long* compiled, long long* failed);
 vr_result_t jit_compile_dtree(int nNodes, int L, int dtype, int op, int arch,
                               size_t* cubinBytes, char* log, size_t logBytes);

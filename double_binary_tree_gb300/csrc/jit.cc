@@ -248,8 +248,8 @@ std::string cache_key(int arch, int dtype, int op, int stack, bool small, const 
 // into a CUBIN.  Returns the lowered names in `names`.
 // mode: kTreeAllReduce (progs, nProgs, stack) or kRingAllReduce (R).
 bool compile(int arch, int dtype, int op, int mode, int stack, bool small, int kind,
-             const FoldProg* progs, int nProgs, int R, std::string* cubin, std::string* name,
-             std::string* log) {
+             const FoldProg* progs, int nProgs, int R, int minBlocks, std::string* cubin,
+             std::string* name, std::string* log) {
   const Nvrtc& n = nvrtc();
   const std::string dir = source_dir();
   const char* T = type_name(dtype);
@@ -257,6 +257,7 @@ bool compile(int arch, int dtype, int op, int mode, int stack, bool small, int k
   std::string src;
   if (mode == kTreeAllReduce ? !generate(progs, nProgs, &src) : !generate_ring(R, &src))
     return false;
+  if (minBlocks > 0) src = "#define VR_JIT_MIN_BLOCKS " + std::to_string(minBlocks) + "\n" + src;
   const int S = stack <= 4 ? 4 : 8;
   const std::string M = std::to_string(mode);
   const std::string expr =
@@ -308,14 +309,14 @@ namespace {
 // The compiled kernel for `key`, compiling and loading it on first use.
 vr_result_t cached_kernel(const std::string& key, int dtype, int op, int mode, int stack,
                           bool small, bool staged, const FoldProg* progs, int nProgs, int R,
-                          int arch, const void** out) {
+                          int minBlocks, int arch, const void** out) {
   std::lock_guard<std::mutex> g(g_jitMu);
   auto it = g_cache.find(key);
   if (it == g_cache.end()) {
     Entry e;
     std::string cubin, name;
-    if (compile(arch, dtype, op, mode, stack, small, staged ? 1 : 0, progs, nProgs, R, &cubin,
-                &name, nullptr) &&
+    if (compile(arch, dtype, op, mode, stack, small, staged ? 1 : 0, progs, nProgs, R, minBlocks,
+                &cubin, &name, nullptr) &&
         cudaLibraryLoadData(&e.lib, cubin.data(), nullptr, nullptr, 0, nullptr, nullptr, 0) ==
             cudaSuccess)
       e.ok = cudaLibraryGetKernel(&e.kernel, e.lib, name.c_str()) == cudaSuccess;
@@ -341,28 +342,30 @@ vr_result_t device_arch(int* arch) {
 }  // namespace
 
 vr_result_t jit_tree_kernel(int dtype, int op, int stack, bool small, bool staged,
-                            const FoldProg* progs, int nProgs, const void** out) {
+                            const FoldProg* progs, int nProgs, const void** out, int minBlocks) {
   int arch = 0;
   const vr_result_t e = device_arch(&arch);
   if (e != VR_SUCCESS) return e;
   small = small && !staged;
-  const std::string key = std::string(staged ? "t1/" : "t0/") +
+  if (staged) minBlocks = 0;
+  const std::string key = std::string(staged ? "t1/" : "t0/") + std::to_string(minBlocks) + "/" +
                           cache_key(arch, dtype, op, stack, small, progs, nProgs);
   return cached_kernel(key, dtype, op, kTreeAllReduce, stack, small, staged, progs, nProgs, 0,
-                       arch, out);
+                       minBlocks, arch, out);
 }
 
 vr_result_t jit_ring_kernel(int dtype, int op, int R, bool small, bool staged,
-                            const void** out) {
+                            const void** out, int minBlocks) {
   int arch = 0;
   const vr_result_t e = device_arch(&arch);
   if (e != VR_SUCCESS) return e;
   small = small && !staged;
-  const std::string key = std::string(staged ? "r1/" : "r0/") + std::to_string(arch) + "/" +
-                          std::to_string(dtype) + "/" + std::to_string(op) + "/" +
-                          std::to_string(R) + (small ? "/s" : "/g");
-  return cached_kernel(key, dtype, op, kRingAllReduce, 0, small, staged, nullptr, 0, R, arch,
-                       out);
+  if (staged) minBlocks = 0;
+  const std::string key = std::string(staged ? "r1/" : "r0/") + std::to_string(minBlocks) + "/" +
+                          std::to_string(arch) + "/" + std::to_string(dtype) + "/" +
+                          std::to_string(op) + "/" + std::to_string(R) + (small ? "/s" : "/g");
+  return cached_kernel(key, dtype, op, kRingAllReduce, 0, small, staged, nullptr, 0, R,
+                       minBlocks, arch, out);
 }
 
 void jit_counts(long long* compiled, long long* failed) {
@@ -381,7 +384,7 @@ vr_result_t jit_compile_dtree(int nNodes, int L, int dtype, int op, int arch,
   const int stack = p[0].depth > p[1].depth ? p[0].depth : p[1].depth;
   if (!nvrtc().ok || source_dir().empty()) return VR_ERR_UNSUPPORTED;
   std::string cubin, name, text;
-  const bool ok = compile(arch, dtype, op, kTreeAllReduce, stack, false, 0, p, 2, 0, &cubin,
+  const bool ok = compile(arch, dtype, op, kTreeAllReduce, stack, false, 0, p, 2, 0, 0, &cubin,
                           &name, &text);
   if (log && logBytes) {
     std::strncpy(log, text.c_str(), logBytes - 1);
@@ -401,7 +404,7 @@ vr_result_t jit_compile_ring(int R, int dtype, int op, int arch, size_t* cubinBy
   *cubinBytes = 0;
   for (int kind = 0; kind < 2; ++kind) {
     std::string cubin, name;
-    if (!compile(arch, dtype, op, kRingAllReduce, 0, false, kind, nullptr, 0, R, &cubin, &name,
+    if (!compile(arch, dtype, op, kRingAllReduce, 0, false, kind, nullptr, 0, R, 0, &cubin, &name,
                  &text)) {
       if (log && logBytes) {
         std::strncpy(log, text.c_str(), logBytes - 1);

@@ -29,6 +29,12 @@ constexpr int kBlock = 256;  // threads per CTA of the register-path kernels
 constexpr int kMinBlocksTree = 2;
 constexpr int kMinBlocksRing = VR_MIN_BLOCKS_RING;
 constexpr int kMinBlocksSmall = 3;
+// Kernels compiled at run time may ask for more resident CTAs (jit.cc).
+#ifdef VR_JIT_MIN_BLOCKS
+constexpr int kMinBlocksJit = VR_JIT_MIN_BLOCKS;
+#else
+constexpr int kMinBlocksJit = 0;
+#endif
 
 // Rank pointers (and tree programs) copied to shared memory: they are indexed
 // by a runtime rank.
@@ -58,9 +64,10 @@ __device__ __forceinline__ void stage_args(const KArgs& a, const char** s_src, c
 // the kernel fits 3 CTAs per SM (85 registers) -- with few ranks a thread
 // has few loads in flight, and only more resident threads make up for it.
 template <typename T, int OP, int MODE, bool VEC, int S, bool SMALL>
-__global__ void __launch_bounds__(kBlock, SMALL ? kMinBlocksSmall
-                                               : (MODE == kTreeAllReduce ? kMinBlocksTree
-                                                                         : kMinBlocksRing))
+__global__ void __launch_bounds__(kBlock, kMinBlocksJit ? kMinBlocksJit
+                                          : SMALL ? kMinBlocksSmall
+                                          : (MODE == kTreeAllReduce ? kMinBlocksTree
+                                                                    : kMinBlocksRing))
     allreduce_kernel(const __grid_constant__ KArgs a) {
   constexpr int U = Ty<T>::U;
   constexpr int NV = VEC ? U : 1;

@@ -50,6 +50,11 @@
  *   VR_SMALL_RANKS=0                no few-rank register-path variant
  *   VR_SPREAD=0                     256-thread CTAs even when a small call
  *                                   would leave SMs idle
+ *   VR_JIT_OCC=0|4                  specialised register-path kernels at
+ *                                   four CTAs per SM: never / always (by
+ *                                   default a tree of at most three rounds
+ *                                   per thread takes them when they save
+ *                                   one)
  *   VR_PDL=0                        launch without programmatic stream
  *                                   serialisation (by default a kernel may
  *                                   start while the previous one on the

@@ -19,7 +19,9 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU runs deselect these
 
 import double_binary_tree_gb300 as vr  # noqa: E402
 
-TREE = vr.VR_ALGO_TREE
+TREE, RING = vr.VR_ALGO_TREE, vr.VR_ALGO_RING
+F32, F16, BF16 = vr.VR_FLOAT32, vr.VR_FLOAT16, vr.VR_BFLOAT16
+SUM = vr.VR_SUM
 
 
 def _run(inp, dtype, op, nch, cb, L, jit, path):
@@ -107,3 +109,23 @@ def test_specialised_ring_equals_oracle(R, dtype, op, count, nch, cb, path):
     assert vr.vr_jit_status()[2] == 0
     for r in range(R):
         assert np.array_equal(got[r], want[r]), "rank %d" % r
+
+
+@pytest.mark.parametrize("occ", ["0", "4"])
+def test_four_ctas_per_sm_same_bits(occ, monkeypatch):
+    """The specialised register-path kernels compiled for four CTAs per SM
+    (VR_JIT_OCC=4, rings included) give the oracle's bits, like those at
+    their natural occupancy (VR_JIT_OCC=0)."""
+    monkeypatch.setenv("VR_JIT_OCC", occ)
+    for R, dtype, algo, count in [(8, BF16, TREE, 300001), (7, BF16, TREE, 300001),
+                                  (4, F32, TREE, 200003), (5, F16, RING, 300001),
+                                  (8, F32, RING, 200003)]:
+        inp = workloads.generate(R, count, dtype, "normal", 900 + R)
+        raws = [workloads.raw_numpy(t) for t in inp]
+        want = oracle.allreduce(raws, dtype, SUM, algo, 12, 4096)
+        src = [t.cuda() for t in inp]
+        dst = [torch.empty_like(t) for t in src]
+        vr.vr_allreduce(src, dst, R, count, dtype, SUM, algo, 12, 4096, torch.cuda.current_stream())
+        assert vr.vr_stream_status(torch.cuda.current_stream()) == 0
+        for d, w in zip(dst, want):
+            assert np.array_equal(workloads.raw_numpy(d), w), (R, dtype, algo)
