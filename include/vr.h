@@ -52,8 +52,9 @@
  *                                   would leave SMs idle
  *   VR_JIT_OCC=0|4                  specialised register-path kernels at
  *                                   four CTAs per SM: never / always (by
- *                                   default a tree of at most three rounds
- *                                   per thread takes them when they save
+ *                                   default a tree call takes them when
+ *                                   each thread folds at most three units
+ *                                   and the larger grid saves every thread
  *                                   one)
  *   VR_PDL=0                        launch without programmatic stream
  *                                   serialisation (by default a kernel may
