@@ -234,6 +234,13 @@ REWRITES = [
     ("crossover of the wrong sign", costmodel, "crossover",
      "m = num / den", "m = -num / den",
      ["test_cost_model_crossover_matches_search"]),
+    ("least-squares columns transposed", costmodel, "fit",
+     "np.asarray(stages, float), np.asarray(traffic, float)",
+     "np.asarray(traffic, float), np.asarray(stages, float)",
+     ["test_cost_model_fit_recovers_parameters"]),
+    ("selection picks the slower algorithm", costmodel, "select",
+     "t_ring(N, M, *ring) <= t_tree(D, M, *tree)", "t_ring(N, M, *ring) > t_tree(D, M, *tree)",
+     ["test_cost_model_selects_lower_prediction_by_hand"]),
     ("tree cost model counts one pass of the tree", costmodel, "tree_terms",
      "return 2 * D, 2.0 * M", "return D, 2.0 * M",
      ["test_cost_model_step_counts_and_traffic"]),

@@ -632,6 +632,19 @@ def test_cost_model_crossover_matches_search():
             assert cm.select(N, D, m * 0.5, ring, tree) != cm.select(N, D, m * 2, ring, tree)
 
 
+def test_cost_model_selects_lower_prediction_by_hand():
+    # N = 4 ranks, tree depth D = 2: ring 6 alpha + 1.5 M beta, tree 4 alpha
+    # + 2 M beta.  Ring (alpha 1, beta 1e-3), tree (alpha 0.5, beta 1e-3):
+    # at M = 0 ring 6 vs tree 2 -> tree; at M = 1e6 ring 1506 vs tree 2002 ->
+    # ring; they cross at 4 / 0.5e-3 = 8000 bytes.
+    from oracle import costmodel as cm
+    ring, tree = (1.0, 1e-3), (0.5, 1e-3)
+    assert cm.t_ring(4, 0, *ring) == 6.0 and cm.t_tree(2, 0, *tree) == 2.0
+    assert cm.select(4, 2, 0, ring, tree) == "tree"
+    assert cm.select(4, 2, 1e6, ring, tree) == "ring"
+    assert abs(cm.crossover(4, 2, ring, tree) - 8000.0) < 1e-6
+
+
 def test_cost_model_fit_recovers_parameters():
     from oracle import costmodel as cm
     stages = [6] * 10 + [14] * 10
