@@ -204,6 +204,27 @@ REWRITES = [
     ("bf16 widened with a 15-bit shift", numerics, "bf16_bits_to_f32",
      "<< np.uint32(16)", "<< np.uint32(15)",
      ["test_bf16_rne_matches_torch"]),
+    ("tree depth counted in nodes, not edges", topology, "exact_depth",
+     "worst = max(worst, d)", "worst = max(worst, d + 1)",
+     ["test_probe_table"]),
+    ("internal nodes leave out the root", topology, "internal_nodes",
+     "if any(c != -1 for c in t.down)", "if t.up != -1 and any(c != -1 for c in t.down)",
+     ["test_probe_table", "test_odd_overlap_at_node0"]),
+    ("ring prev points forward", topology, "build_ring",
+     "(r - 1 + R) % R", "(r + 1) % R",
+     ["test_ring_topology"]),
+    ("ring all-gather sends not counted", schedules, "ring_allreduce_loop",
+     "held[(r + 1) % R][j] = msg\n            if counters is not None:\n"
+     "                counters.sent[r] += msg.size",
+     "held[(r + 1) % R][j] = msg\n            if counters is not None:\n"
+     "                counters.sent[r] += 0",
+     ["test_ring_traffic_closed_form", "test_ring_four_ranks_sends_one_and_a_half_S"]),
+    ("tree broadcast sends not counted", schedules, "tree_allreduce_chunk",
+     "nxt.append(c)\n                    if counters is not None:\n"
+     "                        counters.sent[v] += length",
+     "nxt.append(c)\n                    if counters is not None:\n"
+     "                        counters.sent[v] += 0",
+     ["test_tree_sends_at_most_2S_per_rank_even_mirror"]),
     ("ring loop of one chunk instead of R", partition, "ring_blocks",
      "step = R * chunk_elems", "step = chunk_elems",
      ["test_partition_small_ring_case"]),
