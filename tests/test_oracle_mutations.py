@@ -225,6 +225,21 @@ REWRITES = [
      "nxt.append(c)\n                    if counters is not None:\n"
      "                        counters.sent[v] += 0",
      ["test_tree_sends_at_most_2S_per_rank_even_mirror"]),
+    ("log2 rounded up", topology, "log2i",
+     "n >>= 1", "n = (n + 1) >> 1",
+     ["test_log2i_is_floor"]),
+    ("tree log line with up and rank swapped", topology, "format_tree_log",
+     "(channel, t.up, r, kids)", "(channel, r, t.up, kids)",
+     ["test_active_chains_and_log_line"]),
+    ("prediction divides by the inverse bandwidth", costmodel, "predict",
+     "traffic * inv_bw", "traffic / inv_bw",
+     ["test_cost_model_selects_lower_prediction_by_hand", "test_cost_model_fit_recovers_parameters"]),
+    ("narrowing uses the other 16-bit format", numerics, "from_f32",
+     "return f32_to_f16_bits(x)", "return f32_to_bf16_bits(x)",
+     ["test_within_fp64_bounds"]),
+    ("ReduceScatter sampler starts at the owner", sample, "reduce_scatter_element",
+     "(block + 1 + k) % R", "(block + k) % R",
+     ["test_reduce_scatter_sampler_matches_literal"]),
     ("ring loop of one chunk instead of R", partition, "ring_blocks",
      "step = R * chunk_elems", "step = chunk_elems",
      ["test_partition_small_ring_case"]),

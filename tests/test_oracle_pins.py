@@ -210,6 +210,16 @@ def test_tree_invariants(L):
             assert not (node_int[0] & node_int[1])
 
 
+def test_log2i_is_floor():
+    # the depth field's floor(log2 nNodes): hand values, and the bit length
+    # of n minus one for every n up to 4096
+    assert [topology.log2i(n) for n in (1, 2, 3, 4, 5, 7, 8, 9, 1023, 1024, 1025)] == \
+        [0, 1, 1, 2, 2, 2, 3, 3, 9, 10, 10]
+    assert all(topology.log2i(n) == n.bit_length() - 1 for n in range(1, 4097))
+    # R = 6 as 3 nodes x 2 ranks: depth 2 - 1 + floor(log2 3) = 2
+    assert {t.depth for t in topology.build_dtree(3, 2, 1)[0]} == {2}
+
+
 def test_channel_to_tree_split():
     for nch in range(1, 25):
         idx = [topology.channel_tree_index(c, nch) for c in range(nch)]
