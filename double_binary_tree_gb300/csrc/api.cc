@@ -425,9 +425,9 @@ const void* more_resident(const void* special, long long units, int dtype, int o
   if (device_info(&di, &device) != VR_SUCCESS) return special;
   const int now = blocks_per_sm(special, device);
   if (now >= 4) return special;
-  const long long perBlock = (long long)kBlockThreads * di.sms;
-  const long long roundsNow = (units + perBlock * now - 1) / (perBlock * now);
-  const long long roundsFour = (units + perBlock * 4 - 1) / (perBlock * 4);
+  const long long oneCtaPerSm = (long long)kBlockThreads * di.sms;  // threads
+  const long long roundsNow = (units + oneCtaPerSm * now - 1) / (oneCtaPerSm * now);
+  const long long roundsFour = (units + oneCtaPerSm * 4 - 1) / (oneCtaPerSm * 4);
   if (occ != 4 && (roundsNow > 3 || roundsFour >= roundsNow)) return special;
   const bool small = use_small(dtype, mode, true, stack, a.R);
   const void* four = nullptr;
