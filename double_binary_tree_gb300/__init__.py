@@ -73,6 +73,8 @@ _SIGNATURES = {
     "vr_stream_status": (I, [VP]),
     "vr_launch_count": (ctypes.c_ulonglong, []),
     "vr_debug_stall_next": (I, [ctypes.c_longlong]),
+    "vr_set_option": (I, [ctypes.c_char_p, ctypes.c_longlong]),
+    "vr_get_option": (I, [ctypes.c_char_p, P(ctypes.c_longlong)]),
     "vr_get_error_string": (ctypes.c_char_p, [I]),
     "vr_finalize": (None, []),
 }
@@ -344,6 +346,16 @@ def vr_launch_count():
 
 def vr_debug_stall_next(tile):
     _check(_L().vr_debug_stall_next(tile), "vr_debug_stall_next")
+
+
+def vr_set_option(name, value):
+    _check(_L().vr_set_option(name.encode(), int(value)), "vr_set_option")
+
+
+def vr_get_option(name):
+    v = ctypes.c_longlong()
+    _check(_L().vr_get_option(name.encode(), ctypes.byref(v)), "vr_get_option")
+    return v.value
 
 
 def vr_get_error_string(code):

@@ -32,12 +32,6 @@ std::map<std::pair<int, int>, std::array<FoldProg, 2>> g_progs;  // (nNodes, loc
 std::map<std::pair<const void*, int>, int> g_smemSet;            // (kernel, device) -> bytes
 std::atomic<long long> g_stallNext{-1};                          // test hook
 
-// Tuning overrides read from the environment (0 when unset).
-unsigned env_uint(const char* name, unsigned dflt) {
-  const char* v = std::getenv(name);
-  return v ? (unsigned)std::strtoul(v, nullptr, 10) : dflt;
-}
-
 unsigned long long wait_timeout_ns() {
   static const unsigned long long ns = [] {
     const char* v = std::getenv("VR_WAIT_TIMEOUT_NS");
@@ -47,15 +41,9 @@ unsigned long long wait_timeout_ns() {
   return ns;
 }
 
-// Test and tuning override (read on every call): VR_KERNEL_PATH=register
-// or =staged forces aligned AllReduce / ReduceScatter onto one kernel family.
-int forced_path() {
-  const char* v = std::getenv("VR_KERNEL_PATH");
-  if (!v) return 0;
-  if (std::strcmp(v, "register") == 0) return 1;
-  if (std::strcmp(v, "staged") == 0) return 2;
-  return 0;
-}
+// Test and tuning option VR_KERNEL_PATH: 1 (register) or 2 (staged) forces
+// aligned AllReduce / ReduceScatter onto one kernel family.
+int forced_path() { return (int)option(kOptKernelPath); }
 
 size_t elem_size(int dtype) {
   switch (dtype) {
@@ -214,11 +202,11 @@ const void* pick_staged(int dtype, int mode, int op, int stack = 0) {
 
 // Register-path kernel; fp32 with at most 4 ranks takes the variant compiled
 // for 3 CTAs per SM (1.2-1.5x faster from 16 MiB per rank; slower for 16-bit
-// types, which keep the general kernel).  VR_SMALL_RANKS=0, read per call,
-// turns it off for tuning.
+// types, which keep the general kernel).  The option VR_SMALL_RANKS=0 turns
+// it off for tuning.
 bool use_small(int dtype, int mode, bool vec, int stack, int R) {
   return dtype == VR_FLOAT32 && vec && R <= 4 && stack <= 4 && mode != kReduceScatter &&
-         env_uint("VR_SMALL_RANKS", 1) != 0;
+         option(kOptSmallRanks) != 0;
 }
 const void* pick_kernel(int dtype, int mode, int op, bool vec, int stack = 0, int R = 64) {
   const bool small = use_small(dtype, mode, vec, stack, R);
@@ -244,7 +232,7 @@ cudaError_t launch_kernel(const void* fn, dim3 grid, dim3 block, void** args, si
   cfg.dynamicSmemBytes = smem;
   cfg.stream = (cudaStream_t)stream;
   cudaLaunchAttribute attr[1];
-  if (pdl && env_uint("VR_PDL", 1)) {
+  if (pdl && option(kOptPdl)) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
@@ -270,7 +258,7 @@ vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream,
   // warp multiple), so that the work spreads over all SMs instead of
   // queueing on a few (each SM's load bandwidth bounds a small call).
   int block = kBlockThreads;
-  if (wanted < di.sms && env_uint("VR_SPREAD", 1)) {
+  if (wanted < di.sms && option(kOptSpread)) {
     const long long perSm = (units + di.sms - 1) / di.sms;
     block = (int)std::min<long long>(kBlockThreads, std::max<long long>(32, (perSm + 31) / 32 * 32));
   }
@@ -292,7 +280,7 @@ vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream,
 // run time (jit.cc), for the tree of 8-64 ranks (the interpreting staged tree
 // is 2-3x slower than the register path).
 bool use_staged(int mode, int R, size_t bytesPerRank) {
-  const size_t minBytes = env_uint("VR_STAGED_MIN_BYTES", 16u << 20);
+  const size_t minBytes = (size_t)option(kOptStagedMinBytes);
   if (R < 8 || bytesPerRank < minBytes) return false;
   if (mode == kRingAllReduce) return true;
   if (mode == kTreeAllReduce) return jit_enabled();
@@ -308,7 +296,7 @@ bool use_staged(int mode, int R, size_t bytesPerRank) {
 // against 101 us): both stay on the register path.
 bool use_staged_rs(int R, int dtype, size_t sendBytesPerRank) {
   return dtype == VR_FLOAT32 && R >= 2 && R <= 8 &&
-         sendBytesPerRank >= env_uint("VR_STAGED_MIN_BYTES", 16u << 20);
+         sendBytesPerRank >= (size_t)option(kOptStagedMinBytes);
 }
 
 // Per-rank tile bytes of the staged kernel (bulk copies below 2 KB lose
@@ -336,10 +324,10 @@ vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
   // Largest per-rank tile (fewer, larger bulk copies) that still leaves
   // at least kMinStages stages in the opt-in shared memory.
   const int room = di.smemOptin - kStagedHeader;
-  unsigned tb = env_uint("VR_STAGED_TILE_BYTES", 0);
+  unsigned tb = (unsigned)option(kOptStagedTileBytes);
   // Above 32 ranks two stages with larger tiles (more consumer warps) beat
   // three smaller ones: measured 2.5% (tree) to 20% (ring) faster at 64.
-  int minStages = (int)env_uint("VR_STAGED_MIN_STAGES", a.R > 32 ? 2 : 3);
+  int minStages = (int)option_or(kOptStagedMinStages, a.R > 32 ? 2 : 3);
   if (!tb) {
     tb = staged_tile_bytes(a.R, mode);
     if (a.R > 32 && mode != kReduceScatter)  // the largest 512-byte multiple that fits
@@ -354,7 +342,7 @@ vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
   a.stageBytes = ((unsigned)a.R * a.tileBytes + 127u) & ~127u;
   const int fit = room / (int)a.stageBytes;
   a.stages = std::min(kStagedMaxStages, fit);
-  const int cap = (int)env_uint("VR_STAGED_STAGES", 0);
+  const int cap = (int)option(kOptStagedStages);
   if (cap) a.stages = std::min(a.stages, cap);
   if (a.stages < 2) return VR_ERR_INTERNAL;
   a.consumers = std::max(1, std::min(kStagedMaxConsumers, a.tileUnits / 32));
@@ -418,7 +406,7 @@ void fill_partition(KArgs& a, size_t count, size_t E, int nCh, size_t chunkBytes
 // their kernels.  VR_JIT_OCC=0 never switches, =4 always does (rings too).
 const void* more_resident(const void* special, long long units, int dtype, int op, int mode,
                           int stack, const KArgs& a) {
-  const unsigned occ = env_uint("VR_JIT_OCC", 1);
+  const long long occ = option(kOptJitOcc);
   if (occ == 0 || (occ != 4 && mode != kTreeAllReduce)) return special;
   DeviceInfo di;
   int device = 0;
@@ -461,7 +449,7 @@ vr_result_t launch_allreduce_range(KArgs& a, int dtype, int mode, int op, int st
   // The ring specialised for R ranks: measured 6-12% faster on the register
   // path for 3-16 ranks, neutral on the staged one (VR_JIT_RING=1 also takes
   // it there, 0 turns it off).
-  const unsigned jr = env_uint("VR_JIT_RING", 2);
+  const long long jr = option(kOptJitRing);
   if (mode == kRingAllReduce && vec && a.R >= 3 && a.R <= 16 && jr != 0 &&
       (!staged || jr == 1) && jit_enabled() &&
       jit_ring_kernel(dtype, op, a.R, use_small(dtype, mode, vec, stack, a.R), staged,
@@ -835,9 +823,9 @@ vr_result_t vr_allgather(const void* const* sendbufs, void* const* recvbufs, int
     int device = 0;
     if ((e = device_info(&di, &device)) != VR_SUCCESS) return e;
     // geometry: tuning overrides VR_AG_TILE / VR_AG_STAGES / VR_AG_CTAS
-    const int tile = (int)env_uint("VR_AG_TILE", (unsigned)gather_tile_bytes());
-    const int stages = (int)env_uint("VR_AG_STAGES", (unsigned)gather_stages());
-    const int ctas = (int)std::max(1u, env_uint("VR_AG_CTAS", (unsigned)gather_ctas_per_sm()));
+    const int tile = (int)option_or(kOptAgTile, gather_tile_bytes());
+    const int stages = (int)option_or(kOptAgStages, gather_stages());
+    const int ctas = (int)std::max(1LL, option_or(kOptAgCtas, gather_ctas_per_sm()));
     const void* fn = kernel_ptr_allgather_tma(tile, stages);
     if (!fn) return VR_ERR_INVALID_ARGUMENT;
     const size_t smem = (size_t)tile * stages;

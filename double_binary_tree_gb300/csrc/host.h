@@ -7,6 +7,31 @@
 
 namespace vr {
 
+// Tuning and test options (options.cc): the environment's values at the
+// first use, then whatever vr_set_option stored.  -1: the call site's
+// default applies.
+enum Option : int {
+  kOptKernelPath,      // 0 auto, 1 register path, 2 staged kernel
+  kOptJit,             // 0: interpreting folds only
+  kOptJitRing,         // 0 never, 1 also staged, 2 register path only
+  kOptJitOcc,          // 0 never, 4 always, else by rounds
+  kOptSmallRanks,      // 0: no few-rank register-path variant
+  kOptPdl,             // 0: no programmatic stream serialisation
+  kOptSpread,          // 0: no CTA shrinking for small calls
+  kOptStagedMinBytes,  // staged kernel from this many bytes per rank
+  kOptStagedTileBytes, // 0: the built-in tile
+  kOptStagedMinStages, // -1: by rank count
+  kOptStagedStages,    // 0: as many as fit
+  kOptAgTile,          // -1: gather_tile_bytes()
+  kOptAgStages,        // -1: gather_stages()
+  kOptAgCtas,          // -1: gather_ctas_per_sm()
+  kOptDebug,           // bit set of kDebug* subsystems
+  kOptCount
+};
+constexpr long long kDebugGraph = 1;  // print tree, ring and partition tables
+long long option(Option o);
+long long option_or(Option o, long long dflt);
+
 void btree(int n, int r, int* up, int* d0, int* d1, int* childType);
 void dtree(int n, int r, int t[2][4]);
 int channel_tree(int c, int nCh);

@@ -299,8 +299,7 @@ bool compile(int arch, int dtype, int op, int mode, int stack, bool small, int k
 }  // namespace
 
 bool jit_enabled() {
-  const char* v = std::getenv("VR_JIT");  // read per call: 0 turns the specialisation off
-  if (v && v[0] == '0') return false;
+  if (option(kOptJit) == 0) return false;  // the option VR_JIT=0 turns the specialisation off
   return nvrtc().ok && !source_dir().empty();
 }
 

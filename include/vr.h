@@ -39,11 +39,14 @@
  *   - Results are deterministic: the same call on the same inputs gives the
  *     same bits, and every rank's output is bit-identical.
  *
- * Environment overrides, for tests and tuning (read on every call unless
- * noted; no override changes a result, only which kernel computes it):
+ * Options, for tests and tuning (no option changes a result, only which
+ * kernel computes it, or what the library prints).  Each is read from the
+ * environment once, at the first call that needs an option, and changed
+ * afterwards only through vr_set_option (same names and values):
  *   VR_KERNEL_PATH=staged|register  force the shared-memory-staged or the
  *                                   register-path AllReduce / ReduceScatter
- *                                   kernel (aligned buffers)
+ *                                   kernel (aligned buffers); vr_set_option
+ *                                   takes 2 or 1 (0: automatic)
  *   VR_JIT=0                        interpreting tree / ring folds only
  *   VR_JIT_RING=0|1                 ring folds specialised: never / also on
  *                                   the staged kernel
@@ -71,10 +74,16 @@
  *                                   and stages that are compiled: 8192/4,
  *                                   8192/8, 16384/4, 16384/6, 32768/3,
  *                                   4096/8; others are INVALID_ARGUMENT)
- *   VR_WAIT_TIMEOUT_NS=n            (read once) limit of every bounded wait
+ *   VR_DEBUG=GRAPH                  print every tree set, ring and channel
+ *                                   partition a call plans to stderr, in
+ *                                   the log formats of [Course13] "从 GRAPH
+ *                                   日志复原 active tree" (vr_set_option
+ *                                   takes 1)
+ * Read once at first use, not changeable:
+ *   VR_WAIT_TIMEOUT_NS=n            limit of every bounded wait
  *                                   (default 1 s)
- *   VR_VALIDATE_POINTERS=1          (read once) check that every buffer is
- *                                   reachable from the current device
+ *   VR_VALIDATE_POINTERS=1          check that every buffer is reachable
+ *                                   from the current device
  */
 #ifndef VR_H
 #define VR_H
@@ -480,6 +489,17 @@ unsigned long long vr_launch_count(void);
  * VR_ERR_TIMEOUT; the stream and the context stay usable.  -1 cancels a
  * pending request.  Errors: VR_ERR_INVALID_ARGUMENT for tile < -1. */
 vr_result_t vr_debug_stall_next(long long tile);
+
+/* Sets one of the options listed at the top of this header for the rest of
+ * the process (all threads, all devices); value -1 restores the built-in
+ * default.  Calls already enqueued are not affected.  Meant for tests and
+ * tuning: options choose among kernels that compute the same bits.
+ * Errors: VR_ERR_INVALID_ARGUMENT for an unknown name or value < -1. */
+vr_result_t vr_set_option(const char* name, long long value);
+
+/* The current value of an option (-1: the call site's built-in default).
+ * Errors: VR_ERR_INVALID_ARGUMENT for an unknown name or NULL value. */
+vr_result_t vr_get_option(const char* name, long long* value);
 
 /* Static English text for a result code ("unknown result" for others). */
 const char* vr_get_error_string(vr_result_t result);

@@ -9,7 +9,6 @@ and the next call must be bit-exact again.  Nothing here traps, faults or
 waits without a bound.
 """
 
-import os
 import time
 
 import numpy as np
@@ -26,18 +25,14 @@ if not torch.cuda.is_available():  # pragma: no cover
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
 import double_binary_tree_gb300 as vr  # noqa: E402
+from tests.options import options  # noqa: E402
 
 
 @pytest.fixture(autouse=True)
 def staged_path():
     """The bounded waits live in the shared-memory-staged kernels."""
-    old = os.environ.get("VR_KERNEL_PATH")
-    os.environ["VR_KERNEL_PATH"] = "staged"
-    yield
-    if old is None:
-        os.environ.pop("VR_KERNEL_PATH", None)
-    else:
-        os.environ["VR_KERNEL_PATH"] = old
+    with options(vr, VR_KERNEL_PATH="staged"):
+        yield
 
 
 @pytest.mark.parametrize("algo", [vr.VR_ALGO_RING, vr.VR_ALGO_TREE])

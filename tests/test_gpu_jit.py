@@ -2,7 +2,6 @@
 NVRTC) against the interpreting kernels and the oracle: both bit-exact on
 the same inputs, on the register and the staged path."""
 
-import os
 
 import numpy as np
 import pytest
@@ -18,6 +17,7 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU runs deselect these
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
 import double_binary_tree_gb300 as vr  # noqa: E402
+from tests.options import options  # noqa: E402
 
 TREE, RING = vr.VR_ALGO_TREE, vr.VR_ALGO_RING
 F32, F16, BF16 = vr.VR_FLOAT32, vr.VR_FLOAT16, vr.VR_BFLOAT16
@@ -26,22 +26,13 @@ SUM = vr.VR_SUM
 
 def _run(inp, dtype, op, nch, cb, L, jit, path):
     R, count = len(inp), inp[0].numel()
-    old = {k: os.environ.get(k) for k in ("VR_JIT", "VR_KERNEL_PATH")}
-    os.environ["VR_JIT"] = "1" if jit else "0"
-    os.environ["VR_KERNEL_PATH"] = path
-    try:
+    with options(vr, VR_JIT=1 if jit else 0, VR_KERNEL_PATH=path):
         src = [t.cuda() for t in inp]
         dst = [torch.empty_like(s) for s in src]
         vr.vr_allreduce_ex(src, dst, R, count, dtype, op, TREE, nch, cb, L,
                            torch.cuda.current_stream())
         assert vr.vr_stream_status(torch.cuda.current_stream()) == 0
         return [workloads.raw_numpy(d.cpu()) for d in dst]
-    finally:
-        for k, v in old.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = v
 
 
 def test_specialisation_is_available():
@@ -91,32 +82,23 @@ def test_specialised_ring_equals_oracle(R, dtype, op, count, nch, cb, path):
     inp = workloads.generate(R, count, dtype, "normal", 400 + R)
     want = oracle.allreduce([workloads.raw_numpy(t) for t in inp], dtype, op,
                             vr.VR_ALGO_RING, nch, cb)
-    old = {k: os.environ.get(k) for k in ("VR_JIT_RING", "VR_KERNEL_PATH")}
-    os.environ.update(VR_JIT_RING="1", VR_KERNEL_PATH=path)
-    try:
+    with options(vr, VR_JIT_RING=1, VR_KERNEL_PATH=path):
         src = [t.cuda() for t in inp]
         dst = [torch.empty_like(s) for s in src]
         vr.vr_allreduce(src, dst, R, count, dtype, op, vr.VR_ALGO_RING, nch, cb,
                         torch.cuda.current_stream())
         assert vr.vr_stream_status(torch.cuda.current_stream()) == 0
         got = [workloads.raw_numpy(d.cpu()) for d in dst]
-    finally:
-        for k, v in old.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = v
     assert vr.vr_jit_status()[2] == 0
     for r in range(R):
         assert np.array_equal(got[r], want[r]), "rank %d" % r
 
 
 @pytest.mark.parametrize("occ", ["0", "4"])
-def test_four_ctas_per_sm_same_bits(occ, monkeypatch):
+def test_four_ctas_per_sm_same_bits(occ):
     """The specialised register-path kernels compiled for four CTAs per SM
     (VR_JIT_OCC=4, rings included) give the oracle's bits, like those at
     their natural occupancy (VR_JIT_OCC=0)."""
-    monkeypatch.setenv("VR_JIT_OCC", occ)
     for R, dtype, algo, count in [(8, BF16, TREE, 300001), (7, BF16, TREE, 300001),
                                   (4, F32, TREE, 200003), (5, F16, RING, 300001),
                                   (8, F32, RING, 200003)]:
@@ -125,7 +107,9 @@ def test_four_ctas_per_sm_same_bits(occ, monkeypatch):
         want = oracle.allreduce(raws, dtype, SUM, algo, 12, 4096)
         src = [t.cuda() for t in inp]
         dst = [torch.empty_like(t) for t in src]
-        vr.vr_allreduce(src, dst, R, count, dtype, SUM, algo, 12, 4096, torch.cuda.current_stream())
+        with options(vr, VR_JIT_OCC=int(occ)):
+            vr.vr_allreduce(src, dst, R, count, dtype, SUM, algo, 12, 4096,
+                            torch.cuda.current_stream())
         assert vr.vr_stream_status(torch.cuda.current_stream()) == 0
         for d, w in zip(dst, want):
             assert np.array_equal(workloads.raw_numpy(d), w), (R, dtype, algo)

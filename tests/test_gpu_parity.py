@@ -7,7 +7,6 @@ Inputs come from workloads.py only; no expected value comes from the GPU.
 """
 
 import itertools
-import os
 
 import numpy as np
 import pytest
@@ -17,6 +16,7 @@ torch = pytest.importorskip("torch")
 import oracle  # noqa: E402
 import workloads  # noqa: E402
 from oracle import numerics, partition, schedules, topology  # noqa: E402
+from tests.options import options  # noqa: E402
 from tests.tolerances import check_against_fp64  # noqa: E402
 
 pytestmark = pytest.mark.gpu
@@ -39,13 +39,8 @@ def path(request):
     """Runs the test on one kernel family: the register path or the
     shared-memory-staged path (unaligned buffers always take the register
     path's element kernels)."""
-    old = os.environ.get("VR_KERNEL_PATH")
-    os.environ["VR_KERNEL_PATH"] = request.param
-    yield request.param
-    if old is None:
-        os.environ.pop("VR_KERNEL_PATH", None)
-    else:
-        os.environ["VR_KERNEL_PATH"] = old
+    with options(vr, VR_KERNEL_PATH=request.param):
+        yield request.param
 
 
 class Bufs:

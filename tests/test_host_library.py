@@ -526,3 +526,38 @@ def test_buffer_rules_match_brute_force(kind):
         assert (code != INV) == want, (trial, R, n, send, recv)
         seen[want] += 1
     assert seen[True] > 100 and seen[False] > 100
+
+
+def test_options_set_get_and_restore():
+    assert vr.vr_get_option("VR_KERNEL_PATH") in (0, 1, 2)
+    old = vr.vr_get_option("VR_STAGED_TILE_BYTES")
+    vr.vr_set_option("VR_STAGED_TILE_BYTES", 4096)
+    assert vr.vr_get_option("VR_STAGED_TILE_BYTES") == 4096
+    vr.vr_set_option("VR_STAGED_TILE_BYTES", -1)      # the built-in default
+    assert vr.vr_get_option("VR_STAGED_TILE_BYTES") == 0
+    vr.vr_set_option("VR_STAGED_TILE_BYTES", old)
+    for bad in (("VR_NO_SUCH_OPTION", 1), ("VR_PDL", -2)):
+        with pytest.raises(vr.VrError) as e:
+            vr.vr_set_option(*bad)
+        assert e.value.code == vr.VR_ERR_INVALID_ARGUMENT
+    with pytest.raises(vr.VrError):
+        vr.vr_get_option("VR_NO_SUCH_OPTION")
+
+
+def test_options_read_from_the_environment_once():
+    """A fresh process sees the environment's values at first use; changing
+    the environment later has no effect (no getenv on the call path)."""
+    import subprocess
+    import sys
+    code = (
+        "import os, double_binary_tree_gb300 as vr\n"
+        "a = vr.vr_get_option('VR_KERNEL_PATH'), vr.vr_get_option('VR_STAGED_STAGES'), "
+        "vr.vr_get_option('VR_DEBUG')\n"
+        "os.environ['VR_KERNEL_PATH'] = 'register'\n"
+        "os.environ['VR_STAGED_STAGES'] = '9'\n"
+        "b = vr.vr_get_option('VR_KERNEL_PATH'), vr.vr_get_option('VR_STAGED_STAGES')\n"
+        "print(a, b)\n")
+    env = dict(os.environ, VR_KERNEL_PATH="staged", VR_STAGED_STAGES="3", VR_DEBUG="X,GRAPH")
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, check=True,
+                         capture_output=True, text=True).stdout.strip()
+    assert out == "(2, 3, 1) (2, 3)"
