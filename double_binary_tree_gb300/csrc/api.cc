@@ -3,6 +3,7 @@
 #include <algorithm>
 #include <array>
 #include <atomic>
+#include <climits>
 #include <cstdint>
 #include <cstdlib>
 #include <cmath>
@@ -369,6 +370,14 @@ vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
   return VR_SUCCESS;
 }
 
+// A buffer of `count` elements of E bytes, `mult` blocks of it (the R blocks
+// of a ReduceScatter send or an AllGather receive buffer): its byte count
+// must fit the kernels' signed 64-bit offsets, and every count * E below is
+// computed only after this check.
+bool bytes_fit(size_t count, size_t E, size_t mult = 1) {
+  return E && mult && count <= (size_t)LLONG_MAX / E / mult;
+}
+
 bool valid_common(int R, int dtype, int nChannels, size_t chunkBytes) {
   return R >= 1 && R <= kMaxRanks && elem_size(dtype) && nChannels >= 1 &&
          nChannels <= kMaxChannels && chunkBytes > 0 && chunkBytes % kGrainBytes == 0;
@@ -579,11 +588,12 @@ vr_result_t plan_allreduce(const void* const* sendbufs, void* const* recvbufs, i
                            int nChannels, size_t chunkBytes, int localRanks, KArgs& a, int& mode,
                            int& stack) {
   if (algo == VR_ALGO_AUTO && valid_common(R, dtype, nChannels, chunkBytes) && localRanks >= 1 &&
-      R % localRanks == 0 &&
+      R % localRanks == 0 && bytes_fit(count, elem_size(dtype)) &&
       vr_select_algo(R, localRanks, count * elem_size(dtype), nullptr, &algo) != VR_SUCCESS)
     return VR_ERR_INTERNAL;
   if (!valid_common(R, dtype, nChannels, chunkBytes) || (op != VR_SUM && op != VR_MAX) ||
-      (algo != VR_ALGO_RING && algo != VR_ALGO_TREE) || localRanks < 1 || R % localRanks)
+      (algo != VR_ALGO_RING && algo != VR_ALGO_TREE) || localRanks < 1 || R % localRanks ||
+      !bytes_fit(count, elem_size(dtype)))
     return VR_ERR_INVALID_ARGUMENT;
   const size_t E = elem_size(dtype);
   vr_result_t e = check_buffers(sendbufs, recvbufs, R, count * E, count * E, kAR, E);
@@ -625,6 +635,17 @@ bool is_host_memory(const void* p) {
 }
 
 }  // namespace
+
+vr_result_t check_stepwise_args(const void* const* sendbufs, void* const* recvbufs, int R,
+                                size_t count, int dtype, int op, int nChannels,
+                                size_t chunkBytes) {
+  if (!valid_common(R, dtype, nChannels, chunkBytes) || (op != VR_SUM && op != VR_MAX) ||
+      !bytes_fit(count, elem_size(dtype)))
+    return VR_ERR_INVALID_ARGUMENT;
+  const size_t E = elem_size(dtype);
+  return check_buffers(sendbufs, recvbufs, R, count * E, count * E, kAR, E);
+}
+
 }  // namespace vr
 
 extern "C" {
@@ -658,7 +679,7 @@ vr_result_t vr_allreduce_host(const void* const* sendbufs, void* const* recvbufs
                               void* const* workbufs, size_t pieceBytes, void* stream) {
   if (pieceBytes == 0) pieceBytes = VR_HOST_PIECE_BYTES;
   if (pieceBytes % kGrainBytes || !sendbufs || !recvbufs || !workbufs ||
-      !valid_common(R, dtype, nChannels, chunkBytes))
+      !valid_common(R, dtype, nChannels, chunkBytes) || !bytes_fit(count, elem_size(dtype)))
     return VR_ERR_INVALID_ARGUMENT;
   const size_t E = elem_size(dtype);
   // the host side: distinct buffers, in place allowed, NULL receive buffers skipped
@@ -734,7 +755,8 @@ vr_result_t vr_allreduce(const void* const* sendbufs, void* const* recvbufs, int
 vr_result_t vr_allreduce_trees(const void* const* sendbufs, void* const* recvbufs, int R,
                                size_t count, vr_dtype_t dtype, vr_op_t op, int nChannels,
                                size_t chunkBytes, const vr_tree_t* trees, void* stream) {
-  if (!valid_common(R, dtype, nChannels, chunkBytes) || (op != VR_SUM && op != VR_MAX) || !trees)
+  if (!valid_common(R, dtype, nChannels, chunkBytes) || (op != VR_SUM && op != VR_MAX) || !trees ||
+      !bytes_fit(count, elem_size(dtype)))
     return VR_ERR_INVALID_ARGUMENT;
   for (int c = 0; c < nChannels; ++c)
     if (!valid_tree(trees + (size_t)c * R, R)) return VR_ERR_INVALID_ARGUMENT;
@@ -774,7 +796,8 @@ vr_result_t vr_reduce_scatter(const void* const* sendbufs, void* const* recvbufs
                               size_t recvcount, vr_dtype_t dtype, vr_op_t op, vr_algo_t algo,
                               int nChannels, size_t chunkBytes, void* stream) {
   if (!valid_common(R, dtype, nChannels, chunkBytes) || (op != VR_SUM && op != VR_MAX) ||
-      (algo != VR_ALGO_RING && algo != VR_ALGO_TREE))
+      (algo != VR_ALGO_RING && algo != VR_ALGO_TREE) ||
+      !bytes_fit(recvcount, elem_size(dtype), (size_t)R))
     return VR_ERR_INVALID_ARGUMENT;
   if (algo == VR_ALGO_TREE) return VR_ERR_UNSUPPORTED;
   const size_t E = elem_size(dtype);
@@ -803,7 +826,8 @@ vr_result_t vr_allgather(const void* const* sendbufs, void* const* recvbufs, int
                          size_t sendcount, vr_dtype_t dtype, vr_algo_t algo, int nChannels,
                          size_t chunkBytes, void* stream) {
   if (!valid_common(R, dtype, nChannels, chunkBytes) ||
-      (algo != VR_ALGO_RING && algo != VR_ALGO_TREE))
+      (algo != VR_ALGO_RING && algo != VR_ALGO_TREE) ||
+      !bytes_fit(sendcount, elem_size(dtype), (size_t)R))
     return VR_ERR_INVALID_ARGUMENT;
   if (algo == VR_ALGO_TREE) return VR_ERR_UNSUPPORTED;
   const size_t bytes = sendcount * elem_size(dtype);
@@ -858,18 +882,17 @@ vr_result_t vr_allgather(const void* const* sendbufs, void* const* recvbufs, int
 
 size_t vr_ring_stepwise_scratch_bytes(size_t count, vr_dtype_t dtype) {
   const size_t E = elem_size(dtype);
-  return E ? (count * E + 15) / 16 * 16 : 0;
+  return bytes_fit(count, E) ? (count * E + 15) / 16 * 16 : 0;
 }
 
 vr_result_t vr_allreduce_ring_stepwise(const void* const* sendbufs, void* const* recvbufs, int R,
                                        size_t count, vr_dtype_t dtype, vr_op_t op,
                                        int nChannels, size_t chunkBytes, void* scratch,
                                        size_t scratchBytes, void* stream) {
-  if (!valid_common(R, dtype, nChannels, chunkBytes) || (op != VR_SUM && op != VR_MAX))
-    return VR_ERR_INVALID_ARGUMENT;
-  const size_t E = elem_size(dtype);
-  vr_result_t e = check_buffers(sendbufs, recvbufs, R, count * E, count * E, kAR, E);
+  vr_result_t e = check_stepwise_args(sendbufs, recvbufs, R, count, dtype, op, nChannels,
+                                      chunkBytes);
   if (e != VR_SUCCESS || count == 0) return e;
+  const size_t E = elem_size(dtype);
   const size_t need = vr_ring_stepwise_scratch_bytes(count, dtype);
   if (!scratch || scratchBytes < need || (uintptr_t)scratch % E) return VR_ERR_INVALID_ARGUMENT;
   for (int r = 0; r < R; ++r)
@@ -910,7 +933,7 @@ vr_result_t vr_allreduce_tree_updown(const void* const* sendbufs, void* const* r
                                      size_t count, vr_dtype_t dtype, vr_op_t op, int nChannels,
                                      size_t chunkBytes, int localRanks, void* stream) {
   if (!valid_common(R, dtype, nChannels, chunkBytes) || (op != VR_SUM && op != VR_MAX) ||
-      localRanks < 1 || R % localRanks)
+      localRanks < 1 || R % localRanks || !bytes_fit(count, elem_size(dtype)))
     return VR_ERR_INVALID_ARGUMENT;
   const size_t E = elem_size(dtype);
   vr_result_t e = check_buffers(sendbufs, recvbufs, R, count * E, count * E, kAR, E);

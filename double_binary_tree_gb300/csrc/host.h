@@ -32,6 +32,12 @@ constexpr long long kDebugGraph = 1;  // print tree, ring and partition tables
 long long option(Option o);
 long long option_or(Option o, long long dflt);
 
+// The argument and buffer checks of the stepwise ring AllReduce, its
+// scratch aside (api.cc): VR_SUCCESS or the code the call returns.
+vr_result_t check_stepwise_args(const void* const* sendbufs, void* const* recvbufs, int R,
+                                size_t count, int dtype, int op, int nChannels,
+                                size_t chunkBytes);
+
 void btree(int n, int r, int* up, int* d0, int* d1, int* childType);
 void dtree(int n, int r, int t[2][4]);
 int channel_tree(int c, int nCh);

@@ -11,13 +11,14 @@
 #include <map>
 #include <mutex>
 
-#include "../../include/vr.h"
+#include "host.h"
 
 namespace {
 
-// The FIFO.  Every GPU that loads the library holds these
+// The FIFO.  Every GPU that loads this file's module holds these
 // VR_NOALLOC_SCRATCH_BYTES bytes until the process exits; all calls share
-// them.
+// them.  CUDA loads modules lazily by default, so on a device the array
+// comes into being at the first call there (the address lookup below).
 static __device__ __align__(256) unsigned char g_noalloc_fifo[VR_NOALLOC_SCRATCH_BYTES];
 
 std::mutex g_mu;
@@ -48,6 +49,10 @@ extern "C" vr_result_t vr_allreduce_ring_stepwise_noalloc(const void* const* sen
                                                           size_t count, vr_dtype_t dtype,
                                                           vr_op_t op, int nChannels,
                                                           size_t chunkBytes, void* stream) {
+  // the arguments first: a bad call is INVALID_ARGUMENT whatever its size
+  const vr_result_t bad = vr::check_stepwise_args(sendbufs, recvbufs, R, count, dtype, op,
+                                                  nChannels, chunkBytes);
+  if (bad != VR_SUCCESS) return bad;
   const size_t need = vr_ring_stepwise_scratch_bytes(count, dtype);
   if (need > VR_NOALLOC_SCRATCH_BYTES) return VR_ERR_UNSUPPORTED;
   void* fifo = nullptr;

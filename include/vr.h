@@ -365,9 +365,14 @@ vr_result_t vr_allreduce_ring_stepwise(const void* const* sendbufs, void* const*
  * without scratch/scratchBytes, plus VR_ERR_UNSUPPORTED when count elements
  * of dtype exceed VR_NOALLOC_SCRATCH_BYTES (2 Mi fp32 or 4 Mi 16-bit
  * elements per rank at most).
+ * Arguments are checked first (VR_ERR_INVALID_ARGUMENT as for the other
+ * entry point), the size limit after them.
  * Set-up: the first call on a device looks up the array's device address on
- * that device (the device current at the call); make that first call before
- * any stream capture.
+ * that device (the device current at the call).  CUDA loads modules lazily,
+ * so that first call is also when the device's copy of the array is
+ * created: make it before any stream capture, and before the caller's own
+ * allocator takes the device's memory (else it can fail with
+ * VR_ERR_CUDA).  A call with count == 0 does nothing, set-up included.
  * Sharing: every call on a device uses the same array, which keeps the last
  * call's contents; nothing in it needs to start at zero (each step writes
  * every message before it is read).  Calls whose executions overlap on the

@@ -561,3 +561,45 @@ def test_options_read_from_the_environment_once():
     out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, check=True,
                          capture_output=True, text=True).stdout.strip()
     assert out == "(2, 3, 1) (2, 3)"
+
+
+def test_byte_counts_that_overflow_are_invalid_arguments():
+    """A count whose byte size does not fit a signed 64-bit offset (for
+    ReduceScatter and AllGather: R blocks of it) is rejected before any
+    multiplication could wrap; the fake pointers are never touched."""
+    R = 4
+    fake = [0x1000 * (i + 1) << 32 for i in range(R)]
+    out = [0x9000 * (i + 1) << 32 for i in range(R)]
+    huge = 1 << 62                       # * 4 bytes wraps a 64-bit count
+    calls = [
+        lambda: vr.vr_allreduce(fake, out, R, huge, vr.VR_FLOAT32, 0, 0, 1, 16),
+        lambda: vr.vr_allreduce(fake, out, R, huge, vr.VR_FLOAT32, 0, vr.VR_ALGO_AUTO, 1, 16),
+        lambda: vr.vr_allreduce_tree_updown(fake, out, R, huge, vr.VR_FLOAT32, 0, 1, 16, 1),
+        lambda: vr.vr_reduce_scatter(fake, out, R, 1 << 60, vr.VR_FLOAT32, 0, 0, 1, 16),
+        lambda: vr.vr_allgather(fake, out, R, 1 << 60, vr.VR_FLOAT32, 0, 1, 16),
+        lambda: vr.vr_allreduce_ring_stepwise(fake, out, R, huge, vr.VR_FLOAT32, 0, 1, 16,
+                                              0x77 << 40, 1 << 20),
+        lambda: vr.vr_allreduce_ring_stepwise_noalloc(fake, out, R, huge, vr.VR_FLOAT32, 0, 1,
+                                                      16),
+    ]
+    for i, call in enumerate(calls):
+        with pytest.raises(vr.VrError) as e:
+            call()
+        assert e.value.code == vr.VR_ERR_INVALID_ARGUMENT, i
+    assert vr.vr_ring_stepwise_scratch_bytes(huge, vr.VR_FLOAT32) == 0
+
+
+def test_noalloc_checks_arguments_before_its_size_limit():
+    """A call that is wrong in itself is INVALID_ARGUMENT even when it is
+    also too large for the array (too large alone: UNSUPPORTED, checked on
+    the GPU)."""
+    big = vr.VR_NOALLOC_SCRATCH_BYTES  # elements: 4x the array in fp32
+    fake = [0x1000 * (i + 1) << 32 for i in range(2)]
+    for args in [([None, fake[1]], fake, 2, big, 0, 0, 1, 16),     # NULL send buffer
+                 (fake, fake[:1] + [fake[0]], 2, big, 0, 0, 1, 16),  # two ranks, one buffer
+                 (fake, [f + (1 << 40) for f in fake], 0, big, 0, 0, 1, 16),  # R = 0
+                 (fake, [f + (1 << 40) for f in fake], 2, big, 0, 7, 1, 16),  # op
+                 (fake, [f + (1 << 40) for f in fake], 2, big, 0, 0, 1, 15)]:  # chunk bytes
+        with pytest.raises(vr.VrError) as e:
+            vr.vr_allreduce_ring_stepwise_noalloc(*args)
+        assert e.value.code == vr.VR_ERR_INVALID_ARGUMENT, args

@@ -68,3 +68,38 @@ def test_noalloc_rejects_sizes_beyond_its_array():
         vr.vr_allreduce_ring_stepwise_noalloc(src, dst, 2, count, vr.VR_FLOAT32, vr.VR_SUM, 1, 16)
     assert ei.value.code == vr.VR_ERR_UNSUPPORTED
     assert vr.vr_launch_count() == before
+
+
+def test_noalloc_allocates_nothing():
+    """After the first call on the device (which looks up the array and, with
+    lazily loaded modules, brings it into being), further calls leave the
+    device's free memory unchanged: no allocation by the library, by CUDA
+    on its behalf, or by torch."""
+    R, count, dtype = 8, 1 << 20, vr.VR_FLOAT32
+    inp = workloads.generate(R, count, dtype, "normal", 1310)
+    src = [t.cuda() for t in inp]
+    dst = [torch.empty_like(s) for s in src]
+    vr.vr_allreduce_ring_stepwise_noalloc(src, dst, R, count, dtype, vr.VR_SUM, 12, 512 * 1024)
+    assert vr.vr_stream_status() == vr.VR_SUCCESS
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(4):
+        vr.vr_allreduce_ring_stepwise_noalloc(src, dst, R, count, dtype, vr.VR_SUM, 12,
+                                              512 * 1024)
+    assert vr.vr_stream_status() == vr.VR_SUCCESS
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+
+
+def test_noalloc_empty_and_single_rank():
+    """count == 0 launches nothing and leaves the outputs alone; R == 1 is the
+    copy of the input (no ring step)."""
+    src = [torch.arange(16, dtype=torch.float32, device="cuda") for _ in range(3)]
+    dst = [torch.full_like(s, -1.0) for s in src]
+    before = vr.vr_launch_count()
+    vr.vr_allreduce_ring_stepwise_noalloc(src, dst, 3, 0, vr.VR_FLOAT32, vr.VR_SUM, 2, 64)
+    assert vr.vr_launch_count() == before
+    assert all(bool((d == -1.0).all()) for d in dst)
+    inp = workloads.generate(1, 100003, vr.VR_BFLOAT16, "normal", 1320)
+    for _ in range(2):
+        got = _run_noalloc(inp, vr.VR_BFLOAT16, vr.VR_MAX, 3, 4096)
+        assert np.array_equal(got[0], workloads.raw_numpy(inp[0]))
