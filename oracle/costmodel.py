@@ -11,10 +11,15 @@ Sources:
 * [Interview] section "推导 / 关键公式": ring latency term 2(n-1) alpha, per-card
   traffic 2(n-1)/n * S; tree latency ~ 2 log2(n) alpha, traffic ~ 2S.
 
-Reading: the model's two terms are fitted per algorithm by least squares to
+Readings: the model's two terms are fitted per algorithm by least squares to
 measured times (alpha in microseconds per stage, 1/B in microseconds per
 byte of the model's traffic term); the predicted crossover is where the two
-lines meet.
+lines meet.  The pages give the model's form, not how to fit it.  Measured
+times span several decades (8 B to 256 MiB messages), so the fit that sets
+the model's constants weighs every sample by its own size: it minimises the
+sum of squared relative errors (prediction - t) / t (``fit_relative``), and a
+sample whose time is not positive carries no information and is left out.
+``fit`` is the plain (absolute) least-squares fit of the same model.
 """
 
 import numpy as np
@@ -61,6 +66,18 @@ def fit(stages, traffic, times):
     """Least-squares (alpha, inv_bw) for times ~ alpha*stages + inv_bw*traffic."""
     A = np.stack([np.asarray(stages, float), np.asarray(traffic, float)], axis=1)
     sol, *_ = np.linalg.lstsq(A, np.asarray(times, float), rcond=None)
+    return float(sol[0]), float(sol[1])
+
+
+def fit_relative(stages, traffic, times):
+    """(alpha, inv_bw) minimising sum over samples with t > 0 of
+    ((alpha*stages + inv_bw*traffic - t) / t)**2: least squares of the rows
+    (stages/t, traffic/t) against 1."""
+    keep = [i for i, t in enumerate(times) if t > 0]
+    t = np.asarray([times[i] for i in keep], float)
+    A = np.stack([np.asarray([stages[i] for i in keep], float) / t,
+                  np.asarray([traffic[i] for i in keep], float) / t], axis=1)
+    sol, *_ = np.linalg.lstsq(A, np.ones(len(keep)), rcond=None)
     return float(sol[0]), float(sol[1])
 
 

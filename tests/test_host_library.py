@@ -421,8 +421,9 @@ def test_fit_recovers_a_planted_model():
 
 
 def test_fit_minimises_relative_squared_error():
-    """Noisy times: the fit equals the least-squares solution of the rows
-    (stages, traffic) / t against 1, from numpy; samples <= 0 are left out."""
+    """Noisy times: the library's fit equals the oracle's relative
+    least-squares fit (oracle.costmodel.fit_relative) of the same samples,
+    with the oracle's stage and traffic terms; samples <= 0 are left out."""
     rng = np.random.default_rng(6)
     Rs, Ls, Ms = _samples(rng)
     ring = [ocost.t_ring(R, M, 0.6, 1.2e-6) * (1 + 0.2 * rng.standard_normal())
@@ -430,19 +431,14 @@ def test_fit_minimises_relative_squared_error():
     tree = [ocost.t_tree(_oracle_depth(R, L), M, 0.8, 9e-7) * (1 + 0.2 * rng.standard_normal())
             for R, L, M in zip(Rs, Ls, Ms)]
     tree[3] = 0.0                              # left out
+    ring[7] = -1.0                             # left out
     got = vr.vr_fit_cost_model(Rs, Ls, Ms, ring, tree)
     for alg, t in ((0, ring), (1, tree)):
-        rows, rhs = [], []
-        for R, L, M, ti in zip(Rs, Ls, Ms, t):
-            if ti <= 0:
-                continue
-            s, b = (ocost.ring_terms(R, M) if alg == 0 else
-                    ocost.tree_terms(_oracle_depth(R, L), M))
-            rows.append([s / ti, b / ti])
-            rhs.append(1.0)
-        sol = np.linalg.lstsq(np.array(rows), np.array(rhs), rcond=None)[0]
-        assert got[0][alg] == pytest.approx(sol[0], rel=1e-7)
-        assert got[1][alg] == pytest.approx(sol[1], rel=1e-7)
+        terms = [ocost.ring_terms(R, M) if alg == 0 else
+                 ocost.tree_terms(_oracle_depth(R, L), M) for R, L, M in zip(Rs, Ls, Ms)]
+        a, ib = ocost.fit_relative([x[0] for x in terms], [x[1] for x in terms], t)
+        assert got[0][alg] == pytest.approx(a, rel=1e-7)
+        assert got[1][alg] == pytest.approx(ib, rel=1e-7)
 
 
 def test_fit_argument_errors():

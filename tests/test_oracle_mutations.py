@@ -274,6 +274,12 @@ REWRITES = [
      "np.asarray(stages, float), np.asarray(traffic, float)",
      "np.asarray(traffic, float), np.asarray(stages, float)",
      ["test_cost_model_fit_recovers_parameters"]),
+    ("relative fit without the weighting (absolute least squares)", costmodel, "fit_relative",
+     "], float) / t,", "], float) / 1.0,",
+     ["test_cost_model_relative_fit_by_hand"]),
+    ("relative fit keeps samples whose time is not positive", costmodel, "fit_relative",
+     "if t > 0]", "if t > 0 or t <= 0]",
+     ["test_cost_model_relative_fit_by_hand"]),
     ("selection picks the slower algorithm", costmodel, "select",
      "t_ring(N, M, *ring) <= t_tree(D, M, *tree)", "t_ring(N, M, *ring) > t_tree(D, M, *tree)",
      ["test_cost_model_selects_lower_prediction_by_hand"]),

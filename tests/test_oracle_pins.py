@@ -662,3 +662,47 @@ def test_cost_model_fit_recovers_parameters():
     times = [cm.predict(s, b, 2.5, 3e-4) for s, b in zip(stages, traffic)]
     a, ib = cm.fit(stages, traffic, times)
     assert abs(a - 2.5) < 1e-9 and abs(ib - 3e-4) < 1e-12
+
+
+def test_cost_model_relative_fit_by_hand():
+    # samples (stages, traffic, t): (1, 0, 1), (0, 1, 1), (1, 1, 3).  Relative
+    # rows (s/t, b/t) = (1, 0), (0, 1), (1/3, 1/3) against 1; normal equations
+    # [[10/9, 1/9], [1/9, 10/9]] (a, b) = (4/3, 4/3), so a = b = 12/11.  The
+    # absolute fit of the same samples gives 4/3: the weighting is the pin.
+    # Samples whose time is not positive are left out.
+    from oracle import costmodel as cm
+    a, b = cm.fit_relative([1, 0, 1], [0, 1, 1], [1.0, 1.0, 3.0])
+    assert abs(a - 12 / 11) < 1e-12 and abs(b - 12 / 11) < 1e-12
+    a2, b2 = cm.fit([1, 0, 1], [0, 1, 1], [1.0, 1.0, 3.0])
+    assert abs(a2 - 4 / 3) < 1e-12 and abs(b2 - 4 / 3) < 1e-12
+    a3, b3 = cm.fit_relative([1, 0, 5, 1, 2], [0, 1, 5, 1, 3], [1.0, 1.0, 0.0, 3.0, -1.0])
+    assert abs(a3 - 12 / 11) < 1e-12 and abs(b3 - 12 / 11) < 1e-12
+
+
+def test_cost_model_relative_fit_properties():
+    from oracle import costmodel as cm
+    rng = np.random.default_rng(32)
+    stages = list(rng.integers(2, 130, 40).astype(float))
+    traffic = list(np.geomspace(8, 1e9, 40) * (1 + rng.random(40)))
+    exact = [cm.predict(s, b, 0.4, 7e-7) for s, b in zip(stages, traffic)]
+    a, ib = cm.fit_relative(stages, traffic, exact)           # a planted model
+    assert abs(a - 0.4) < 1e-9 and abs(ib / 7e-7 - 1) < 1e-9
+    noisy = [t * (1 + 0.3 * rng.standard_normal()) for t in exact]
+    a, ib = cm.fit_relative(stages, traffic, noisy)
+    # the relative residuals are orthogonal to both relative columns (the
+    # minimum of a least-squares objective)
+    r = [(a * s + ib * b - t) / t for s, b, t in zip(stages, traffic, noisy)]
+    assert abs(sum(ri * s / t for ri, s, t in zip(r, stages, noisy))) < 1e-8 * len(r)
+    assert abs(sum(ri * b / t for ri, b, t in zip(r, traffic, noisy))) < 1e-8 * len(r)
+    # and no nearby point does better
+    def obj(x, y):
+        return sum(((x * s + y * b - t) / t) ** 2 for s, b, t in zip(stages, traffic, noisy))
+    best = obj(a, ib)
+    for da, db in ((1e-3, 0), (-1e-3, 0), (0, 1e-3), (0, -1e-3), (1e-3, 1e-3)):
+        assert obj(a * (1 + da), ib * (1 + db)) > best
+    # a sample scaled as a whole (stages, traffic and time by the same factor)
+    # weighs the same: the fit does not change
+    s2, b2, t2 = list(stages), list(traffic), list(noisy)
+    s2[0], b2[0], t2[0] = s2[0] * 1000, b2[0] * 1000, t2[0] * 1000
+    a2, ib2 = cm.fit_relative(s2, b2, t2)
+    assert abs(a2 / a - 1) < 1e-9 and abs(ib2 / ib - 1) < 1e-9
