@@ -19,34 +19,36 @@
 
 namespace vr {
 
-// Bit-trick binary tree over n nodes, node r.  The lowest set bit b of r
-// (searched among 1, 2, 4, ... below n) is r's level.  Node 0 is the root
-// with the single child "largest power of two below n".  Another node's
-// parent clears b and sets 2b, or only clears b when 2b would leave the
-// range; its children are r -/+ b/2, the upper one moved down by halving the
-// offset until it exists (and dropped once the offset reaches zero).
+// The largest power of two not above x (x >= 1).
+static int bit_floor(int x) {
+  int p = 1;
+  while (p <= x / 2) p <<= 1;
+  return p;
+}
+
+// Node r of the bit-trick binary tree over n nodes ([Course13] "Btree 的 bit
+// 构造"), in closed form.  A node's level is its lowest set bit b.  Its
+// parent is one of r - b and r + b, the one whose own lowest set bit is 2b
+// -- r + b exactly when bit 2b of r is clear -- and r - b when r + b is not
+// a node.  Its lower child is r - b/2; its upper child r + o for the largest
+// power of two o <= b/2 that is still a node (none for the last node).  Node
+// 0 is the root, whose only child is the largest power of two below n.
+// childType: 0 when r is below its parent, else 1 (-1 for the root).
 void btree(int n, int r, int* up, int* d0, int* d1, int* childType) {
-  int b = 1;
-  while (b < n && (b & r) == 0) b <<= 1;
   if (r == 0) {
     *up = -1;
     *d0 = -1;
-    *d1 = n > 1 ? (b >> 1) : -1;
+    *d1 = n > 1 ? bit_floor(n - 1) : -1;
     *childType = -1;
     return;
   }
-  int p = (r ^ b) | (b << 1);
-  if (p >= n) p = r ^ b;
-  *up = p;
-  *childType = r < p ? 0 : 1;
-  int half = b >> 1;
+  const int b = r & -r;
+  const bool above = (r & (b << 1)) == 0 && r + b < n;
+  *up = above ? r + b : r - b;
+  *childType = above ? 0 : 1;
+  const int half = b >> 1, room = n - 1 - r;
   *d0 = half ? r - half : -1;
-  int hi = half ? r + half : -1;
-  while (hi >= n) {            // the page's loop: re-evaluate, then halve
-    hi = half ? r + half : -1;
-    half >>= 1;
-  }
-  *d1 = hi;
+  *d1 = half && room > 0 ? r + bit_floor(half < room ? half : room) : -1;
 }
 
 // Node r's place in both trees: tree 0 is btree; tree 1 runs btree on a

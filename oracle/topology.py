@@ -30,6 +30,8 @@ Readings where the pages are silent:
   [0, ceil(nCh/2)) use tree 0, the rest tree 1; one channel uses tree 0 only.
 """
 
+import functools
+import math
 from dataclasses import dataclass, field
 from typing import List
 
@@ -46,39 +48,56 @@ def build_ring(R, n_channels):
 
 
 # ------------------------------------------------------------------ trees
-def btree(n, r):
-    """Node r of the bit-trick binary tree over n nodes.
+def _level(v):
+    """A node's level in the bit-trick tree: the lowest set bit of its index
+    (1, 2, 4, ...); node 0, the root, lies above every level."""
+    return math.inf if v == 0 else v & -v
 
-    The lowest set bit b of r (scanning b = 1, 2, 4, ... while b < n) fixes
-    r's level.  Node 0 is the root; its single child is the largest power of
-    two below n.  Any other node's parent clears b and sets the next bit up,
-    falling back to only clearing b when that leaves the range.  Its children
-    sit b/2 below and b/2 above; the upper child is pulled closer by halving
-    the offset until it lands inside the range, and disappears at offset 0.
+
+@functools.lru_cache(maxsize=None)
+def _parents(n):
+    """Every node's parent in the tree of the levels over n nodes (see
+    ``btree``): the nearer-level of its nearest higher-level neighbours."""
+    def parent(v):
+        if v == 0:
+            return -1
+        lv = _level(v)
+        left = next(u for u in range(v - 1, -1, -1) if _level(u) > lv)
+        right = next((u for u in range(v + 1, n) if _level(u) > lv), None)
+        if right is None or _level(left) < _level(right):
+            return left
+        return right
+    return tuple(parent(v) for v in range(n))
+
+
+def btree(n, r):
+    """Node r of the bit-trick binary tree over n nodes ([Course13] "Btree 的
+    bit 构造").
+
+    The section builds the tree from each node's lowest set bit: the parent
+    is found by clearing that bit and setting the next one up (only clearing
+    it when that leaves the range), and the children sit half that bit to
+    either side, the upper one pulled closer until it exists.  The tree those
+    steps give is, read in index order, the tree of the levels: every node
+    hangs under the nearer-level one of the nearest higher-level node on its
+    left and the nearest higher-level node on its right (the left one when
+    there is none on the right).  A node's lower child is then the child on
+    its left and its upper child the child on its right.  That form is
+    written out here by brute force over all n nodes, so it shares no step
+    with the bit arithmetic (the pins compare it with the pages' tables).
+
     parentChildType is 0 when r lies below its parent, else 1 (-1 for the
-    root, whose type the page's routine leaves unset).
+    root, whose type the section leaves unset).
 
     Returns (up, d0, d1, parentChildType)."""
     if not (0 <= r < n):
         raise ValueError("rank %d outside [0, %d)" % (r, n))
-    b = 1
-    while b < n and not (b & r):
-        b <<= 1
-    if r == 0:
-        return (-1, -1, (b >> 1) if n > 1 else -1, -1)
-    up = (r ^ b) | (b << 1)
-    if up >= n:
-        up = r ^ b
-    ptype = 0 if r < up else 1
-    low = b >> 1
-    d0 = r - low if low else -1
-    d1 = r + low if low else -1
-    # The page's loop recomputes the candidate before halving the offset, so
-    # its first pass repeats the same value; follow it as written.
-    while d1 >= n:
-        d1 = r + low if low else -1
-        low >>= 1
-    return (up, d0, d1, ptype)
+    par = _parents(n)
+    up = par[r]
+    kids = [v for v in range(n) if par[v] == r]
+    d0 = next((v for v in kids if v < r), -1)
+    d1 = next((v for v in kids if v > r), -1)
+    return (up, d0, d1, -1 if up == -1 else (0 if r < up else 1))
 
 
 def dtree(n, r):

@@ -3,6 +3,7 @@ on the CPU (monkeypatch, undone after the test), makes at least one pin of
 tests/test_oracle_pins.py fail.  A mutation that every pin let through would
 mean a mistake of that kind could hide in the oracle."""
 
+import functools
 import inspect
 import textwrap
 
@@ -29,6 +30,11 @@ def _caught(checks):
 def _rewrite(monkeypatch, module, name, old, new):
     """Install, for the test's duration, module.name with the one occurrence
     of ``old`` in its source replaced by ``new``."""
+    for attr, fn in list(vars(module).items()):
+        if hasattr(fn, "cache_clear"):
+            # a cache of the test's own, so that nothing computed under the
+            # mutation outlives it (or was computed before it)
+            monkeypatch.setattr(module, attr, functools.lru_cache(maxsize=None)(fn.__wrapped__))
     src = textwrap.dedent(inspect.getsource(getattr(module, name)))
     assert src.count(old) == 1, (name, old)
     ns = dict(vars(module))
@@ -174,12 +180,18 @@ REWRITES = [
     ("tree halves swapped", topology, "channel_tree_index",
      "return 0 if channel", "return 1 if channel",
      ["test_channel_to_tree_split"]),
-    ("children one level too far", topology, "btree",
-     "low = b >> 1", "low = b",
+    ("parent is the farther of the higher-level neighbours", topology, "_parents",
+     "_level(left) < _level(right)", "_level(left) > _level(right)",
      ["test_dtree4_figure", "test_hand_derived_trees_r8_r7", "test_tree_invariants"]),
-    ("parent falls back to setting the next bit only", topology, "btree",
-     "up = r ^ b\n", "up = r | (b << 1)\n",
+    ("parent on the right even past the end", topology, "_parents",
+     "if right is None or", "if right is not None and",
      ["test_dtree4_figure", "test_hand_derived_trees_r8_r7", "test_tree_invariants"]),
+    ("level from the highest set bit", topology, "_level",
+     "v & -v", "1 << (v.bit_length() - 1)",
+     ["test_dtree4_figure", "test_hand_derived_trees_r8_r7", "test_tree_invariants"]),
+    ("root not above every level", topology, "_level",
+     "math.inf if v == 0", "0 if v == 0",
+     ["test_btree_root_and_parent_types"]),
     ("odd double tree shifted the other way", topology, "dtree",
      "btree(n, (r - 1 + n) % n)", "btree(n, (r + 1) % n)",
      ["test_probe_table", "test_odd_overlap_at_node0", "test_tree_invariants"]),
