@@ -15,7 +15,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libvr.so")
 SOURCES = ["topology.cc", "api.cc", "kernels_f32.cu", "kernels_f16.cu", "kernels_bf16.cu",
            "kernels_copy.cu", "kernels_ablation.cu", "noalloc.cu", "jit.cc",
-           "costmodel.cc", "options.cc"]
+           "costmodel.cc", "options.cc", "graphlog.cc"]
 HEADERS = ["common.h", "host.h", "fold.cuh", "kernels.cuh", "staged.cuh", "ablation.cuh", "gather.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -514,11 +514,8 @@ extern "C" {
 vr_result_t vr_build_ring(int R, int nChannels, int* next, int* prev) {
   if (R < 1 || R > kMaxRanks || nChannels < 1 || nChannels > kMaxChannels || !next || !prev)
     return VR_ERR_INVALID_ARGUMENT;
-  for (int c = 0; c < nChannels; ++c)
-    for (int r = 0; r < R; ++r) {
-      next[c * R + r] = (r + 1) % R;
-      prev[c * R + r] = (r + R - 1) % R;
-    }
+  build_ring(R, nChannels, next, prev);
+  log_ring(next, R, nChannels);
   return VR_SUCCESS;
 }
 
@@ -526,7 +523,9 @@ vr_result_t vr_build_dtree(int nNodes, int localRanks, int nChannels, vr_tree_t*
   if (nNodes < 1 || localRanks < 1 || nNodes > kMaxRanks || localRanks > kMaxRanks ||
       nNodes * localRanks > kMaxRanks || nChannels < 1 || nChannels > kMaxChannels || !trees)
     return VR_ERR_INVALID_ARGUMENT;
-  return build_dtree(nNodes, localRanks, nChannels, trees);
+  const vr_result_t e = build_dtree(nNodes, localRanks, nChannels, trees);
+  if (e == VR_SUCCESS) log_trees(trees, nNodes * localRanks, nChannels);
+  return e;
 }
 
 vr_result_t vr_build_dtree_ex(int nNodes, int localRanks, int nChannels,
@@ -537,7 +536,10 @@ vr_result_t vr_build_dtree_ex(int nNodes, int localRanks, int nChannels,
       (pattern != VR_PATTERN_TREE && pattern != VR_PATTERN_SPLIT_TREE &&
        pattern != VR_PATTERN_BALANCED_TREE))
     return VR_ERR_INVALID_ARGUMENT;
-  return build_dtree_ex(nNodes, localRanks, nChannels, pattern, intraOrders, trees);
+  const vr_result_t e =
+      build_dtree_ex(nNodes, localRanks, nChannels, pattern, intraOrders, trees);
+  if (e == VR_SUCCESS) log_trees(trees, nNodes * localRanks, nChannels);
+  return e;
 }
 
 vr_result_t vr_partition(size_t count, vr_dtype_t dtype, int nChannels, int channel,
@@ -610,6 +612,15 @@ vr_result_t plan_allreduce(const void* const* sendbufs, void* const* recvbufs, i
     if ((e = tree_programs(R / localRanks, localRanks, &p)) != VR_SUCCESS) return e;
     set_dtree_programs(a, p, nChannels);
     stack = std::max(p[0].depth, p[1].depth);
+  }
+  if (count > 0 && graph_logging()) {
+    static vr_tree_t trees[kMaxRanks * kMaxChannels];  // under the log's own lock below
+    static std::mutex mu;
+    std::lock_guard<std::mutex> g(mu);
+    const bool tree = mode == kTreeAllReduce &&
+                      build_dtree(R / localRanks, localRanks, nChannels, trees) == VR_SUCCESS;
+    log_plan("allreduce", algo, R, localRanks, count, dtype, nChannels, chunkBytes,
+             tree ? trees : nullptr, true);
   }
   return VR_SUCCESS;
 }
@@ -763,6 +774,7 @@ vr_result_t vr_allreduce_trees(const void* const* sendbufs, void* const* recvbuf
   const size_t E = elem_size(dtype);
   vr_result_t e = check_buffers(sendbufs, recvbufs, R, count * E, count * E, kAR, E);
   if (e != VR_SUCCESS || count == 0) return e;
+  log_plan("allreduce", VR_ALGO_TREE, R, 0, count, dtype, nChannels, chunkBytes, trees, true);
   KArgs a;
   std::memset(&a, 0, sizeof(a));
   a.R = R;
@@ -803,6 +815,8 @@ vr_result_t vr_reduce_scatter(const void* const* sendbufs, void* const* recvbufs
   const size_t E = elem_size(dtype);
   vr_result_t e = check_buffers(sendbufs, recvbufs, R, (size_t)R * recvcount * E, recvcount * E, kRS, E);
   if (e != VR_SUCCESS || recvcount == 0) return e;
+  log_plan("reduce_scatter", VR_ALGO_RING, R, 1, recvcount, dtype, nChannels, chunkBytes,
+           nullptr, false);
   KArgs a;
   std::memset(&a, 0, sizeof(a));
   a.R = R;
@@ -834,6 +848,8 @@ vr_result_t vr_allgather(const void* const* sendbufs, void* const* recvbufs, int
   vr_result_t e = check_buffers(sendbufs, recvbufs, R, bytes, (size_t)R * bytes, kAG,
                                 elem_size(dtype));
   if (e != VR_SUCCESS || sendcount == 0) return e;
+  log_plan("allgather", VR_ALGO_RING, R, 1, sendcount, dtype, nChannels, chunkBytes, nullptr,
+           false);
   KArgs a;
   std::memset(&a, 0, sizeof(a));
   a.R = R;

@@ -38,6 +38,16 @@ vr_result_t check_stepwise_args(const void* const* sendbufs, void* const* recvbu
                                 size_t count, int dtype, int op, int nChannels,
                                 size_t chunkBytes);
 
+// The option VR_DEBUG=GRAPH (graphlog.cc): tree and ring tables, and a
+// collective call's plan the first time the process sees it (its channel
+// partition when `partitioned`), printed to stderr; no-ops otherwise.
+bool graph_logging();
+void log_trees(const vr_tree_t* trees, int R, int nCh);
+void log_ring(const int* next, int R, int nCh);
+void log_plan(const char* kind, int algo, int R, int L, size_t count, int dtype, int nCh,
+              size_t chunkBytes, const vr_tree_t* trees, bool partitioned);
+
+void build_ring(int R, int nCh, int* next, int* prev);
 void btree(int n, int r, int* up, int* d0, int* d1, int* childType);
 void dtree(int n, int r, int t[2][4]);
 int channel_tree(int c, int nCh);

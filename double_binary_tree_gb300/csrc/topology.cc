@@ -19,6 +19,16 @@
 
 namespace vr {
 
+// The identity ring of every channel: next = r + 1, prev = r - 1 (mod R)
+// ([Interview] "先弄清楚": each rank sends to its right-hand neighbour).
+void build_ring(int R, int nCh, int* next, int* prev) {
+  for (int c = 0; c < nCh; ++c)
+    for (int r = 0; r < R; ++r) {
+      next[c * R + r] = (r + 1) % R;
+      prev[c * R + r] = (r + R - 1) % R;
+    }
+}
+
 // The largest power of two not above x (x >= 1).
 static int bit_floor(int x) {
   int p = 1;

@@ -599,3 +599,48 @@ def test_noalloc_checks_arguments_before_its_size_limit():
         with pytest.raises(vr.VrError) as e:
             vr.vr_allreduce_ring_stepwise_noalloc(*args)
         assert e.value.code == vr.VR_ERR_INVALID_ARGUMENT, args
+
+
+def _graph_log(code):
+    """stderr of a fresh process that runs `code` with VR_DEBUG=GRAPH."""
+    import subprocess
+    import sys
+    env = dict(os.environ, VR_DEBUG="GRAPH")
+    r = subprocess.run([sys.executable, "-c", "import double_binary_tree_gb300 as vr\n" + code],
+                       cwd=ROOT, env=env, check=True, capture_output=True, text=True)
+    return r.stderr.splitlines()
+
+
+def test_graph_log_of_the_topology_builders(golden):
+    """VR_DEBUG=GRAPH: vr_build_dtree(_ex) prints, per channel, the pages' two
+    log formats for every rank, equal line for line to the oracle's
+    formatting of the oracle's trees; vr_build_ring prints each channel's
+    ring order.  Without the option nothing is printed."""
+    lines = _graph_log("vr.vr_build_dtree(2, 4, 3)\nvr.vr_build_ring(5, 2)\n"
+                       "vr.vr_build_dtree(1, 2, 1)\n"
+                       "vr.vr_build_dtree_ex(1, 4, 2, 0, [[0, 2, 1, 3], [1, 0, 3, 2]])\n")
+    want = []
+    for c, tr in enumerate(otopo.build_dtree(2, 4, 3)):
+        want += otopo.format_tree_log(tr, c, "arrow") + otopo.format_tree_log(tr, c, "bracket")
+    nxt, _ = otopo.build_ring(5, 2)
+    for c in range(2):
+        order, v = [], 0
+        for _ in range(5):
+            order.append(v)
+            v = nxt[c][v]
+        want.append("Ring %d : %s" % (c, " ".join(map(str, order))))
+    tr = otopo.build_dtree(1, 2, 1)[0]
+    want += otopo.format_tree_log(tr, 0, "arrow") + otopo.format_tree_log(tr, 0, "bracket")
+    for c, tr in enumerate(otopo.build_dtree(1, 4, 2, orders=[[0, 2, 1, 3], [1, 0, 3, 2]])):
+        want += otopo.format_tree_log(tr, c, "arrow") + otopo.format_tree_log(tr, c, "bracket")
+    assert lines == want
+    # the pages' own line for the 2-rank chain
+    page_line = dict(row.split(None, 1) for row in golden("active_trees.txt"))["log_line"]
+    assert page_line in lines
+    import subprocess
+    import sys
+    quiet = subprocess.run([sys.executable, "-c", "import double_binary_tree_gb300 as vr\n"
+                            "vr.vr_build_dtree(2, 4, 3)\nvr.vr_build_ring(5, 2)\n"], cwd=ROOT,
+                           env={k: v for k, v in os.environ.items() if k != "VR_DEBUG"},
+                           check=True, capture_output=True, text=True)
+    assert quiet.stderr == ""
