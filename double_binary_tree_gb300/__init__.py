@@ -8,13 +8,16 @@ for the legacy default stream.  A non-zero result code raises VrError.
 The compute path is the CUDA library only: the first call loads libvr.so
 and fails loudly (ImportError) when it has not been built for this machine
 (build it with ``python -m double_binary_tree_gb300.build`` or
-``__graft_entry__.build()``).
+``__graft_entry__.build()``).  With VR_BOUNDS_CHECKED=1 in the environment
+it loads the bounds-checked build libvr_debug.so instead (built by
+``build(debug=True)``), in which every kernel access is checked against its
+call's buffers.
 """
 
 import ctypes
 import os
 
-from .build import LIB, is_fresh
+from .build import LIB, LIB_DEBUG, is_fresh
 
 VR_SUCCESS, VR_ERR_INVALID_ARGUMENT, VR_ERR_UNSUPPORTED = 0, 1, 2
 VR_ERR_CUDA, VR_ERR_TIMEOUT, VR_ERR_INTERNAL = 3, 4, 5
@@ -74,6 +77,10 @@ _SIGNATURES = {
     "vr_launch_count": (ctypes.c_ulonglong, []),
     "vr_debug_stall_next": (I, [ctypes.c_longlong]),
     "vr_set_option": (I, [ctypes.c_char_p, ctypes.c_longlong]),
+    "vr_debug_bounds_checked": (I, []),
+    "vr_debug_shrink_next": (I, [ctypes.c_longlong, I]),
+    "vr_debug_bounds_fault": (I, [P(ctypes.c_ulonglong)]),
+    "vr_debug_access_ok": (I, [PP, P(ctypes.c_ulonglong), P(I), I, VP, ctypes.c_ulonglong, I]),
     "vr_get_option": (I, [ctypes.c_char_p, P(ctypes.c_longlong)]),
     "vr_get_error_string": (ctypes.c_char_p, [I]),
     "vr_finalize": (None, []),
@@ -82,13 +89,23 @@ EXPORTED = tuple(_SIGNATURES)
 _lib = None
 
 
+def library_path():
+    """The library this process loads: libvr.so, or libvr_debug.so when
+    VR_BOUNDS_CHECKED=1."""
+    return LIB_DEBUG if os.environ.get("VR_BOUNDS_CHECKED") == "1" else LIB
+
+
 def _load():
-    if not os.path.exists(LIB):
-        raise ImportError("libvr.so is not built: run python -m double_binary_tree_gb300.build")
-    if not is_fresh():
-        raise ImportError("libvr.so is older than its sources or built for another machine: "
-                          "run python -m double_binary_tree_gb300.build")
-    lib = ctypes.CDLL(LIB)
+    path = library_path()
+    debug = path == LIB_DEBUG
+    name = os.path.basename(path)
+    how = "python -m double_binary_tree_gb300.build" + (" --debug" if debug else "")
+    if not os.path.exists(path):
+        raise ImportError("%s is not built: run %s" % (name, how))
+    if not is_fresh(debug):
+        raise ImportError("%s is older than its sources or built for another machine: "
+                          "run %s" % (name, how))
+    lib = ctypes.CDLL(path)
     for name, (res, args) in _SIGNATURES.items():
         fn = getattr(lib, name)
         fn.restype = res
@@ -366,5 +383,24 @@ def vr_finalize():
     _L().vr_finalize()
 
 
-def library_path():
-    return LIB
+def vr_debug_bounds_checked():
+    return bool(_L().vr_debug_bounds_checked())
+
+
+def vr_debug_shrink_next(nbytes, which=3):
+    _check(_L().vr_debug_shrink_next(nbytes, which), "vr_debug_shrink_next")
+
+
+def vr_debug_bounds_fault():
+    v = ctypes.c_ulonglong()
+    _check(_L().vr_debug_bounds_fault(ctypes.byref(v)), "vr_debug_bounds_fault")
+    return v.value
+
+
+def vr_debug_access_ok(extents, p, size, store):
+    """extents: (lo, bytes, writable) triples; returns the C result (1, 0, -1)."""
+    n = len(extents)
+    lo = (VP * max(n, 1))(*[e[0] for e in extents])
+    by = (ctypes.c_ulonglong * max(n, 1))(*[e[1] for e in extents])
+    wr = (I * max(n, 1))(*[int(e[2]) for e in extents])
+    return _L().vr_debug_access_ok(lo, by, wr, n, p, size, int(store))

@@ -80,14 +80,12 @@ __global__ void __launch_bounds__(kBlock) tree_down_kernel(const __grid_constant
     seek<U, kTreeAllReduce>(a, e0, cur);
     const int root = s_prog[cur.t].root;
     if (n == NV) {
-      const typename Unit<T, NV>::Raw v =
-          *reinterpret_cast<const typename Unit<T, NV>::Raw*>(s_dst[root] + e0 * E);
+      const typename Unit<T, NV>::Raw v = ld_plain<typename Unit<T, NV>::Raw>(s_dst[root] + e0 * E);
       for (int r = 0; r < R; ++r)
         if (r != root) Unit<T, NV>::store(s_dst[r] + e0 * E, v);
     } else {
       for (int i = 0; i < n; ++i) {
-        const typename Ty<T>::Bits v =
-            *reinterpret_cast<const typename Ty<T>::Bits*>(s_dst[root] + (e0 + i) * E);
+        const typename Ty<T>::Bits v = ld_plain<typename Ty<T>::Bits>(s_dst[root] + (e0 + i) * E);
         for (int r = 0; r < R; ++r)
           if (r != root) Unit<T, 1>::store(s_dst[r] + (e0 + i) * E, v);
       }
@@ -138,13 +136,13 @@ __global__ void __launch_bounds__(kBlock)
       char* m = fifo + e0 * E;
       typedef typename Unit<T, NV>::Raw Raw;  // 16 bytes, or one element
       if (phase == kStepSend) {
-        Unit<T, NV>::store(m, *reinterpret_cast<const Raw*>(s_dst[from] + e0 * E));
+        Unit<T, NV>::store(m, ld_plain<Raw>(s_dst[from] + e0 * E));
       } else if (phase == kStepCopy) {
-        Unit<T, NV>::store(s_dst[to] + e0 * E, *reinterpret_cast<const Raw*>(m));
+        Unit<T, NV>::store(s_dst[to] + e0 * E, ld_plain<Raw>(m));
       } else {
         typename Ln::L x[Ln::N], y[Ln::N];
-        Ln::decode(*reinterpret_cast<const typename Unit<T, NV>::Raw*>(s_dst[to] + e0 * E), x);
-        Ln::decode(*reinterpret_cast<const typename Unit<T, NV>::Raw*>(m), y);
+        Ln::decode(ld_plain<Raw>(s_dst[to] + e0 * E), x);
+        Ln::decode(ld_plain<Raw>(m), y);
 #pragma unroll
         for (int e = 0; e < Ln::N; ++e) x[e] = Ln::op(x[e], y[e]);
         Unit<T, NV>::store(s_dst[to] + e0 * E, Ln::encode(x));
@@ -156,17 +154,17 @@ __global__ void __launch_bounds__(kBlock)
         int from, to;
         step_ranks(R, routing, step, cur.j, from, to);
         typedef typename Ty<T>::Bits Bits;
-        Bits* m = reinterpret_cast<Bits*>(fifo + e * E);
+        char* m = fifo + e * E;
         if (phase == kStepSend) {
-          *m = *reinterpret_cast<const Bits*>(s_dst[from] + e * E);
+          st_plain<Bits>(m, ld_plain<Bits>(s_dst[from] + e * E));
         } else if (phase == kStepCopy) {
-          *reinterpret_cast<Bits*>(s_dst[to] + e * E) = *m;
+          st_plain<Bits>(s_dst[to] + e * E, ld_plain<Bits>(m));
         } else {
           typename L1::L x[1], y[1];
-          L1::decode(*reinterpret_cast<const Bits*>(s_dst[to] + e * E), x);
-          L1::decode(*m, y);
+          L1::decode(ld_plain<Bits>(s_dst[to] + e * E), x);
+          L1::decode(ld_plain<Bits>(m), y);
           x[0] = L1::op(x[0], y[0]);
-          *reinterpret_cast<Bits*>(s_dst[to] + e * E) = L1::encode(x);
+          st_plain<Bits>(s_dst[to] + e * E, L1::encode(x));
         }
       }
     }
@@ -194,7 +192,7 @@ __global__ void __launch_bounds__(kBlock) copy_ranks_kernel(const __grid_constan
     if constexpr (VEC) {
       st_global_v4(s_dst[r] + off, ld_global_v4(s_src[r] + off));
     } else {
-      s_dst[r][off] = s_src[r][off];
+      st_plain<char>(s_dst[r] + off, ld_plain<char>(s_src[r] + off));
     }
   }
 }

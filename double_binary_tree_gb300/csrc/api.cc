@@ -26,12 +26,31 @@ struct DeviceInfo {
   int sms = 0;
   int smemOptin = 0;  // largest dynamic shared memory a CTA may opt into
   unsigned* status = nullptr;
+  unsigned long long* boundsWhere = nullptr;  // first refused address (bounds-checked build)
 };
 std::map<int, DeviceInfo> g_devices;                             // by device ordinal
 std::map<std::pair<const void*, int>, int> g_occupancy;          // (kernel, device)
 std::map<std::pair<int, int>, std::array<FoldProg, 2>> g_progs;  // (nNodes, localRanks)
 std::map<std::pair<const void*, int>, int> g_smemSet;            // (kernel, device) -> bytes
+std::map<std::pair<const void*, int>, int> g_staticSmem;         // (kernel, device) -> bytes
 std::atomic<long long> g_stallNext{-1};                          // test hook
+std::atomic<long long> g_shrinkNext{0};                          // test hook (bounds-checked build)
+std::atomic<int> g_shrinkWhich{0};
+
+// Test hook of the bounds-checked build: the next launch's recorded buffer
+// extents (send 1, receive 2, FIFO 4 in `which`) end `n` bytes early -- the
+// buffers themselves are untouched, so its last accesses are refused without
+// any access outside real memory.
+void shrink_extents(KArgs& a) {
+  const long long n = g_shrinkNext.exchange(0);
+  const int which = g_shrinkWhich.load();
+  if (n <= 0) return;
+  const unsigned long long k = (unsigned long long)n;
+  auto cut = [k](unsigned long long x) { return x > k ? x - k : 0ull; };
+  if (which & 1) a.srcBytes = cut(a.srcBytes);
+  if (which & 2) a.dstBytes = cut(a.dstBytes);
+  if (which & 4) a.scratchBytes = cut(a.scratchBytes);
+}
 
 unsigned long long wait_timeout_ns() {
   static const unsigned long long ns = [] {
@@ -65,7 +84,9 @@ vr_result_t device_info(DeviceInfo* out, int* device) {
         cudaDeviceGetAttribute(&d.smemOptin, cudaDevAttrMaxSharedMemoryPerBlockOptin, *device) !=
             cudaSuccess)
       return VR_ERR_CUDA;
-    if (status_word_address(&d.status) != cudaSuccess) return VR_ERR_CUDA;
+    if (status_word_address(&d.status) != cudaSuccess ||
+        bounds_word_address(&d.boundsWhere) != cudaSuccess)
+      return VR_ERR_CUDA;
     it = g_devices.emplace(*device, d).first;
   }
   *out = it->second;
@@ -253,6 +274,8 @@ vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream,
   if ((e = check_reachable(const_cast<const void* const*>(a.dst), a.R, device)) != VR_SUCCESS)
     return e;
   a.status = di.status;
+  a.boundsWhere = di.boundsWhere;
+  shrink_extents(a);
   const long long resident = (long long)di.sms * blocks_per_sm(fn, device);
   const long long wanted = (units + kBlockThreads - 1) / kBlockThreads;
   // Fewer units than 256-thread CTAs to cover every SM: smaller CTAs (a
@@ -322,9 +345,24 @@ vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
   if ((e = check_reachable(const_cast<const void* const*>(a.dst), a.R, device)) != VR_SUCCESS)
     return e;
   a.status = di.status;
+  a.boundsWhere = di.boundsWhere;
+  shrink_extents(a);
   // Largest per-rank tile (fewer, larger bulk copies) that still leaves
   // at least kMinStages stages in the opt-in shared memory.
-  const int room = di.smemOptin - kStagedHeader;
+  // (the bounds-checked build adds a table in static shared memory)
+  int staticSmem = 0;
+  {
+    std::lock_guard<std::mutex> g(g_mu);
+    auto key = std::make_pair(fn, device);
+    auto it = g_staticSmem.find(key);
+    if (it == g_staticSmem.end()) {
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return VR_ERR_CUDA;
+      it = g_staticSmem.emplace(key, (int)fa.sharedSizeBytes).first;
+    }
+    staticSmem = it->second;
+  }
+  const int room = di.smemOptin - staticSmem - kStagedHeader;
   unsigned tb = (unsigned)option(kOptStagedTileBytes);
   // Above 32 ranks two stages with larger tiles (more consumer warps) beat
   // three smaller ones: measured 2.5% (tree) to 20% (ring) faster at 64.
@@ -352,10 +390,10 @@ vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
     std::lock_guard<std::mutex> g(g_mu);
     int& set = g_smemSet[std::make_pair(fn, device)];
     if (set < (int)smem) {
-      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smemOptin) !=
-          cudaSuccess)
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               di.smemOptin - staticSmem) != cudaSuccess)
         return VR_ERR_CUDA;
-      set = di.smemOptin;
+      set = di.smemOptin - staticSmem;
     }
   }
   a.timeoutNs = wait_timeout_ns();
@@ -603,6 +641,7 @@ vr_result_t plan_allreduce(const void* const* sendbufs, void* const* recvbufs, i
   std::memset(&a, 0, sizeof(a));
   a.R = R;
   for (int r = 0; r < R; ++r) { a.src[r] = sendbufs[r]; a.dst[r] = recvbufs[r]; }
+  a.srcBytes = a.dstBytes = count * E;
   fill_partition(a, count, E, nChannels, chunkBytes);
   mode = kRingAllReduce;
   stack = 0;
@@ -779,6 +818,7 @@ vr_result_t vr_allreduce_trees(const void* const* sendbufs, void* const* recvbuf
   std::memset(&a, 0, sizeof(a));
   a.R = R;
   for (int r = 0; r < R; ++r) { a.src[r] = sendbufs[r]; a.dst[r] = recvbufs[r]; }
+  a.srcBytes = a.dstBytes = count * E;
   fill_partition(a, count, E, nChannels, chunkBytes);
   // one program per distinct tree
   int stack = 0;
@@ -824,6 +864,8 @@ vr_result_t vr_reduce_scatter(const void* const* sendbufs, void* const* recvbufs
   a.count = (long long)recvcount;
   a.nCh = nChannels;
   a.chunk = (long long)(chunkBytes / E);
+  a.srcBytes = (size_t)R * recvcount * E;
+  a.dstBytes = recvcount * E;
   const bool vec = aligned16(sendbufs, R, recvcount * E) && aligned16(recvbufs, R, 0);
   const int forced = forced_path();
   if (vec && forced != 1 && (forced == 2 || use_staged_rs(R, dtype, recvcount * E * R))) {
@@ -856,6 +898,8 @@ vr_result_t vr_allgather(const void* const* sendbufs, void* const* recvbufs, int
   for (int r = 0; r < R; ++r) { a.src[r] = sendbufs[r]; a.dst[r] = recvbufs[r]; }
   a.count = (long long)bytes;
   a.nCh = nChannels;
+  a.srcBytes = bytes;
+  a.dstBytes = (size_t)R * bytes;
   const bool vec = aligned16(sendbufs, R, bytes) && aligned16(recvbufs, R, 0);
   if (vec && forced_path() != 1) {
     // the TMA copy: one warp per CTA, tiles of gather_tile_bytes() of one rank
@@ -881,6 +925,8 @@ vr_result_t vr_allgather(const void* const* sendbufs, void* const* recvbufs, int
     }
     a.tiles = (long long)R * (((long long)bytes + tile - 1) / tile);
     a.status = di.status;
+    a.boundsWhere = di.boundsWhere;
+    shrink_extents(a);
     a.timeoutNs = wait_timeout_ns();
     a.injectStall = g_stallNext.exchange(-1);
     const long long grid = std::min<long long>(a.tiles, (long long)di.sms * ctas);
@@ -920,6 +966,8 @@ vr_result_t vr_allreduce_ring_stepwise(const void* const* sendbufs, void* const*
   a.R = R;
   for (int r = 0; r < R; ++r) { a.src[r] = sendbufs[r]; a.dst[r] = recvbufs[r]; }
   a.scratch = scratch;
+  a.srcBytes = a.dstBytes = count * E;
+  a.scratchBytes = need;
   const bool vec = aligned16(sendbufs, R, 0) && aligned16(recvbufs, R, 0) &&
                    (((uintptr_t)scratch & 15) == 0);
   // working copies: recv = send
@@ -958,6 +1006,7 @@ vr_result_t vr_allreduce_tree_updown(const void* const* sendbufs, void* const* r
   std::memset(&a, 0, sizeof(a));
   a.R = R;
   for (int r = 0; r < R; ++r) { a.src[r] = sendbufs[r]; a.dst[r] = recvbufs[r]; }
+  a.srcBytes = a.dstBytes = count * E;
   fill_partition(a, count, E, nChannels, chunkBytes);
   std::array<FoldProg, 2> p;
   if ((e = tree_programs(R / localRanks, localRanks, &p)) != VR_SUCCESS) return e;
@@ -980,6 +1029,13 @@ vr_result_t vr_stream_status(void* stream) {
 }
 
 unsigned long long vr_launch_count(void) { return g_launches.load(); }
+
+vr_result_t vr_debug_shrink_next(long long bytes, int which) {
+  if (bytes < 0 || which < 0 || which > 7) return VR_ERR_INVALID_ARGUMENT;
+  g_shrinkWhich.store(which);
+  g_shrinkNext.store(bytes);
+  return VR_SUCCESS;
+}
 
 vr_result_t vr_debug_stall_next(long long tile) {
   if (tile < -1) return VR_ERR_INVALID_ARGUMENT;
@@ -1042,6 +1098,7 @@ void vr_finalize(void) {
   g_occupancy.clear();
   g_devices.clear();
   g_smemSet.clear();
+  g_staticSmem.clear();
 }
 
 }  // extern "C"

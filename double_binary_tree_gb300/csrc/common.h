@@ -7,6 +7,7 @@ typedef unsigned short uint16_t;
 typedef unsigned int uint32_t;
 typedef unsigned long long uint64_t;
 typedef long long int64_t;
+typedef unsigned long long uintptr_t;
 #else
 #include <stdint.h>
 #endif
@@ -67,6 +68,11 @@ struct KArgs {
   int pad;
   unsigned* status;     // this device's status word
   void* scratch;        // stepwise ring: the message FIFO (count elements)
+  // The call's buffers for the bounds-checked build (bounds.cuh): bytes of
+  // every send buffer, of every receive buffer and of the scratch FIFO, and
+  // the device word that records the first access outside them.
+  unsigned long long srcBytes, dstBytes, scratchBytes;
+  unsigned long long* boundsWhere;
   // TMA-staged kernels (staged.cuh)
   long long unitLo;     // AllReduce: first 16-byte unit of the range
   long long unitsAll;   // AllReduce: end unit of the range, a trailing partial one included
@@ -83,5 +89,8 @@ struct KArgs {
   uint8_t chanProg[kMaxChannels];  // channel c folds with prog[chanProg[c]]
   FoldProg prog[kMaxProgs];
 };
+
+// CUDA's classic limit on a kernel's parameter block.
+static_assert(sizeof(KArgs) <= 4096, "kernel arguments exceed 4 KB");
 
 }  // namespace vr

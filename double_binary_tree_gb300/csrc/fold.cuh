@@ -23,6 +23,7 @@
 #include <stdint.h>
 #endif
 
+#include "bounds.cuh"
 #include "common.h"
 
 namespace vr {
@@ -70,17 +71,36 @@ template <> struct Ty<__nv_bfloat16> {
 };
 
 // ---------------------------------------------------------- memory access
+// Every global access below goes through these helpers (or a bulk copy),
+// each checked in the bounds-checked build (bounds.cuh): a refused load
+// reads zeros, a refused store is dropped.
 __device__ __forceinline__ uint4 ld_global_v4(const void* p) {
   uint4 v;
+  if (!VR_ACCESS_OK(p, 16, false)) return make_uint4(0, 0, 0, 0);
   asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
       : "l"(p));
   return v;
 }
 __device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
+  if (!VR_ACCESS_OK(p, 16, true)) return;
   asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
+}
+// Plain (coherent) load and store of one value of type V.
+template <typename V> __device__ __forceinline__ V ld_plain(const void* p) {
+  if (!VR_ACCESS_OK(p, sizeof(V), false)) return V();
+  return *reinterpret_cast<const V*>(p);
+}
+// Read-only (non-coherent cache) load of one value of type V.
+template <typename V> __device__ __forceinline__ V ld_ro(const void* p) {
+  if (!VR_ACCESS_OK(p, sizeof(V), false)) return V();
+  return __ldg(reinterpret_cast<const V*>(p));
+}
+template <typename V> __device__ __forceinline__ void st_plain(void* p, V v) {
+  if (!VR_ACCESS_OK(p, sizeof(V), true)) return;
+  *reinterpret_cast<V*>(p) = v;
 }
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -92,7 +112,7 @@ template <typename T, int NV> struct Unit {
   typedef typename Select<NV == 1, Bits, uint4>::type Raw;
 
   static __device__ __forceinline__ void store(char* p, Raw v) {
-    if constexpr (NV == 1) *reinterpret_cast<Bits*>(p) = v;
+    if constexpr (NV == 1) st_plain<Bits>(p, v);
     else st_global_v4(p, v);
   }
   static __device__ __forceinline__ void unpack(Raw v, float (&x)[NV]) {
@@ -139,8 +159,12 @@ struct SharedSrc {              // base + r * stride, shared memory
 template <typename T, int NV>
 __device__ __forceinline__ typename Unit<T, NV>::Raw load_unit(const GlobalSrc& s, int r) {
   const char* p = s.ptr[r] + s.off;
-  if constexpr (NV == 1) return __ldg(reinterpret_cast<const typename Ty<T>::Bits*>(p));
-  else return ld_global_v4(p);
+  if constexpr (NV == 1) {
+    if (!VR_ACCESS_OK(p, sizeof(typename Ty<T>::Bits), false)) return 0;
+    return __ldg(reinterpret_cast<const typename Ty<T>::Bits*>(p));
+  } else {
+    return ld_global_v4(p);
+  }
 }
 template <typename T, int NV>
 __device__ __forceinline__ typename Unit<T, NV>::Raw load_unit(const SharedSrc& s, int r) {

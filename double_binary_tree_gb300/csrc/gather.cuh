@@ -27,6 +27,7 @@ constexpr unsigned kGatherTile = 8192;
 constexpr int kGatherCtasPerSm = 2;
 
 __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, unsigned bytes) {
+  if (!VR_ACCESS_OK(dst, bytes, true)) return;
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
                "r"(bytes)
                : "memory");
@@ -59,6 +60,7 @@ __global__ void __launch_bounds__(kWarpSize) allgather_tma_kernel(const __grid_c
     s_src[i] = static_cast<const char*>(a.src[i]);
     s_dst[i] = static_cast<char*>(a.dst[i]);
   }
+  VR_BOUNDS_SETUP(a);
   if (lane == 0) {
     abort_flag = 0;
     for (int s = 0; s < NS; ++s) mbar_init(smem_addr(&full[s]), 1);

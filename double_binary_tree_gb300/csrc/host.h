@@ -100,5 +100,9 @@ const void* ablation_kernel_ptr(int which, int dtype, int op, bool vec, int stac
 // The current device's status word: its address, and read-and-clear.
 cudaError_t status_word_address(unsigned** p);
 cudaError_t read_and_clear_status(unsigned* value);
+// The word where the bounds-checked build records the first refused
+// address: its address, and read-and-clear.
+cudaError_t bounds_word_address(unsigned long long** p);
+cudaError_t read_and_clear_bounds(unsigned long long* value);
 
 }  // namespace vr

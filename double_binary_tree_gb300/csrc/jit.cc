@@ -258,6 +258,9 @@ bool compile(int arch, int dtype, int op, int mode, int stack, bool small, int k
   if (mode == kTreeAllReduce ? !generate(progs, nProgs, &src) : !generate_ring(R, &src))
     return false;
   if (minBlocks > 0) src = "#define VR_JIT_MIN_BLOCKS " + std::to_string(minBlocks) + "\n" + src;
+#ifdef VR_DEBUG_BOUNDS
+  src = "#define VR_DEBUG_BOUNDS 1\n" + src;  // the bounds-checked build's kernels check too
+#endif
   const int S = stack <= 4 ? 4 : 8;
   const std::string M = std::to_string(mode);
   const std::string expr =

@@ -55,6 +55,7 @@ __device__ __forceinline__ void stage_args(const KArgs& a, const char** s_src, c
     const int words = a.nProgs * (int)(sizeof(FoldProg) / 4);
     for (int i = threadIdx.x; i < words; i += blockDim.x) to[i] = from[i];
   }
+  VR_BOUNDS_SETUP(a);
   __syncthreads();
   pdl_wait();
 }
@@ -176,10 +177,10 @@ __global__ void __launch_bounds__(kBlock) allgather_kernel(const __grid_constant
         if (to != from) st_global_v4(to, v);
       }
     } else {
-      const unsigned char v = __ldg(reinterpret_cast<const unsigned char*>(from));
+      const unsigned char v = ld_ro<unsigned char>(from);
       for (int q = 0; q < R; ++q) {
         char* to = s_dst[q] + (long long)r * bytes + off;
-        if (to != from) *reinterpret_cast<unsigned char*>(to) = v;
+        if (to != from) st_plain<unsigned char>(to, v);
       }
     }
   }

@@ -8,6 +8,9 @@ namespace vr {
 // First device-side error recorded by any kernel of this library on this
 // device since it was last read (0 = none).
 __device__ unsigned g_status_word = 0;
+// First address the bounds-checked build refused on this device since it
+// was last read (0 = none).
+__device__ unsigned long long g_bounds_word = 0;
 
 const void* kernel_ptr_allgather(bool vec) {
   return vec ? (const void*)allgather_kernel<true> : (const void*)allgather_kernel<false>;
@@ -36,4 +39,45 @@ cudaError_t status_word_address(unsigned** p) {
   return cudaGetSymbolAddress(reinterpret_cast<void**>(p), g_status_word);
 }
 
+cudaError_t bounds_word_address(unsigned long long** p) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(p), g_bounds_word);
+}
+
+cudaError_t read_and_clear_bounds(unsigned long long* value) {
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_bounds_word, sizeof(*value));
+  if (e != cudaSuccess) return e;
+  const unsigned long long zero = 0;
+  return cudaMemcpyToSymbol(g_bounds_word, &zero, sizeof(zero));
+}
+
 }  // namespace vr
+
+using namespace vr;
+
+extern "C" {
+
+int vr_debug_bounds_checked(void) {
+#ifdef VR_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+vr_result_t vr_debug_bounds_fault(unsigned long long* address) {
+  if (!address) return VR_ERR_INVALID_ARGUMENT;
+  if (read_and_clear_bounds(address) != cudaSuccess) return VR_ERR_CUDA;
+  return VR_SUCCESS;
+}
+
+int vr_debug_access_ok(const void* const* lo, const unsigned long long* bytes,
+                       const int* writable, int n, const void* p, unsigned long long size,
+                       int store) {
+  if (n < 0 || n > 2 * kMaxRanks + 1 || (n > 0 && (!lo || !bytes || !writable))) return -1;
+  Extent ext[2 * kMaxRanks + 1];
+  for (int i = 0; i < n; ++i)
+    ext[i] = Extent{static_cast<const char*>(lo[i]), bytes[i], writable[i]};
+  return access_in(ext, n, static_cast<const char*>(p), size, store != 0) ? 1 : 0;
+}
+
+}  // extern "C"

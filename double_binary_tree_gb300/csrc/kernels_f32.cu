@@ -6,7 +6,6 @@
 
 namespace vr {
 
-// Register-path kernels: `vec` = 16-byte units, else element units.
 // Register-path kernels: `vec` = 16-byte units, else element units;
 // `small`: the variant for at most 4 ranks.
 const void* kernel_ptr_f32(int mode, int op, bool vec, int stack, bool small) {

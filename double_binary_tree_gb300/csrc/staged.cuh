@@ -52,8 +52,18 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, unsigned parity) {
       : "memory");
   return ok != 0;
 }
+// Completes `bytes` of the barrier's expected transaction count without a
+// copy (a bulk load the bounds-checked build refused).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, unsigned bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, unsigned bytes,
                                           uint32_t bar) {
+  if (!VR_ACCESS_OK(src, bytes, false)) {
+    mbar_complete_tx(bar, bytes);
+    return;
+  }
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           dst),
@@ -154,6 +164,7 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
     const int words = a.nProgs * (int)(sizeof(FoldProg) / 4);
     for (int i = threadIdx.x; i < words; i += blockDim.x) to[i] = from[i];
   }
+  VR_BOUNDS_SETUP(a);
   if (threadIdx.x == 0) {
     *abort = 0;
     for (int s = 0; s < NS; ++s) {

@@ -506,6 +506,48 @@ vr_result_t vr_set_option(const char* name, long long value);
  * Errors: VR_ERR_INVALID_ARGUMENT for an unknown name or NULL value. */
 vr_result_t vr_get_option(const char* name, long long* value);
 
+/* ------------------------------------------------ bounds-checked build
+ * The library's calls return at enqueue, so a kernel's fault would surface
+ * later and asynchronously ([Internals] "API 返回只意味着提交边界").  The
+ * bounds-checked build of this library (libvr_debug.so, built by
+ * double_binary_tree_gb300.build with debug=True; loaded by the Python
+ * binding when VR_BOUNDS_CHECKED=1) compiles every global-memory access of
+ * every kernel with a check against the buffers of its call: the send and
+ * receive buffers (count elements, or the collective's sizes) and the
+ * stepwise ring's FIFO.  An access outside them (a store outside the
+ * receive buffers and the FIFO) is skipped, VR_ERR_INTERNAL is recorded in
+ * the status word (vr_stream_status) and the first such address in a second
+ * device word.  Results and performance of the normal build are unchanged:
+ * there the checks compile to nothing. */
+
+/* 1 in the bounds-checked build, 0 in the normal one. */
+int vr_debug_bounds_checked(void);
+
+/* The first address the bounds-checked build refused on the current device
+ * since the last call (0: none), then cleared.  Errors: VR_ERR_INVALID_ARGUMENT
+ * for NULL address, VR_ERR_CUDA when the device cannot be read. */
+vr_result_t vr_debug_bounds_fault(unsigned long long* address);
+
+/* Test hook of the bounds-checked build: the next kernel launch records some
+ * of its buffers as ending `bytes` earlier than they do (`which`: 1 the
+ * send buffers, 2 the receive buffers, 4 the FIFO, or a sum), so the checks
+ * refuse its last accesses to them while every access still lies inside
+ * real memory: refused loads read zeros (a refused bulk copy into shared
+ * memory completes its barrier without copying), refused stores are not
+ * made, and vr_stream_status reports VR_ERR_INTERNAL.  No effect in the
+ * normal build.  bytes == 0 cancels a pending request.
+ * Errors: VR_ERR_INVALID_ARGUMENT for bytes < 0 or which outside 0..7. */
+vr_result_t vr_debug_shrink_next(long long bytes, int which);
+
+/* The bounds predicate of the device checks, run on the host (for tests):
+ * 1 when [p, p + size) lies inside one of the n extents [lo[i], lo[i] +
+ * bytes[i]) -- a writable one (writable[i] != 0) when store != 0 -- else 0;
+ * -1 for bad arguments (n < 0, n > 129, NULL arrays with n > 0).  NULL
+ * extents never match.  Touches no memory at p. */
+int vr_debug_access_ok(const void* const* lo, const unsigned long long* bytes,
+                       const int* writable, int n, const void* p, unsigned long long size,
+                       int store);
+
 /* Static English text for a result code ("unknown result" for others). */
 const char* vr_get_error_string(vr_result_t result);
 

@@ -29,7 +29,7 @@ def golden():
 def _ensure_library():
     """Build libvr.so for this machine before any test imports the binding."""
     from double_binary_tree_gb300 import build as _b
-    _b.build()
+    _b.build(debug=True)
 
 
 _ensure_library()

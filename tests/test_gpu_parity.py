@@ -73,6 +73,15 @@ def to_device(inputs, shift=0):
     return out
 
 
+@pytest.fixture(autouse=True)
+def no_refused_access():
+    """Under the bounds-checked build, no test's calls touched memory outside
+    their buffers."""
+    yield
+    if vr.vr_debug_bounds_checked():
+        assert vr.vr_debug_bounds_fault() == 0
+
+
 def bits(t):
     return workloads.raw_numpy(t.cpu())
 

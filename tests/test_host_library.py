@@ -644,3 +644,70 @@ def test_graph_log_of_the_topology_builders(golden):
                            env={k: v for k, v in os.environ.items() if k != "VR_DEBUG"},
                            check=True, capture_output=True, text=True)
     assert quiet.stderr == ""
+
+
+def test_bounds_predicate_edges():
+    """The bounds-checked build's predicate, run on the host: an access is
+    allowed when it lies wholly inside one extent (a writable one for a
+    store)."""
+    A, B = 1 << 40, 1 << 41
+    ext = [(A, 4096, 0), (B, 64, 1)]
+    ok = vr.vr_debug_access_ok
+    assert ok(ext, A, 16, False) == 1
+    assert ok(ext, A + 4080, 16, False) == 1          # the last unit
+    assert ok(ext, A + 4081, 16, False) == 0          # straddles the end
+    assert ok(ext, A + 4096, 1, False) == 0           # one past the end
+    assert ok(ext, A - 1, 1, False) == 0              # one before
+    assert ok(ext, A + 4096, 0, False) == 1           # empty access at the end
+    assert ok(ext, A, 16, True) == 0                  # send buffers are read-only
+    assert ok(ext, B + 48, 16, True) == 1
+    assert ok(ext, B + 48, 17, True) == 0
+    assert ok(ext, A, 1 << 63, False) == 0            # no wrap-around
+    assert ok([(None, 1 << 62, 1)], 0, 16, True) == 0  # a missing buffer matches nothing
+    assert ok([], A, 1, False) == 0
+    assert ok([(A, 1, 1)] * 130, A, 1, False) == -1   # more extents than a call has
+
+
+def test_bounds_predicate_matches_brute_force():
+    rng = np.random.default_rng(12)
+    hits = 0
+    for _ in range(300):
+        n = int(rng.integers(1, 9))
+        ext = [(int(rng.integers(1, 1 << 20)) * 16, int(rng.integers(0, 4096)),
+                int(rng.integers(0, 2))) for _ in range(n)]
+        a, b, _ = ext[int(rng.integers(0, n))]        # near one of the extents
+        p = a + int(rng.integers(-32, b + 33))
+        size = int(rng.choice([0, 1, 2, 4, 16, 4096]))
+        store = bool(rng.integers(0, 2))
+        want = any(p >= a and p + size <= a + b and (w or not store) for a, b, w in ext)
+        assert vr.vr_debug_access_ok(ext, p, size, store) == int(want)
+        hits += want
+    assert 60 < hits < 240                             # both outcomes well represented
+
+
+def test_bounds_checked_build_is_loaded_on_request():
+    import subprocess
+    import sys
+    code = "import double_binary_tree_gb300 as vr; print(vr.vr_debug_bounds_checked())"
+    for flag, want in (("1", "True"), ("0", "False")):
+        env = dict(os.environ, VR_BOUNDS_CHECKED=flag)
+        out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, check=True,
+                             capture_output=True, text=True).stdout.strip()
+        assert out == want
+
+
+def test_bounds_checked_specialised_kernels_compile():
+    """In the bounds-checked build the folds specialised at run time are
+    compiled with the checks too (NVRTC, no device)."""
+    import subprocess
+    import sys
+    if not vr.vr_jit_status()[0]:
+        pytest.skip("NVRTC or the kernel sources not found")
+    code = ("import double_binary_tree_gb300 as vr\n"
+            "assert vr.vr_debug_bounds_checked()\n"
+            "print(vr.vr_jit_compile_dtree(2, 4, vr.VR_BFLOAT16, vr.VR_SUM, 103) > 0,\n"
+            "      vr.vr_jit_compile_ring(4, vr.VR_FLOAT32, vr.VR_MAX, 103) > 0)\n")
+    env = dict(os.environ, VR_BOUNDS_CHECKED="1")
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, check=True,
+                         capture_output=True, text=True).stdout.strip()
+    assert out == "True True"

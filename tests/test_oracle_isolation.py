@@ -100,6 +100,6 @@ def test_stale_library_raises(monkeypatch):
     """A library older than its sources (or built elsewhere) is not loaded."""
     import double_binary_tree_gb300 as vr
     monkeypatch.setattr(vr, "_lib", None)
-    monkeypatch.setattr(vr, "is_fresh", lambda: False)
+    monkeypatch.setattr(vr, "is_fresh", lambda debug=False: False)
     with pytest.raises(ImportError, match="older than its sources"):
         vr.vr_build_ring(4, 2)
