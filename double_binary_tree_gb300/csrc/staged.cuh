@@ -96,8 +96,12 @@ __device__ __forceinline__ void raise_error(unsigned* status, volatile int* abor
   *abort = 1;
 }
 
-// Tile t of the message: the byte offset of its slice inside each source
+// Tile i of a CTA's work: the byte offset of its slice inside each source
 // rank's buffer, the bytes the producer copies, and the units it covers.
+// AllReduce: every CTA owns an equal run [cub, cue) of the message's units
+// (to one unit) and cuts it into tiles of tileUnits, the last one shorter,
+// so no CTA waits on a whole extra tile at the end.  ReduceScatter: tile t
+// (= tb + i) of the whole call, tiles not crossing a block.
 struct TileGeom {
   long long srcOff;   // bytes from each source buffer's start
   unsigned bytes;     // bytes copied per rank (full 16-byte units only)
@@ -107,7 +111,8 @@ struct TileGeom {
 };
 
 template <int MODE>
-__device__ __forceinline__ TileGeom tile_geom(const KArgs& a, long long t) {
+__device__ __forceinline__ TileGeom tile_geom(const KArgs& a, long long t, long long cub,
+                                              long long cue) {
   const int TU = a.tileUnits;
   TileGeom g;
   if constexpr (MODE == kReduceScatter) {
@@ -121,9 +126,9 @@ __device__ __forceinline__ TileGeom tile_geom(const KArgs& a, long long t) {
     g.srcOff = (long long)g.b * perB * 16 + g.u0 * 16;
   } else {
     g.b = 0;
-    g.u0 = a.unitLo + t * TU;
-    g.units = (int)min((long long)TU, a.unitsAll - g.u0);
-    const long long full = min((long long)TU, max(0LL, a.unitsFull - g.u0));
+    g.u0 = cub + t * TU;
+    g.units = (int)min((long long)TU, cue - g.u0);
+    const long long full = min((long long)g.units, max(0LL, a.unitsFull - g.u0));
     g.bytes = (unsigned)full * 16u;
     g.srcOff = g.u0 * 16;
   }
@@ -177,9 +182,18 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
   __syncthreads();
   pdl_wait();  // the previous kernel on the stream is done
 
-  const long long tb = udiv(a.tiles * blockIdx.x, gridDim.x);
-  const long long te = udiv(a.tiles * (blockIdx.x + 1), gridDim.x);
-  const long long n = te - tb;
+  // this CTA's work: tiles [tb, tb + n) of the call (ReduceScatter), or the
+  // units [cub, cue) cut into n tiles (AllReduce)
+  long long tb = 0, n = 0, cub = 0, cue = 0;
+  if constexpr (MODE == kReduceScatter) {
+    tb = udiv(a.tiles * blockIdx.x, gridDim.x);
+    n = udiv(a.tiles * (blockIdx.x + 1), gridDim.x) - tb;
+  } else {
+    const long long total = a.unitsAll - a.unitLo;
+    cub = a.unitLo + udiv(total * blockIdx.x, gridDim.x);
+    cue = a.unitLo + udiv(total * (blockIdx.x + 1), gridDim.x);
+    n = (cue - cub + a.tileUnits - 1) / a.tileUnits;
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -197,7 +211,7 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
         }
       }
       if (__shfl_sync(~0u, *abort, 0)) break;
-      const TileGeom g = tile_geom<MODE>(a, tb + i);
+      const TileGeom g = tile_geom<MODE>(a, tb + i, cub, cue);
       if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * s, (unsigned)R * g.bytes);
       __syncwarp();
       issued = i + 1;
@@ -233,7 +247,7 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
       if (lane == 0 && !*abort) raise_error(a.status, abort, VR_ERR_TIMEOUT);
       break;
     }
-    const TileGeom g = tile_geom<MODE>(a, tb + i);
+    const TileGeom g = tile_geom<MODE>(a, tb + i, cub, cue);
     const unsigned char* base = stage0 + (size_t)s * stageBytes;
     for (int lu = ct; lu < g.units; lu += nct) {
       if constexpr (MODE == kReduceScatter) {
