@@ -85,8 +85,13 @@ __global__ void __launch_bounds__(kBlock, kMinBlocksJit ? kMinBlocksJit
   const long long units = (count + NV - 1) / NV - u0;
   const long long ub = u0 + udiv(units * blockIdx.x, gridDim.x);
   const long long ue = u0 + udiv(units * (blockIdx.x + 1), gridDim.x);
+  // The trailing partial unit of a vector call (count % NV elements) is not
+  // one thread's work: its elements go to the first threads of the CTA that
+  // owns it, below, so their loads are not waited for in turn.
+  const long long tailU = VEC && count % NV ? count / NV : -1;
   Cursor cur{0, -1, 0, 0, 0, 0, 0};
   for (long long u = ub + threadIdx.x; u < ue; u += blockDim.x) {
+    if (u == tailU) continue;
     const long long e0 = u * NV;
     const int n = (int)min((long long)NV, count - e0);
     seek<U, MODE>(a, e0, cur);
@@ -105,7 +110,8 @@ __global__ void __launch_bounds__(kBlock, kMinBlocksJit ? kMinBlocksJit
       const uint4 o = ring_fold_split_rare<T, OP>(src, R, cur.j, (int)(cur.hi - e0));
       for (int r = 0; r < R; ++r) st_global_v4(s_dst[r] + e0 * E, o);
     } else {
-      // a unit cut by the end of the message or by several block boundaries
+      // a unit cut by several block boundaries (or, on the element path,
+      // the one element of the unit)
       for (int i = 0; i < n; ++i) {
         const long long e = e0 + i;
         const GlobalSrc src{s_src, e * E};
@@ -113,6 +119,12 @@ __global__ void __launch_bounds__(kBlock, kMinBlocksJit ? kMinBlocksJit
         for (int r = 0; r < R; ++r) Unit<T, 1>::store(s_dst[r] + e * E, o);
       }
     }
+  }
+  if (tailU >= ub && tailU < ue && threadIdx.x < count - tailU * NV) {
+    const long long e = tailU * NV + threadIdx.x;
+    const GlobalSrc src{s_src, e * E};
+    const typename Ty<T>::Bits o = fold_element_rare<T, OP, MODE, S>(a, src, s_prog, e, cur);
+    for (int r = 0; r < R; ++r) Unit<T, 1>::store(s_dst[r] + e * E, o);
   }
 }
 

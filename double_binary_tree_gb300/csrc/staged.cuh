@@ -280,18 +280,23 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
               for (int r = 0; r < R; ++r) Unit<T, 1>::store(s_dst[r] + (e0 + x) * E, o);
             }
           }
-        } else {
-          // the partial unit at the end of the message: not copied, read here
-          for (long long e = e0; e < a.hi; ++e) {
-            const GlobalSrc src{s_src, e * E};
-            const typename Ty<T>::Bits o = fold_element<T, OP, MODE, S>(a, src, s_prog, e, cur);
-            for (int r = 0; r < R; ++r) Unit<T, 1>::store(s_dst[r] + e * E, o);
-          }
         }
+        // (the partial unit at the end of the message: below, after the tiles)
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
+  }
+  // The partial unit at the end of the message (not copied): its elements,
+  // read from global memory, go to different consumer threads of the CTA
+  // that owns it, so their loads are not waited for in turn.
+  if constexpr (MODE != kReduceScatter) {
+    if (cue == a.unitsAll && a.unitsAll > a.unitsFull && ct < a.hi - a.unitsFull * U) {
+      const long long e = a.unitsFull * U + ct;
+      const GlobalSrc src{s_src, e * E};
+      const typename Ty<T>::Bits o = fold_element<T, OP, MODE, S>(a, src, s_prog, e, cur);
+      for (int r = 0; r < R; ++r) Unit<T, 1>::store(s_dst[r] + e * E, o);
+    }
   }
 }
 

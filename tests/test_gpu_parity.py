@@ -183,6 +183,17 @@ def test_tree_bit_exact(R, L, count, nch, cb, dtype, path):
 
 
 @pytest.mark.parametrize("algo", [RING, TREE])
+@pytest.mark.parametrize("dtype,count", [(F32, (4 << 20) + 3), (BF16, (8 << 20) + 7)])
+def test_ragged_tail_at_16_mib(algo, dtype, count):
+    """16 MiB per rank plus a partial 16-byte unit (3 fp32 or 7 bf16
+    elements): the default kernel choice (the staged kernel), whose trailing
+    elements are folded by separate threads."""
+    inp = workloads.generate(8, count, dtype, "normal", 150)
+    _, want = expect_allreduce(inp, dtype, SUM, algo, 12, 512 * 1024)
+    assert_bits_equal(run_allreduce(inp, dtype, SUM, algo, 12, 512 * 1024), want)
+
+
+@pytest.mark.parametrize("algo", [RING, TREE])
 @pytest.mark.parametrize("dtype", [F32, F16, BF16])
 def test_max_exact(algo, dtype, path):
     for R, L, count in [(2, 1, 1000), (7, 1, 4097), (64, 8, 3001)]:
