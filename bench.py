@@ -67,7 +67,7 @@ WORKLOAD = dict(name="ring_allreduce_r8_64mib_fp32", R=8, count=16 * 1024 * 1024
                 seed=1)
 PROFILE_SUMMARY = os.path.join(HERE, "profiles", "ring_allreduce_r8_64mib_fp32.md")
 KERNEL_SOURCES = [os.path.join(HERE, "double_binary_tree_gb300", "csrc", f)
-                  for f in ("fold.cuh", "staged.cuh", "kernels_f32.cu", "common.h")]
+                  for f in ("fold.cuh", "staged.cuh", "kernels_f32.cu", "common.h", "bounds.cuh")]
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 THROTTLE_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",

@@ -190,7 +190,12 @@ __global__ void __launch_bounds__(kBlock) copy_ranks_kernel(const __grid_constan
     if (s_src[r] == s_dst[r]) continue;
     const long long off = (u - (long long)r * per) * NB;
     if constexpr (VEC) {
-      st_global_v4(s_dst[r] + off, ld_global_v4(s_src[r] + off));
+      if (off + 16 <= bytes) {
+        st_global_v4(s_dst[r] + off, ld_global_v4(s_src[r] + off));
+      } else {  // the buffer's last bytes, short of a whole 16-byte unit
+        for (long long b = off; b < bytes; ++b)
+          st_plain<char>(s_dst[r] + b, ld_plain<char>(s_src[r] + b));
+      }
     } else {
       st_plain<char>(s_dst[r] + off, ld_plain<char>(s_src[r] + off));
     }

@@ -86,7 +86,11 @@ def test_ring_stepwise_matches_hop_rounding(dtype, op):
                 s.copy_(t)
         else:
             src = [t.cuda() for t in inp]
-        dst = src if inplace else [torch.empty_like(s) for s in src]
+        # outputs inside canary bytes (64 before, 64 after) that must survive
+        E = vr.ELEM_SIZE[dtype]
+        raw = [] if inplace else [torch.full(((count + 2 * 64) * E,), 0x5A, dtype=torch.uint8,
+                                             device="cuda") for _ in src]
+        dst = src if inplace else [b[64 * E:(64 + count) * E].view(TDT[dtype]) for b in raw]
         nbytes = vr.vr_ring_stepwise_scratch_bytes(count, dtype)
         scratch = torch.empty(nbytes + 16, dtype=torch.uint8, device="cuda")
         sptr = scratch.data_ptr() + (vr.ELEM_SIZE[dtype] if shift else 0)  # element-aligned
@@ -94,6 +98,8 @@ def test_ring_stepwise_matches_hop_rounding(dtype, op):
         vr.vr_allreduce_ring_stepwise(src, dst, R, count, dtype, op, nch, cb, sptr, nbytes)
         _status_ok()
         assert vr.vr_launch_count() - before == 1 + 4 * (R - 1)
+        for b in raw:   # nothing written past either end of an output
+            assert bool((b[:64 * E] == 0x5A).all()) and bool((b[(64 + count) * E:] == 0x5A).all())
         _check([_bits(d) for d in dst], want, "stepwise R=%d" % R)
         if dtype == F32 or op == MAX:
             fused = oracle.allreduce(raws, dtype, op, 0, nch, cb)
