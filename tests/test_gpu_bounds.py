@@ -10,9 +10,10 @@
    no access ever leaves real memory), the accesses to the last 16 bytes
    are refused: VR_ERR_INTERNAL (not a timeout: a refused bulk copy still
    completes its barrier), the refused address is reported, and the
-   outputs equal the oracle everywhere else -- with receive buffers cut,
-   their last 16 bytes keep their old contents; with send buffers cut, all
-   but the tail a refused tile covers.  Ring, tree, ReduceScatter and
+   outputs equal the oracle everywhere else (outside the last 16 bytes, or
+   the last tile where a refused access was a bulk copy of a whole tile),
+   and with receive buffers cut, their last 16 bytes keep their old
+   contents.  Ring, tree, ReduceScatter and
    AllGather on the register path and the staged / TMA kernels.
 No bad plan is ever given to a kernel.
 """
@@ -71,7 +72,10 @@ def run(coll, R, n, dtype, algo, path, which):
     what = (coll, path, which)
     assert status == vr.VR_ERR_INTERNAL, (what, status)   # refused, not timed out
     bufs = dst if which == 2 else src
-    span = 16 if which == 2 else TAIL
+    # a refused bulk copy (staged loads, the TMA AllGather's stores) covers a
+    # whole tile, so it reports the tile's start
+    bulk = which == 1 or (coll == "ag" and path == "staged")
+    span = TAIL if bulk else 16
     ends = [(b.data_ptr() + b.numel() * E - span, b.data_ptr() + b.numel() * E) for b in bufs]
     assert any(lo <= where < hi for lo, hi in ends), (what, hex(where))
     raws = [workloads.raw_numpy(t) for t in inp]
@@ -83,13 +87,10 @@ def run(coll, R, n, dtype, algo, path, which):
         want = oracle.allgather(raws)
     for d, w in zip(dst, want):
         got = workloads.raw_numpy(d.cpu())
-        if which == 2:   # only the last unit of every output was refused
-            k = 16 // E
-            assert np.array_equal(got[:-k], w[:-k]), what
+        k = span // E    # outputs exact before the refused span
+        assert np.array_equal(got[:-k], w[:-k]), what
+        if which == 2:   # the refused stores were not made
             assert bool((d.view(torch.uint8)[-16:] == SENT).all()), what
-        else:            # inputs refused at the end: outputs exact before the tail
-            k = TAIL // E
-            assert np.array_equal(got[:-k], w[:-k]), what
     assert vr.vr_stream_status(st) == 0 and vr.vr_debug_bounds_fault() == 0
 
 for path in ("register", "staged"):
