@@ -87,11 +87,18 @@ __global__ void __launch_bounds__(kBlock, kMinBlocksJit ? kMinBlocksJit
   const long long ue = u0 + udiv(units * (blockIdx.x + 1), gridDim.x);
   // The trailing partial unit of a vector call (count % NV elements) is not
   // one thread's work: its elements go to the first threads of the CTA that
-  // owns it, below, so their loads are not waited for in turn.
-  const long long tailU = VEC && count % NV ? count / NV : -1;
+  // owns it, before that CTA's main loop, which stops short of it.
+  const long long fullU = count / NV;  // (the element path has no partial unit)
+  if (VEC && count % NV && fullU >= ub && fullU < ue && threadIdx.x < count - fullU * NV) {
+    const long long e = fullU * NV + threadIdx.x;
+    const GlobalSrc src{s_src, e * E};
+    const typename Ty<T>::Bits o = fold_element_rare<T, OP, MODE, S>(
+        a, src, s_prog, e, Cursor{0, -1, 0, 0, 0, 0, 0});
+    for (int r = 0; r < R; ++r) Unit<T, 1>::store(s_dst[r] + e * E, o);
+  }
+  const long long uEnd = VEC && ue > fullU ? fullU : ue;
   Cursor cur{0, -1, 0, 0, 0, 0, 0};
-  for (long long u = ub + threadIdx.x; u < ue; u += blockDim.x) {
-    if (u == tailU) continue;
+  for (long long u = ub + threadIdx.x; u < uEnd; u += blockDim.x) {
     const long long e0 = u * NV;
     const int n = (int)min((long long)NV, count - e0);
     seek<U, MODE>(a, e0, cur);
@@ -119,12 +126,6 @@ __global__ void __launch_bounds__(kBlock, kMinBlocksJit ? kMinBlocksJit
         for (int r = 0; r < R; ++r) Unit<T, 1>::store(s_dst[r] + e * E, o);
       }
     }
-  }
-  if (tailU >= ub && tailU < ue && threadIdx.x < count - tailU * NV) {
-    const long long e = tailU * NV + threadIdx.x;
-    const GlobalSrc src{s_src, e * E};
-    const typename Ty<T>::Bits o = fold_element_rare<T, OP, MODE, S>(a, src, s_prog, e, cur);
-    for (int r = 0; r < R; ++r) Unit<T, 1>::store(s_dst[r] + e * E, o);
   }
 }
 
