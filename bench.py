@@ -399,13 +399,15 @@ def gpu_arm(args, rank, world, local_rank):
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    for _ in range(args.warmup):
-        step()
-    if vr.vr_stream_status(stream) != 0:
-        raise RuntimeError("device status error during warm-up")
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clk:
         clk.wait_first()
+        # the warm-up steps run right before the timed ones (after the
+        # sampler's start-up, which leaves the GPU idle)
+        for _ in range(args.warmup):
+            step()
+        if vr.vr_stream_status(stream) != 0:
+            raise RuntimeError("device status error during warm-up")
         barrier()
         launches0 = vr.vr_launch_count()
         t_wall0 = time.time()
