@@ -296,16 +296,45 @@ vr_result_t launch(const void* fn, KArgs& a, long long units, void* stream,
   return VR_SUCCESS;
 }
 
-// Which kernel family serves an aligned AllReduce.  With few ranks the
-// staged kernel's stages hold too few bytes in flight, and below 16 MiB per
-// rank its pipeline does not fill.  Measured on GB300: from 16 MiB per rank
-// the staged kernel beats the
-// register path for the ring of 8-64 ranks and, with its fold specialised at
-// run time (jit.cc), for the tree of 8-64 ranks (the interpreting staged tree
-// is 2-3x slower than the register path).
+// Staged geometry of an AllReduce of 2-7 ranks: bytes per rank per tile and
+// stages (0: no staged kernel).  Measured on GB300 (fp32, 16 / 64 / 256 MiB
+// per rank, cold buffers, graph replays, tiles of 4-14 KB per rank and 3-5
+// stages): the best stages hold 20-43 KB, three to five of them -- a short
+// pipeline of large copies, where 8 and more ranks do best with many small
+// stages.  With 2-5 ranks the register path keeps every thread's few loads
+// waiting in turn and reaches 0.67-0.91 of the copy bandwidth; these tiles
+// reach 0.93-0.99 from 64 MiB per rank (2 ranks: tree 0.86-0.93).  The ring
+// of 2 ranks and of 6 ranks keeps the register path (the staged ring was
+// slower there); from 16 to 64 MiB the gain grows from none to 4-10 %.
+struct SmallGeometry {
+  unsigned tile;
+  int stages;
+};
+SmallGeometry small_geometry(int mode, int R) {
+  static const SmallGeometry ring[8] = {{0, 0},    {0, 0},    {0, 0},    {14336, 3},
+                                        {8192, 4}, {6144, 3}, {0, 0},    {4096, 4}};
+  static const SmallGeometry tree[8] = {{0, 0},    {0, 0},    {14336, 4}, {8192, 4},
+                                        {7168, 3}, {6144, 3}, {4096, 4},  {4096, 3}};
+  if (R < 2 || R > 7) return {0, 0};
+  return mode == kRingAllReduce ? ring[R] : mode == kTreeAllReduce ? tree[R] : SmallGeometry{0, 0};
+}
+constexpr size_t kSmallStagedMinBytes = 32u << 20;  // per rank, 2-7 ranks
+
+// Which kernel family serves an aligned AllReduce.  Below 16 MiB per rank
+// the staged kernel's pipeline does not fill.  Measured on GB300: from 16 MiB
+// per rank the staged kernel beats the register path for the ring of 8-64
+// ranks and, with its fold specialised at run time (jit.cc), for the tree of
+// 8-64 ranks (the interpreting staged tree is 2-3x slower than the register
+// path); with 2-7 ranks it wins from 32 MiB per rank with the geometry above.
 bool use_staged(int mode, int R, size_t bytesPerRank) {
   const size_t minBytes = (size_t)option(kOptStagedMinBytes);
-  if (R < 8 || bytesPerRank < minBytes) return false;
+  if (R < 8) {
+    if (small_geometry(mode, R).tile == 0 ||
+        bytesPerRank < std::max(minBytes, kSmallStagedMinBytes))
+      return false;
+  } else if (bytesPerRank < minBytes) {
+    return false;
+  }
   if (mode == kRingAllReduce) return true;
   if (mode == kTreeAllReduce) return jit_enabled();
   return false;
@@ -328,6 +357,7 @@ bool use_staged_rs(int R, int dtype, size_t sendBytesPerRank) {
 // up to 16 KB per rank).
 unsigned staged_tile_bytes(int R, int mode) {
   if (mode == kReduceScatter) return std::min(16384u, (65536u / (unsigned)R) & ~15u);
+  if (R < 8 && small_geometry(mode, R).tile) return small_geometry(mode, R).tile;
   return R > 8 && R <= 16 ? 4096u : 2048u;
 }
 
@@ -381,7 +411,9 @@ vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
   a.stageBytes = ((unsigned)a.R * a.tileBytes + 127u) & ~127u;
   const int fit = room / (int)a.stageBytes;
   a.stages = std::min(kStagedMaxStages, fit);
-  const int cap = (int)option(kOptStagedStages);
+  int cap = (int)option(kOptStagedStages);
+  if (!cap && a.R < 8 && mode != kReduceScatter && (unsigned)tb == small_geometry(mode, a.R).tile)
+    cap = small_geometry(mode, a.R).stages;  // the few-rank geometry's short pipeline
   if (cap) a.stages = std::min(a.stages, cap);
   if (a.stages < 2) return VR_ERR_INTERNAL;
   a.consumers = std::max(1, std::min(kStagedMaxConsumers, a.tileUnits / 32));
