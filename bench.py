@@ -885,6 +885,9 @@ def profile_case(args):
     import double_binary_tree_gb300 as vr
     coll, R, L, dtype, op, algo = PROFILE_CASES[args.profile]
     count = args.count
+    for opt in args.option:   # library options for the capture, NAME=VALUE
+        name, value = opt.split("=", 1)
+        vr.vr_set_option(name, int(value))
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
     g = torch.Generator(device=dev)
@@ -971,6 +974,8 @@ def main():
                    help="run one collective configuration only (for ncu)")
     p.add_argument("--count", type=int, default=8 * 1024 * 1024,
                    help="elements per rank for --profile")
+    p.add_argument("--option", action="append", default=[],
+                   help="NAME=VALUE library option (vr_set_option) for --profile")
     args = p.parse_args()
     if args.warmup < 3:
         p.error("--warmup must be at least 3")

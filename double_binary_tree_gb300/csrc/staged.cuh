@@ -99,8 +99,9 @@ __device__ __forceinline__ void raise_error(unsigned* status, volatile int* abor
 // Tile i of a CTA's work: the byte offset of its slice inside each source
 // rank's buffer, the bytes the producer copies, and the units it covers.
 // AllReduce: every CTA owns an equal run [cub, cue) of the message's units
-// (to one unit) and cuts it into tiles of tileUnits, the last one shorter,
-// so no CTA waits on a whole extra tile at the end.  ReduceScatter: tile t
+// (to 8 units: the runs start on 128-byte boundaries) and cuts it into
+// tiles of tileUnits, the last one shorter, so no CTA waits on a whole extra
+// tile at the end.  ReduceScatter: tile t
 // (= tb + i) of the whole call, tiles not crossing a block.
 struct TileGeom {
   long long srcOff;   // bytes from each source buffer's start
@@ -189,9 +190,17 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
     tb = udiv(a.tiles * blockIdx.x, gridDim.x);
     n = udiv(a.tiles * (blockIdx.x + 1), gridDim.x) - tb;
   } else {
+    // split points on 128-byte boundaries of every rank's buffer (8 units):
+    // a bulk copy that started inside a 32-byte sector would read one more
+    // sector per rank (measured: 1-3 % slower at 2 KB and 1.5 KB tiles)
     const long long total = a.unitsAll - a.unitLo;
-    cub = a.unitLo + udiv(total * blockIdx.x, gridDim.x);
-    cue = a.unitLo + udiv(total * (blockIdx.x + 1), gridDim.x);
+    auto split = [&](unsigned b) -> long long {
+      if (b == 0) return a.unitLo;
+      if (b == gridDim.x) return a.unitsAll;
+      return max(a.unitLo, (a.unitLo + udiv(total * b, gridDim.x)) & ~7LL);
+    };
+    cub = split(blockIdx.x);
+    cue = split(blockIdx.x + 1);
     n = (cue - cub + a.tileUnits - 1) / a.tileUnits;
   }
 
