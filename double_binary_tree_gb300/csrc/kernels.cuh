@@ -2,12 +2,12 @@
 //
 // Each thread loads the R ranks' copies of a unit straight from global
 // memory (up to kBatch loads in flight), folds them (fold.cuh) and stores the
-// result to every receiving rank.  They serve AllReduce of fewer than 8
-// ranks or under 16 MiB per rank, the tree when run-time specialisation is
-// off, ReduceScatter outside the staged kernel's range (16-bit types, more
-// than 8 ranks, under 16 MiB sent per rank), and buffers that are not
-// 16-byte aligned (element units).  AllReduce of 8 or more ranks from 16 MiB
-// per rank runs the TMA-staged kernel of staged.cuh.
+// result to every receiving rank.  They serve AllReduce under 16 MiB per
+// rank (under 32 MiB for 2-7 ranks) and the rings of 2 and 6 ranks, the tree
+// when run-time specialisation is off, ReduceScatter outside the staged
+// kernel's range (16-bit types, more than 8 ranks, under 16 MiB sent per
+// rank), and buffers that are not 16-byte aligned (element units).  Larger
+// aligned AllReduce runs the TMA-staged kernel of staged.cuh.
 //
 // Persistent grid: CTA b owns a contiguous run of units and its threads
 // stride through it, so a warp touches 512 contiguous bytes of each rank per
