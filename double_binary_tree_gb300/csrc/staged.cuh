@@ -98,11 +98,10 @@ __device__ __forceinline__ void raise_error(unsigned* status, volatile int* abor
 
 // Tile i of a CTA's work: the byte offset of its slice inside each source
 // rank's buffer, the bytes the producer copies, and the units it covers.
-// AllReduce: every CTA owns an equal run [cub, cue) of the message's units
-// (to 8 units: the runs start on 128-byte boundaries) and cuts it into
-// tiles of tileUnits, the last one shorter, so no CTA waits on a whole extra
-// tile at the end.  ReduceScatter: tile t
-// (= tb + i) of the whole call, tiles not crossing a block.
+// AllReduce: every CTA owns a run [cub, cue) of whole tiles of the message
+// (the last tile of the message shorter) and takes them in turn.
+// ReduceScatter: tile t (= tb + i) of the whole call, tiles not crossing a
+// block.
 struct TileGeom {
   long long srcOff;   // bytes from each source buffer's start
   unsigned bytes;     // bytes copied per rank (full 16-byte units only)
@@ -184,24 +183,21 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
   pdl_wait();  // the previous kernel on the stream is done
 
   // this CTA's work: tiles [tb, tb + n) of the call (ReduceScatter), or the
-  // units [cub, cue) cut into n tiles (AllReduce)
+  // units [cub, cue), n tiles (AllReduce)
   long long tb = 0, n = 0, cub = 0, cue = 0;
   if constexpr (MODE == kReduceScatter) {
     tb = udiv(a.tiles * blockIdx.x, gridDim.x);
     n = udiv(a.tiles * (blockIdx.x + 1), gridDim.x) - tb;
   } else {
-    // split points on 128-byte boundaries of every rank's buffer (8 units):
-    // a bulk copy that started inside a 32-byte sector would read one more
-    // sector per rank (measured: 1-3 % slower at 2 KB and 1.5 KB tiles)
-    const long long total = a.unitsAll - a.unitLo;
-    auto split = [&](unsigned b) -> long long {
-      if (b == 0) return a.unitLo;
-      if (b == gridDim.x) return a.unitsAll;
-      return max(a.unitLo, (a.unitLo + udiv(total * b, gridDim.x)) & ~7LL);
-    };
-    cub = split(blockIdx.x);
-    cue = split(blockIdx.x + 1);
-    n = (cue - cub + a.tileUnits - 1) / a.tileUnits;
+    // whole tiles per CTA, on the tile grid of the message: measured 0.5-1.5 %
+    // faster than equal runs of units (R = 4, 8 and 64), whose copies do not
+    // start on the tile grid (and 1-3 % more when those do not start on
+    // 32-byte sectors either)
+    const long long tb2 = udiv(a.tiles * blockIdx.x, gridDim.x);
+    const long long te2 = udiv(a.tiles * (blockIdx.x + 1), gridDim.x);
+    cub = a.unitLo + tb2 * a.tileUnits;
+    cue = min(a.unitsAll, a.unitLo + te2 * a.tileUnits);
+    n = te2 - tb2;
   }
 
   if (warp == 0) {
