@@ -224,14 +224,17 @@ const void* pick_staged(int dtype, int mode, int op, int stack = 0) {
 
 // Register-path kernel; fp32 with at most 4 ranks takes the variant compiled
 // for 3 CTAs per SM (1.2-1.5x faster from 16 MiB per rank; slower for 16-bit
-// types, which keep the general kernel).  The option VR_SMALL_RANKS=0 turns
-// it off for tuning.
-bool use_small(int dtype, int mode, bool vec, int stack, int R) {
+// types, which keep the general kernel).  Rings below 8 MiB per rank keep
+// the general kernel too: measured at 4 ranks, 17 % faster at 1 MiB and 2 %
+// at 4 MiB, 7 % slower at 16 and 24 MiB (trees: no difference).  The option
+// VR_SMALL_RANKS=0 turns it off for tuning.
+bool use_small(int dtype, int mode, bool vec, int stack, int R, size_t bytesPerRank) {
   return dtype == VR_FLOAT32 && vec && R <= 4 && stack <= 4 && mode != kReduceScatter &&
-         option(kOptSmallRanks) != 0;
+         (mode != kRingAllReduce || bytesPerRank >= (8u << 20)) && option(kOptSmallRanks) != 0;
 }
-const void* pick_kernel(int dtype, int mode, int op, bool vec, int stack = 0, int R = 64) {
-  const bool small = use_small(dtype, mode, vec, stack, R);
+const void* pick_kernel(int dtype, int mode, int op, bool vec, int stack = 0, int R = 64,
+                        size_t bytesPerRank = 0) {
+  const bool small = use_small(dtype, mode, vec, stack, R, bytesPerRank);
   switch (dtype) {
     case VR_FLOAT32: return kernel_ptr_f32(mode, op, vec, stack, small);
     case VR_FLOAT16: return kernel_ptr_f16(mode, op, vec, stack, small);
@@ -496,7 +499,7 @@ const void* more_resident(const void* special, long long units, int dtype, int o
   const long long roundsNow = (units + oneCtaPerSm * now - 1) / (oneCtaPerSm * now);
   const long long roundsFour = (units + oneCtaPerSm * 4 - 1) / (oneCtaPerSm * 4);
   if (occ != 4 && (roundsNow > 3 || roundsFour >= roundsNow)) return special;
-  const bool small = use_small(dtype, mode, true, stack, a.R);
+  const bool small = use_small(dtype, mode, true, stack, a.R, (size_t)a.count * elem_size(dtype));
   const void* four = nullptr;
   const vr_result_t e =
       mode == kTreeAllReduce
@@ -514,6 +517,7 @@ const void* more_resident(const void* special, long long units, int dtype, int o
 vr_result_t launch_allreduce_range(KArgs& a, int dtype, int mode, int op, int stack, bool vec,
                                    bool staged, long long lo, long long hi, void* stream) {
   const long long E = (long long)elem_size(dtype);
+  const size_t bytes = (size_t)a.count * (size_t)E;  // per rank, the whole message
   a.lo = lo;
   a.hi = hi;
   // Trees on 16-byte units: the kernels specialised for this call's programs
@@ -522,8 +526,8 @@ vr_result_t launch_allreduce_range(KArgs& a, int dtype, int mode, int op, int st
   // interpreting one at 64 ranks: above 32 only the staged one is used.)
   const void* special = nullptr;
   if (mode == kTreeAllReduce && vec && (staged || a.R <= 32) && jit_enabled() &&
-      jit_tree_kernel(dtype, op, stack, use_small(dtype, mode, vec, stack, a.R), staged, a.prog,
-                      a.nProgs, &special) != VR_SUCCESS)
+      jit_tree_kernel(dtype, op, stack, use_small(dtype, mode, vec, stack, a.R, bytes), staged,
+                      a.prog, a.nProgs, &special) != VR_SUCCESS)
     special = nullptr;
   // The ring specialised for R ranks: measured 6-12% faster on the register
   // path for 3-16 ranks, neutral on the staged one (VR_JIT_RING=1 also takes
@@ -531,7 +535,7 @@ vr_result_t launch_allreduce_range(KArgs& a, int dtype, int mode, int op, int st
   const long long jr = option(kOptJitRing);
   if (mode == kRingAllReduce && vec && a.R >= 3 && a.R <= 16 && jr != 0 &&
       (!staged || jr == 1) && jit_enabled() &&
-      jit_ring_kernel(dtype, op, a.R, use_small(dtype, mode, vec, stack, a.R), staged,
+      jit_ring_kernel(dtype, op, a.R, use_small(dtype, mode, vec, stack, a.R, bytes), staged,
                       &special) != VR_SUCCESS)
     special = nullptr;
   if (staged) {
@@ -544,8 +548,8 @@ vr_result_t launch_allreduce_range(KArgs& a, int dtype, int mode, int op, int st
   const long long NV = vec ? kGrainBytes / E : 1;
   const long long units = (hi + NV - 1) / NV - lo / NV;
   if (special) special = more_resident(special, units, dtype, op, mode, stack, a);
-  return launch(special ? special : pick_kernel(dtype, mode, op, vec, stack, a.R), a, units,
-                stream);
+  return launch(special ? special : pick_kernel(dtype, mode, op, vec, stack, a.R, bytes), a,
+                units, stream);
 }
 
 // Per device: the two copy streams and three events of vr_allreduce_host,
@@ -677,10 +681,20 @@ vr_result_t plan_allreduce(const void* const* sendbufs, void* const* recvbufs, i
   fill_partition(a, count, E, nChannels, chunkBytes);
   mode = kRingAllReduce;
   stack = 0;
-  if (algo == VR_ALGO_TREE && count > 0) {
+  // Two ranks: the ring folds every element as x_j (op) x_(j+1), and for two
+  // operands both orders give the same bits (IEEE addition and the Max of
+  // the total order commute), so it is also the two-rank tree's fold, local
+  // input first.  The ring of two ranks runs the tree kernels (with the
+  // few-rank staged geometry of the tree): measured on GB300, 5.2 against
+  // 8.0 us at 4 MiB per rank and 0.86 against 0.66 of the copy bandwidth at
+  // 64 MiB.
+  const bool twoRankRing = algo == VR_ALGO_RING && R == 2;
+  if ((algo == VR_ALGO_TREE || twoRankRing) && count > 0) {
     mode = kTreeAllReduce;
     std::array<FoldProg, 2> p;
-    if ((e = tree_programs(R / localRanks, localRanks, &p)) != VR_SUCCESS) return e;
+    if ((e = tree_programs(twoRankRing ? 2 : R / localRanks, twoRankRing ? 1 : localRanks,
+                           &p)) != VR_SUCCESS)
+      return e;
     set_dtree_programs(a, p, nChannels);
     stack = std::max(p[0].depth, p[1].depth);
   }
@@ -688,7 +702,7 @@ vr_result_t plan_allreduce(const void* const* sendbufs, void* const* recvbufs, i
     static vr_tree_t trees[kMaxRanks * kMaxChannels];  // under the log's own lock below
     static std::mutex mu;
     std::lock_guard<std::mutex> g(mu);
-    const bool tree = mode == kTreeAllReduce &&
+    const bool tree = algo == VR_ALGO_TREE &&
                       build_dtree(R / localRanks, localRanks, nChannels, trees) == VR_SUCCESS;
     log_plan("allreduce", algo, R, localRanks, count, dtype, nChannels, chunkBytes,
              tree ? trees : nullptr, true);

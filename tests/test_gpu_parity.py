@@ -182,6 +182,17 @@ def test_tree_bit_exact(R, L, count, nch, cb, dtype, path):
     assert_bits_equal(run_allreduce(inp, dtype, SUM, TREE, nch, cb, L), want)
 
 
+@pytest.mark.parametrize("dtype", [F32, F16, BF16])
+@pytest.mark.parametrize("op", [SUM, MAX])
+def test_two_rank_ring_at_64_mib(dtype, op):
+    """The ring of two ranks runs the tree kernels (two operands fold to the
+    same bits in either order): every element equal to the oracle's ring."""
+    count = (64 << 20) // vr.ELEM_SIZE[dtype] + 5
+    inp = workloads.generate(2, count, dtype, "normal", 160 + dtype)
+    _, want = expect_allreduce(inp, dtype, op, RING, 12, 512 * 1024)
+    assert_bits_equal(run_allreduce(inp, dtype, op, RING, 12, 512 * 1024), want)
+
+
 @pytest.mark.parametrize("algo", [RING, TREE])
 @pytest.mark.parametrize("dtype,count", [(F32, (4 << 20) + 3), (BF16, (8 << 20) + 7)])
 def test_ragged_tail_at_16_mib(algo, dtype, count):
