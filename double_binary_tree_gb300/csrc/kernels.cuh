@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kBlock, kMinBlocksRing)
     const int j = b + 1 == R ? 0 : b + 1;
     if (n == NV) {
       const GlobalSrc src{s_src, ((long long)b * rc + p0) * E};
-      Unit<T, NV>::store(s_dst[b] + p0 * E, ring_fold<T, OP, NV>(src, R, j));
+      Unit<T, NV>::store(s_dst[b] + p0 * E, ring_fold_2<T, OP, NV>(src, R, j));
     } else {
       for (int i = 0; i < n; ++i) {
         const GlobalSrc src{s_src, ((long long)b * rc + p0 + i) * E};
