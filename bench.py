@@ -289,14 +289,16 @@ TIE = 0.05            # ring and tree within 5 % of each other: a tie
 
 
 def stats_of(xs):
-    """Median, P95 (nearest rank), mean and CV of per-iteration times (ms)."""
+    """Median, P95 (nearest rank), mean and CV of per-iteration times (ms),
+    and the samples themselves (us, in the order taken)."""
+    raw = [round(x * 1e3, 3) for x in xs]
     xs = sorted(xs)
     n = len(xs)
     mean = sum(xs) / n
     sd = statistics.pstdev(xs) if n > 1 else 0.0
     return {"median_us": round(statistics.median(xs) * 1e3, 3),
             "p95_us": round(xs[min(n - 1, max(0, -(-95 * n // 100) - 1))] * 1e3, 3),
-            "cv": round(sd / mean, 4) if mean > 0 else 0.0, "n": n}
+            "cv": round(sd / mean, 4) if mean > 0 else 0.0, "n": n, "samples_us": raw}
 
 
 def measure(samplers, samples=SAMPLES):

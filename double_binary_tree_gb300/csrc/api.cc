@@ -24,6 +24,7 @@ std::mutex g_mu;
 
 struct DeviceInfo {
   int sms = 0;
+  int l2Bytes = 0;
   int smemOptin = 0;  // largest dynamic shared memory a CTA may opt into
   unsigned* status = nullptr;
   unsigned long long* boundsWhere = nullptr;  // first refused address (bounds-checked build)
@@ -82,7 +83,8 @@ vr_result_t device_info(DeviceInfo* out, int* device) {
     DeviceInfo d;
     if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, *device) != cudaSuccess ||
         cudaDeviceGetAttribute(&d.smemOptin, cudaDevAttrMaxSharedMemoryPerBlockOptin, *device) !=
-            cudaSuccess)
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&d.l2Bytes, cudaDevAttrL2CacheSize, *device) != cudaSuccess)
       return VR_ERR_CUDA;
     if (status_word_address(&d.status) != cudaSuccess ||
         bounds_word_address(&d.boundsWhere) != cudaSuccess)
@@ -952,11 +954,22 @@ vr_result_t vr_allgather(const void* const* sendbufs, void* const* recvbufs, int
     DeviceInfo di;
     int device = 0;
     if ((e = device_info(&di, &device)) != VR_SUCCESS) return e;
+    // Destination-major (one store per loaded tile, the sources re-read from
+    // L2) when the R sources together take at most a quarter of L2, with
+    // 32 KB tiles in 3 stages.  Measured on GB300 (graph replays): R=64 x
+    // 16 MiB fp16 152-153 us against 166 us source-major (7.2 TB/s: the
+    // writes dominate, so this passes the read+write copy bandwidth), R=16
+    // 40.6 against 42.8 us, R=4 and R=8 equal to 2 %; with larger sources
+    // (R=8 x 128 MiB, R=64 x 64 MiB) source-major was 2-6 % faster.
+    const long long order = option(kOptAgOrder);
+    const bool destMajor =
+        order == 2 || (order == 0 && (size_t)R * bytes <= (size_t)di.l2Bytes / 4);
     // geometry: tuning overrides VR_AG_TILE / VR_AG_STAGES / VR_AG_CTAS
-    const int tile = (int)option_or(kOptAgTile, gather_tile_bytes());
-    const int stages = (int)option_or(kOptAgStages, gather_stages());
+    const int tile = (int)option_or(kOptAgTile, destMajor ? 32768 : gather_tile_bytes());
+    const int stages = (int)option_or(kOptAgStages, destMajor ? 3 : gather_stages());
     const int ctas = (int)std::max(1LL, option_or(kOptAgCtas, gather_ctas_per_sm()));
-    const void* fn = kernel_ptr_allgather_tma(tile, stages);
+    const void* fn = destMajor ? kernel_ptr_allgather_tma_dest(tile, stages)
+                               : kernel_ptr_allgather_tma(tile, stages);
     if (!fn) return VR_ERR_INVALID_ARGUMENT;
     const size_t smem = (size_t)tile * stages;
     {
@@ -969,7 +982,7 @@ vr_result_t vr_allgather(const void* const* sendbufs, void* const* recvbufs, int
         set = (int)smem;
       }
     }
-    a.tiles = (long long)R * (((long long)bytes + tile - 1) / tile);
+    a.tiles = (long long)R * (((long long)bytes + tile - 1) / tile) * (destMajor ? R : 1);
     a.status = di.status;
     a.boundsWhere = di.boundsWhere;
     shrink_extents(a);

@@ -107,4 +107,136 @@ __global__ void __launch_bounds__(kWarpSize) allgather_tma_kernel(const __grid_c
   bulk_wait_all();
 }
 
+// Destination-major AllGather for small sources (the R source buffers
+// together well inside L2): the output space is cut into tiles, taken in
+// destination order, so each CTA writes long runs of one destination buffer
+// -- one bulk load (of a source tile, an L2 hit after its first read) and one
+// bulk store per tile, where the source-major kernel stores every loaded tile
+// R times to R places.  Loads run NS - 1 tiles ahead of the stores; sources
+// are loaded with an L2 evict-last policy and the output is stored with
+// evict-first, so the streaming output does not push the sources out.
+// a.tiles: R destinations x R blocks x tiles per block.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, unsigned bytes,
+                                               uint32_t bar, uint64_t policy) {
+  if (!VR_ACCESS_OK(src, bytes, false)) {
+    mbar_complete_tx(bar, bytes);
+    return;
+  }
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_store_hint(void* dst, uint32_t src, unsigned bytes,
+                                                uint64_t policy) {
+  if (!VR_ACCESS_OK(dst, bytes, true)) return;
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::
+                   "l"(dst), "r"(src), "r"(bytes), "l"(policy)
+               : "memory");
+}
+
+template <unsigned TILE, int NS>
+__global__ void __launch_bounds__(kWarpSize)
+    allgather_tma_dest_kernel(const __grid_constant__ KArgs a) {
+  extern __shared__ __align__(128) unsigned char stage_mem[];
+  unsigned char(*stage)[TILE] = reinterpret_cast<unsigned char(*)[TILE]>(stage_mem);
+  __shared__ __align__(8) uint64_t full[NS];
+  __shared__ int abort_flag;
+  __shared__ const char* s_src[kMaxRanks];
+  __shared__ char* s_dst[kMaxRanks];
+  const int lane = threadIdx.x;
+  const int R = a.R;
+  for (int i = lane; i < R; i += kWarpSize) {
+    s_src[i] = static_cast<const char*>(a.src[i]);
+    s_dst[i] = static_cast<char*>(a.dst[i]);
+  }
+  VR_BOUNDS_SETUP(a);
+  if (lane == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < NS; ++s) mbar_init(smem_addr(&full[s]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncwarp();
+
+  const long long bytes = a.count;
+  const long long perRank = (bytes + TILE - 1) / TILE;
+  const long long perDest = (long long)R * perRank;
+  const long long tb = udiv(a.tiles * blockIdx.x, gridDim.x);
+  const long long n = udiv(a.tiles * (blockIdx.x + 1), gridDim.x) - tb;
+  const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
+  // tile i of this CTA: destination q, source block r, byte offset off, size
+  auto geom = [&](long long i, int& q, int& r, long long& off, unsigned& sz) {
+    const long long t = tb + i;
+    q = (int)udiv(t, perDest);
+    const long long rem = t - (long long)q * perDest;
+    r = (int)udiv(rem, perRank);
+    off = (rem - (long long)r * perRank) * TILE;
+    sz = (unsigned)min((long long)TILE, bytes - off);
+  };
+  const long long stallAt = blockIdx.x == 0 ? a.injectStall : -1;
+  long long issued = 0;  // loads issued: tiles [0, issued)
+  auto issue = [&](long long i) {
+    issued = i + 1;
+    int q, r;
+    long long off;
+    unsigned sz;
+    geom(i, q, r, off, sz);
+    const int s = (int)(i % NS);
+    if (lane == 0) {
+      mbar_arrive_expect_tx(smem_addr(&full[s]), sz);
+      // test hook: CTA 0 never loads its tile a.injectStall (the bounded
+      // wait for it runs out: the failure path, without any fault)
+      if (i != stallAt)
+        bulk_load_hint(smem_addr(stage[s]), s_src[r] + off, sz, smem_addr(&full[s]), keep);
+    }
+  };
+  for (long long i = 0; i < NS - 1 && i < n; ++i) issue(i);
+  for (long long i = 0; i < n; ++i) {
+    const int s = (int)(i % NS);
+    const bool ok = __any_sync(~0u, wait_phase(smem_addr(&full[s]), (unsigned)((i / NS) & 1),
+                                               &abort_flag, false, a.timeoutNs));
+    if (!ok) {
+      if (lane == 0) raise_error(a.status, &abort_flag, VR_ERR_TIMEOUT);
+      // every load issued must land (bounded) before the CTA's shared
+      // memory goes away; the tile the test hook skipped never comes
+      for (long long j = i; j < issued; ++j)
+        if (j != stallAt)
+          (void)__any_sync(~0u, wait_phase(smem_addr(&full[(int)(j % NS)]),
+                                           (unsigned)((j / NS) & 1), &abort_flag, false,
+                                           a.timeoutNs));
+      break;
+    }
+    int q, r;
+    long long off;
+    unsigned sz;
+    geom(i, q, r, off, sz);
+    char* to = s_dst[q] + (long long)r * bytes + off;
+    if (lane == 0) {
+      if (to != s_src[r] + off) bulk_store_hint(to, smem_addr(stage[s]), sz, stream);
+      bulk_commit();
+    }
+    // the next load reuses the stage of tile i - 1, whose store must have
+    // read it out (only tile i's store may still be reading)
+    if (i + NS - 1 < n) {
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+      issue(i + NS - 1);
+    }
+  }
+  if (lane == 0) bulk_wait_all();
+  __syncwarp();
+}
+
 }  // namespace vr

@@ -25,6 +25,7 @@ enum Option : int {
   kOptAgTile,          // -1: gather_tile_bytes()
   kOptAgStages,        // -1: gather_stages()
   kOptAgCtas,          // -1: gather_ctas_per_sm()
+  kOptAgOrder,         // 0 by source size, 1 source-major, 2 destination-major
   kOptDebug,           // bit set of kDebug* subsystems
   kOptCount
 };
@@ -86,6 +87,8 @@ const void* kernel_ptr_bf16(int mode, int op, bool vec, int stack, bool small);
 const void* kernel_ptr_allgather(bool vec);
 // TMA AllGather (16-byte aligned buffers): one warp per CTA.
 const void* kernel_ptr_allgather_tma(int tile, int stages);
+// The destination-major one (sources small enough to stay in L2).
+const void* kernel_ptr_allgather_tma_dest(int tile, int stages);
 int gather_tile_bytes();
 int gather_stages();
 int gather_ctas_per_sm();

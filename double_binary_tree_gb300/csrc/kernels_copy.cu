@@ -24,6 +24,14 @@ const void* kernel_ptr_allgather_tma(int tile, int stages) {
 #undef VR_AG
   return nullptr;
 }
+// Destination-major TMA AllGather variants (small sources).
+const void* kernel_ptr_allgather_tma_dest(int tile, int stages) {
+#define VR_AG(T, S) \
+  if (tile == T && stages == S) return (const void*)allgather_tma_dest_kernel<T, S>;
+  VR_AG(8192, 4) VR_AG(8192, 8) VR_AG(16384, 4) VR_AG(16384, 6) VR_AG(32768, 3) VR_AG(4096, 8)
+#undef VR_AG
+  return nullptr;
+}
 int gather_tile_bytes() { return (int)kGatherTile; }
 int gather_stages() { return kGatherStages; }
 int gather_ctas_per_sm() { return kGatherCtasPerSm; }

@@ -74,6 +74,13 @@
  *                                   and stages that are compiled: 8192/4,
  *                                   8192/8, 16384/4, 16384/6, 32768/3,
  *                                   4096/8; others are INVALID_ARGUMENT)
+ *   VR_AG_ORDER=1|2                 TMA AllGather tile order: source-major
+ *                                   (each loaded tile stored to all R
+ *                                   outputs) / destination-major (each
+ *                                   output written in long runs, sources
+ *                                   re-read from L2); by default
+ *                                   destination-major when the R sources
+ *                                   take at most a quarter of L2
  *   VR_DEBUG=GRAPH                  print every tree set, ring and channel
  *                                   partition a call plans to stderr, in
  *                                   the log formats of [Course13] "从 GRAPH

@@ -75,19 +75,23 @@ def test_stall_request_is_consumed_once_and_cancellable():
         vr.vr_debug_stall_next(-2)
 
 
-def test_allgather_stalled_tile_times_out_and_recovers():
-    """The TMA AllGather's waits are bounded too: CTA 0 skips the load of its
-    first tile, the call reports VR_ERR_TIMEOUT, and the next call is exact."""
+@pytest.mark.parametrize("order", [1, 2])
+def test_allgather_stalled_tile_times_out_and_recovers(order):
+    """The TMA AllGather's waits are bounded too (source-major and
+    destination-major kernels): CTA 0 skips the load of its first tile, the
+    call reports VR_ERR_TIMEOUT, and the next call is exact."""
     R, sc = 4, 1 << 20
     src = [torch.full((sc,), float(r + 1), device="cuda") for r in range(R)]
     dst = [torch.zeros(R * sc, device="cuda") for _ in range(R)]
     stream = torch.cuda.current_stream()
-    vr.vr_debug_stall_next(0)
-    t0 = time.time()
-    vr.vr_allgather(src, dst, R, sc, vr.VR_FLOAT32, vr.VR_ALGO_RING, 12, 512 * 1024, stream)
-    assert vr.vr_stream_status(stream) == vr.VR_ERR_TIMEOUT
-    assert time.time() - t0 < 30
-    vr.vr_allgather(src, dst, R, sc, vr.VR_FLOAT32, vr.VR_ALGO_RING, 12, 512 * 1024, stream)
+    with options(vr, VR_AG_ORDER=order):
+        vr.vr_debug_stall_next(0)
+        t0 = time.time()
+        vr.vr_allgather(src, dst, R, sc, vr.VR_FLOAT32, vr.VR_ALGO_RING, 12, 512 * 1024, stream)
+        assert vr.vr_stream_status(stream) == vr.VR_ERR_TIMEOUT
+        assert time.time() - t0 < 30
+        vr.vr_allgather(src, dst, R, sc, vr.VR_FLOAT32, vr.VR_ALGO_RING, 12, 512 * 1024,
+                        stream)
     assert vr.vr_stream_status(stream) == 0
     want = torch.cat(src)
     for d in dst:

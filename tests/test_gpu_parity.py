@@ -320,6 +320,33 @@ def test_reduce_scatter_bit_exact(dtype, op, path):
         assert_bits_equal([bits(d) for d in dst], want, "rs R=%d" % R)
 
 
+@pytest.mark.parametrize("order", [1, 2])
+@pytest.mark.parametrize("dtype", [F32, BF16])
+def test_allgather_tma_both_orders(order, dtype):
+    """The TMA AllGather, source-major (1) and destination-major (2): bit
+    copies equal to the oracle's, in place and out of place, ragged tiles."""
+    E = vr.ELEM_SIZE[dtype]
+    for R, sc, inplace in [(2, 4096, False), (8, 40960 // E, True), (5, 100000 - 100000 % 8, False),
+                           (64, 8192 // E + 8, False), (3, 8, False)]:
+        inp = workloads.generate(R, sc, dtype, "normal", 850 + R)
+        want = oracle.allgather([workloads.raw_numpy(t) for t in inp])
+        if inplace:
+            outs = [torch.empty(R * sc, dtype=TDT[dtype], device="cuda") for _ in range(R)]
+            for r in range(R):
+                outs[r][r * sc:(r + 1) * sc].copy_(inp[r].cuda())
+            src, dst, bufs = [outs[r][r * sc:(r + 1) * sc] for r in range(R)], outs, None
+        else:
+            src = to_device(inp)
+            bufs = Bufs(R, R * sc, dtype)
+            dst = bufs.views
+        with options(vr, VR_AG_ORDER=order):
+            vr.vr_allgather(src, dst, R, sc, dtype, RING, 12, 512)
+        assert_status_ok()
+        if bufs:
+            bufs.check_canaries()
+        assert_bits_equal([bits(d) for d in dst], want, "ag order %d R=%d" % (order, R))
+
+
 @pytest.mark.parametrize("dtype", [F32, F16, BF16])
 def test_allgather_exact(dtype, path):
     for R, sc, inplace, shift in [(1, 7, False, 0), (2, 1, False, 0), (3, 1001, False, 0),
