@@ -109,7 +109,7 @@ typedef enum {
   VR_ERR_UNSUPPORTED = 2,      /* valid arguments, combination not offered  */
   VR_ERR_CUDA = 3,             /* a CUDA runtime call failed                */
   VR_ERR_TIMEOUT = 4,          /* a bounded device-side wait ran out        */
-  VR_ERR_INTERNAL = 5          /* a library invariant failed                */
+  VR_ERR_INTERNAL = 5          /* a library invariant failed (bounds fault) */
 } vr_result_t;
 
 typedef enum { VR_FLOAT32 = 0, VR_FLOAT16 = 1, VR_BFLOAT16 = 2 } vr_dtype_t;
@@ -219,13 +219,15 @@ vr_result_t vr_ring_block(size_t count, vr_dtype_t dtype, int R, int nChannels,
  * loop and the chunk of a tree channel.
  * In place: sendbufs[r] == recvbufs[r] is allowed.
  * Buffers: any alignment.  16-byte aligned buffers run 16-byte units: from
- * 16 MiB per rank the ring and the tree with 8..64 ranks run
- * on a kernel that stages each tile of all R ranks in shared memory with bulk
- * asynchronous copies (the tree's fold specialised at run time, see
- * vr_jit_status), everything else on a kernel that loads the ranks' units
- * into registers (rings of at most 64 Ki elements per rank: one element per
- * thread).  The environment variable VR_KERNEL_PATH=staged|register (read on
- * every call) forces one of the two for testing and tuning; results are
+ * 16 MiB per rank the ring and the tree with 8..64 ranks, and from 32 MiB
+ * per rank those with 2..7 ranks (but the ring of 6), run on a kernel that
+ * stages each tile of all R ranks in shared memory with bulk asynchronous
+ * copies (the tree's fold specialised at run time, see vr_jit_status),
+ * everything else on a kernel that loads the ranks' units into registers
+ * (rings of at most 64 Ki elements per rank: one element per thread).  The
+ * ring of two ranks runs the tree kernels (two operands fold to the same bits
+ * in either order).  The option VR_KERNEL_PATH (staged|register; see the top
+ * of this header) forces one of the two for testing and tuning; results are
  * identical.  Unaligned buffers run element units on the register kernel.
  * Errors (nothing enqueued): VR_ERR_INVALID_ARGUMENT for R outside
  * [1, VR_MAX_RANKS], NULL arrays, a NULL buffer with count > 0, a buffer not
@@ -448,8 +450,8 @@ vr_result_t vr_set_cost_model(const vr_cost_model_t* model);
  * same order, so results are unchanged.  Kernels are cached per architecture,
  * element type, op and set of trees; the first call with new trees compiles
  * them (about a second).  Without NVRTC, without the kernel sources beside
- * the library, or with the environment variable VR_JIT=0 (read per call),
- * the built-in interpreting kernels run. */
+ * the library, or with the option VR_JIT=0 (see the top of this header), the
+ * built-in interpreting kernels run. */
 
 /* Whether specialised trees are in use, and how many kernel sets were
  * compiled and failed to compile or load so far.  Errors:
@@ -483,7 +485,8 @@ vr_result_t vr_jit_compile_ring(int R, vr_dtype_t dtype, vr_op_t op, int smArch,
 /* Synchronises `stream`, then returns and clears the current device's status
  * word: VR_SUCCESS, or the first device-side error any kernel of this library
  * recorded since the last call (VR_ERR_TIMEOUT for a bounded wait that ran
- * out, VR_ERR_INTERNAL for a broken invariant), or VR_ERR_CUDA when the
+ * out, VR_ERR_INTERNAL for a broken invariant: in the bounds-checked build,
+ * an access outside the call's buffers, refused), or VR_ERR_CUDA when the
  * synchronisation itself fails.  The word is per device, not per stream. */
 vr_result_t vr_stream_status(void* stream);
 
