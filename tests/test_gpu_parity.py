@@ -182,6 +182,18 @@ def test_tree_bit_exact(R, L, count, nch, cb, dtype, path):
     assert_bits_equal(run_allreduce(inp, dtype, SUM, TREE, nch, cb, L), want)
 
 
+@pytest.mark.parametrize("algo", [RING, TREE])
+@pytest.mark.parametrize("R", [3, 5, 6, 7])
+def test_few_rank_geometry_at_32_mib(R, algo):
+    """2-7 ranks from 32 MiB per rank take the staged kernel with the
+    few-rank tile and stage table (the 6-rank ring keeps the register path):
+    every element equal to the oracle, with a ragged tail."""
+    count = (8 << 20) + 3
+    inp = workloads.generate(R, count, F32, "normal", 170 + R)
+    _, want = expect_allreduce(inp, F32, SUM, algo, 12, 512 * 1024)
+    assert_bits_equal(run_allreduce(inp, F32, SUM, algo, 12, 512 * 1024), want)
+
+
 @pytest.mark.parametrize("dtype", [F32, F16, BF16])
 @pytest.mark.parametrize("op", [SUM, MAX])
 def test_two_rank_ring_at_64_mib(dtype, op):
