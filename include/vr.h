@@ -28,8 +28,9 @@
  *     result only after synchronising the stream or through a stream-ordered
  *     dependency.
  *   - The library allocates no device buffers at run time.  Its own device
- *     state is static: one status word per device and the 8 MiB FIFO of
- *     vr_allreduce_ring_stepwise_noalloc (__device__ variables), plus the code
+ *     state is static: one status word and one bounds word per device and
+ *     the 8 MiB FIFO of vr_allreduce_ring_stepwise_noalloc (__device__
+ *     variables), plus the code
  *     of kernels compiled at run time (vr_jit_status) and, once
  *     vr_allreduce_host has run on a device, two streams and four events
  *     there.  vr_finalize releases what is not static.
