@@ -66,7 +66,8 @@
  *                                   stream drains; it waits for it before
  *                                   touching memory)
  *   VR_STAGED_MIN_BYTES=n           staged kernel from n bytes per rank
- *                                   (default 16 MiB)
+ *                                   (default 16 MiB; 2-7 ranks: from the
+ *                                   larger of n and 32 MiB)
  *   VR_STAGED_TILE_BYTES, VR_STAGED_STAGES, VR_STAGED_MIN_STAGES
  *                                   staged geometry: bytes per rank per
  *                                   tile, most stages, fewest stages
