@@ -76,6 +76,7 @@ _SIGNATURES = {
     "vr_stream_status": (I, [VP]),
     "vr_launch_count": (ctypes.c_ulonglong, []),
     "vr_debug_stall_next": (I, [ctypes.c_longlong]),
+    "vr_debug_sched_slot": (I, [VP, P(ctypes.c_ulonglong), I]),
     "vr_set_option": (I, [ctypes.c_char_p, ctypes.c_longlong]),
     "vr_debug_bounds_checked": (I, []),
     "vr_debug_shrink_next": (I, [ctypes.c_longlong, I]),
@@ -363,6 +364,15 @@ def vr_launch_count():
 
 def vr_debug_stall_next(tile):
     _check(_L().vr_debug_stall_next(tile), "vr_debug_stall_next")
+
+
+def vr_debug_sched_slot(stream=None, words=None):
+    """The four words of the tile scheduler slot of calls on ``stream``:
+    returned when ``words`` is None, else written (four integers)."""
+    buf = (ctypes.c_ulonglong * 4)(*(words or (0, 0, 0, 0)))
+    _check(_L().vr_debug_sched_slot(_stream(stream), buf, 0 if words is None else 1),
+           "vr_debug_sched_slot")
+    return tuple(buf)
 
 
 def vr_set_option(name, value):

@@ -10,6 +10,8 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <thread>
+#include <tuple>
 #include <utility>
 
 #include "host.h"
@@ -28,12 +30,17 @@ struct DeviceInfo {
   int smemOptin = 0;  // largest dynamic shared memory a CTA may opt into
   unsigned* status = nullptr;
   unsigned long long* boundsWhere = nullptr;  // first refused address (bounds-checked build)
+  unsigned long long* sched = nullptr;        // tile scheduler slots (kSchedSlots x 4 words)
 };
 std::map<int, DeviceInfo> g_devices;                             // by device ordinal
 std::map<std::pair<const void*, int>, int> g_occupancy;          // (kernel, device)
 std::map<std::pair<int, int>, std::array<FoldProg, 2>> g_progs;  // (nNodes, localRanks)
 std::map<std::pair<const void*, int>, int> g_smemSet;            // (kernel, device) -> bytes
 std::map<std::pair<const void*, int>, int> g_staticSmem;         // (kernel, device) -> bytes
+// Tile scheduler slots handed out: one per stream (per host thread for the
+// per-thread default stream) and one per launch captured into a graph.
+std::map<std::tuple<int, cudaStream_t, std::thread::id>, int> g_streamSlots;
+std::map<int, int> g_streamSlotsUsed, g_captureSlotsUsed;  // by device
 std::atomic<long long> g_stallNext{-1};                          // test hook
 std::atomic<long long> g_shrinkNext{0};                          // test hook (bounds-checked build)
 std::atomic<int> g_shrinkWhich{0};
@@ -87,7 +94,8 @@ vr_result_t device_info(DeviceInfo* out, int* device) {
         cudaDeviceGetAttribute(&d.l2Bytes, cudaDevAttrL2CacheSize, *device) != cudaSuccess)
       return VR_ERR_CUDA;
     if (status_word_address(&d.status) != cudaSuccess ||
-        bounds_word_address(&d.boundsWhere) != cudaSuccess)
+        bounds_word_address(&d.boundsWhere) != cudaSuccess ||
+        sched_table_address(&d.sched) != cudaSuccess)
       return VR_ERR_CUDA;
     it = g_devices.emplace(*device, d).first;
   }
@@ -215,11 +223,11 @@ bool aligned16(const void* const* p, int R, size_t extraStride) {
   return true;
 }
 
-const void* pick_staged(int dtype, int mode, int op, int stack = 0) {
+const void* pick_staged(int dtype, int mode, int op, int stack = 0, bool drawn = false) {
   switch (dtype) {
-    case VR_FLOAT32: return staged_kernel_ptr_f32(mode, op, stack);
-    case VR_FLOAT16: return staged_kernel_ptr_f16(mode, op, stack);
-    case VR_BFLOAT16: return staged_kernel_ptr_bf16(mode, op, stack);
+    case VR_FLOAT32: return staged_kernel_ptr_f32(mode, op, stack, drawn);
+    case VR_FLOAT16: return staged_kernel_ptr_f16(mode, op, stack, drawn);
+    case VR_BFLOAT16: return staged_kernel_ptr_bf16(mode, op, stack, drawn);
     default: return nullptr;
   }
 }
@@ -364,6 +372,50 @@ unsigned staged_tile_bytes(int R, int mode) {
   if (mode == kReduceScatter) return std::min(16384u, (65536u / (unsigned)R) & ~15u);
   if (R < 8 && small_geometry(mode, R).tile) return small_geometry(mode, R).tile;
   return R > 8 && R <= 16 ? 4096u : 2048u;
+}
+
+// The tile scheduler slot of a staged tree launch on `stream` (staged.cuh):
+// the stream's own slot, or a fresh one for a launch being captured into a
+// graph (each captured launch runs as its own graph node, whose replays CUDA
+// runs one after another); -1 when none is left or the stream's capture
+// state cannot be read -- the launch then splits its tiles in fixed runs.
+int sched_slot(int device, void* stream) {
+  const cudaStream_t s = (cudaStream_t)stream;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  std::lock_guard<std::mutex> g(g_mu);
+  if (cap == cudaStreamCaptureStatusActive) {
+    int& used = g_captureSlotsUsed[device];
+    if (used >= kSchedSlots - kSchedStreamSlots) return -1;
+    return kSchedStreamSlots + used++;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return -1;
+  const std::thread::id tid = s == cudaStreamPerThread ? std::this_thread::get_id()
+                                                        : std::thread::id();
+  const auto key = std::make_tuple(device, s, tid);
+  auto it = g_streamSlots.find(key);
+  if (it != g_streamSlots.end()) return it->second;
+  int& used = g_streamSlotsUsed[device];
+  if (used >= kSchedStreamSlots) return -1;
+  g_streamSlots.emplace(key, used);
+  return used++;
+}
+
+// Whether a staged tree of R ranks draws its tiles at run time (VR_SCHED=1).
+// Measured against fixed runs on one GB300: 1-4 % faster for 4-7 ranks
+// (32-256 MiB per rank), 12-16 % for 9-16 (4 KB tiles), 10-12 % for 17-64;
+// 9 % slower for 2 and 3 ranks, and 7-10 % slower for 8, the one geometry
+// with both 2 KB tiles and a deep pipeline (13 stages): the SMs' rates stay
+// even there, and each tile's drawn index costs its consumers a shared-memory
+// round trip on one unit of work per thread.
+bool sched_tiles(int R) {
+  const long long o = option(kOptSched);
+  if (o == 0) return false;
+  if (o >= 2) return true;
+  return R >= 4 && R != 8;
 }
 
 // Staged geometry: tiles of tileUnits 16-byte units per rank; as many stages
@@ -526,10 +578,22 @@ vr_result_t launch_allreduce_range(KArgs& a, int dtype, int mode, int op, int st
   // when they can be had (jit.cc), else the interpreting ones.
   // (The specialised register-path kernel measured slower than the
   // interpreting one at 64 ranks: above 32 only the staged one is used.)
+  // A staged tree draws its tiles through its stream's scheduler slot
+  // where that measured faster (staged.cuh).
+  a.sched = nullptr;
+  if (staged && mode == kTreeAllReduce && sched_tiles(a.R)) {
+    DeviceInfo di;
+    int device = 0;
+    const vr_result_t e = device_info(&di, &device);
+    if (e != VR_SUCCESS) return e;
+    const int slot = sched_slot(device, stream);
+    if (slot >= 0) a.sched = di.sched + 4 * (size_t)slot;
+  }
+  const bool drawn = a.sched != nullptr;
   const void* special = nullptr;
   if (mode == kTreeAllReduce && vec && (staged || a.R <= 32) && jit_enabled() &&
       jit_tree_kernel(dtype, op, stack, use_small(dtype, mode, vec, stack, a.R, bytes), staged,
-                      a.prog, a.nProgs, &special) != VR_SUCCESS)
+                      a.prog, a.nProgs, &special, 0, drawn) != VR_SUCCESS)
     special = nullptr;
   // The ring specialised for R ranks: measured 6-12% faster on the register
   // path for 3-16 ranks, neutral on the staged one (VR_JIT_RING=1 also takes
@@ -544,7 +608,7 @@ vr_result_t launch_allreduce_range(KArgs& a, int dtype, int mode, int op, int st
     a.unitLo = lo * E / 16;
     a.unitsAll = (hi * E + 15) / 16;
     a.unitsFull = hi * E / 16;
-    return launch_staged(special ? special : pick_staged(dtype, mode, op, stack), a, mode,
+    return launch_staged(special ? special : pick_staged(dtype, mode, op, stack, drawn), a, mode,
                          stream);
   }
   const long long NV = vec ? kGrainBytes / E : 1;
@@ -1099,6 +1163,28 @@ vr_result_t vr_debug_shrink_next(long long bytes, int which) {
 vr_result_t vr_debug_stall_next(long long tile) {
   if (tile < -1) return VR_ERR_INVALID_ARGUMENT;
   g_stallNext.store(tile);
+  return VR_SUCCESS;
+}
+
+vr_result_t vr_debug_sched_slot(void* stream, unsigned long long* words, int write) {
+  if (!words) return VR_ERR_INVALID_ARGUMENT;
+  DeviceInfo di;
+  int device = 0;
+  vr_result_t e = device_info(&di, &device);
+  if (e != VR_SUCCESS) return e;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing((cudaStream_t)stream, &cap) != cudaSuccess ||
+      cap != cudaStreamCaptureStatusNone)
+    return VR_ERR_INVALID_ARGUMENT;
+  const int slot = sched_slot(device, stream);
+  if (slot < 0) return VR_ERR_UNSUPPORTED;
+  unsigned long long* p = di.sched + 4 * (size_t)slot;
+  const cudaStream_t s = (cudaStream_t)stream;
+  const cudaError_t c = write ? cudaMemcpyAsync(p, words, 4 * sizeof(*words),
+                                                cudaMemcpyHostToDevice, s)
+                              : cudaMemcpyAsync(words, p, 4 * sizeof(*words),
+                                                cudaMemcpyDeviceToHost, s);
+  if (c != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return VR_ERR_CUDA;
   return VR_SUCCESS;
 }
 

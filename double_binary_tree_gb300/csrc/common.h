@@ -25,6 +25,10 @@ constexpr int kStagedMaxStages = 16; // shared-memory stages of a staged kernel
 constexpr int kStagedMaxConsumers = 7;  // its consumer warps (8 warps per CTA: 2 per SM sub-partition)
 constexpr int kStagedHeader = 4096;  // its barriers, flags, pointer tables and programs
 constexpr int kMaxProgs = 16;        // distinct tree fold programs per call
+// Tile scheduler slots (staged.cuh): 4 words each, one slot per stream and
+// one per launch captured into a graph.
+constexpr int kSchedSlots = 4096;
+constexpr int kSchedStreamSlots = 1024;  // slots [0, 1024) serve streams, the rest captures
 
 // A tree's reduction order as a stream of rank loads.  Slot i loads rank
 // rank[i]; before it, ctl[i] & 15 "pop-add" steps fold the top partial into
@@ -73,6 +77,9 @@ struct KArgs {
   // the device word that records the first access outside them.
   unsigned long long srcBytes, dstBytes, scratchBytes;
   unsigned long long* boundsWhere;
+  // Staged tree AllReduce: this launch's tile scheduler slot (tiles drawn at
+  // run time), or null (every CTA takes a fixed run of tiles).
+  unsigned long long* sched;
   // TMA-staged kernels (staged.cuh)
   long long unitLo;     // AllReduce: first 16-byte unit of the range
   long long unitsAll;   // AllReduce: end unit of the range, a trailing partial one included

@@ -26,6 +26,7 @@ enum Option : int {
   kOptAgStages,        // -1: gather_stages()
   kOptAgCtas,          // -1: gather_ctas_per_sm()
   kOptAgOrder,         // 0 by source size, 1 source-major, 2 destination-major
+  kOptSched,           // staged trees' tiles: 0 fixed runs, 1 drawn where faster, 2 always drawn
   kOptDebug,           // bit set of kDebug* subsystems
   kOptCount
 };
@@ -60,13 +61,14 @@ vr_result_t compile_fold(const vr_tree_t* tree, int R, FoldProg* prog);
 vr_result_t dtree_programs(int nNodes, int L, FoldProg out[2]);
 
 // Tree kernel specialised at run time for a call's fold programs (jit.cc):
-// the shared-memory-staged one when `staged`, else the register-path one
-// (16-byte units; the few-rank variant when `small`; compiled for at least
-// `minBlocks` resident CTAs per SM when it is above 0).
+// the shared-memory-staged one when `staged` (drawing its tiles through
+// KArgs::sched when `drawn`), else the register-path one (16-byte units; the
+// few-rank variant when `small`; compiled for at least `minBlocks` resident
+// CTAs per SM when it is above 0).
 bool jit_enabled();
 vr_result_t jit_tree_kernel(int dtype, int op, int stack, bool small, bool staged,
                             const FoldProg* progs, int nProgs, const void** out,
-                            int minBlocks = 0);
+                            int minBlocks = 0, bool drawn = false);
 // The ring AllReduce kernel specialised for R ranks (the same variants).
 vr_result_t jit_ring_kernel(int dtype, int op, int R, bool small, bool staged, const void** out,
                             int minBlocks = 0);
@@ -92,9 +94,10 @@ const void* kernel_ptr_allgather_tma_dest(int tile, int stages);
 int gather_tile_bytes();
 int gather_stages();
 int gather_ctas_per_sm();
-const void* staged_kernel_ptr_f32(int mode, int op, int stack);
-const void* staged_kernel_ptr_f16(int mode, int op, int stack);
-const void* staged_kernel_ptr_bf16(int mode, int op, int stack);
+// `drawn` (trees): the variant whose CTAs draw tiles through KArgs::sched.
+const void* staged_kernel_ptr_f32(int mode, int op, int stack, bool drawn);
+const void* staged_kernel_ptr_f16(int mode, int op, int stack, bool drawn);
+const void* staged_kernel_ptr_bf16(int mode, int op, int stack, bool drawn);
 
 // Non-fused variants (kernels_ablation.cu).
 enum AblationKernel : int { kTreeUp = 0, kTreeDown = 1, kRingStep = 2, kCopyRanks = 3 };
@@ -107,5 +110,7 @@ cudaError_t read_and_clear_status(unsigned* value);
 // address: its address, and read-and-clear.
 cudaError_t bounds_word_address(unsigned long long** p);
 cudaError_t read_and_clear_bounds(unsigned long long* value);
+// The current device's tile scheduler slots (kSchedSlots x 4 words).
+cudaError_t sched_table_address(unsigned long long** p);
 
 }  // namespace vr

@@ -247,6 +247,7 @@ std::string cache_key(int arch, int dtype, int op, int stack, bool small, const 
 // Compiles the register-path and staged tree kernels of `progs` for sm_<arch>a
 // into a CUBIN.  Returns the lowered names in `names`.
 // mode: kTreeAllReduce (progs, nProgs, stack) or kRingAllReduce (R).
+// kind: 0 register path, 1 staged, 2 staged drawing its tiles (trees).
 bool compile(int arch, int dtype, int op, int mode, int stack, bool small, int kind,
              const FoldProg* progs, int nProgs, int R, int minBlocks, std::string* cubin,
              std::string* name, std::string* log) {
@@ -267,7 +268,7 @@ bool compile(int arch, int dtype, int op, int mode, int stack, bool small, int k
       kind == 0 ? std::string("vr::allreduce_kernel<") + T + ", " + std::to_string(op) + ", " +
                       M + ", true, " + std::to_string(S) + (small ? ", true>" : ", false>")
                 : std::string("vr::staged_kernel<") + T + ", " + std::to_string(op) + ", " + M +
-                      ", " + std::to_string(S) + ">";
+                      ", " + std::to_string(S) + (kind == 2 ? ", true>" : ">");
   nvrtcProgram prog;
   if (n.create(&prog, src.c_str(), "vr_jit_tree.cu", 0, nullptr, nullptr) != NVRTC_SUCCESS)
     return false;
@@ -310,14 +311,14 @@ namespace {
 
 // The compiled kernel for `key`, compiling and loading it on first use.
 vr_result_t cached_kernel(const std::string& key, int dtype, int op, int mode, int stack,
-                          bool small, bool staged, const FoldProg* progs, int nProgs, int R,
+                          bool small, int kind, const FoldProg* progs, int nProgs, int R,
                           int minBlocks, int arch, const void** out) {
   std::lock_guard<std::mutex> g(g_jitMu);
   auto it = g_cache.find(key);
   if (it == g_cache.end()) {
     Entry e;
     std::string cubin, name;
-    if (compile(arch, dtype, op, mode, stack, small, staged ? 1 : 0, progs, nProgs, R, minBlocks,
+    if (compile(arch, dtype, op, mode, stack, small, kind, progs, nProgs, R, minBlocks,
                 &cubin, &name, nullptr) &&
         cudaLibraryLoadData(&e.lib, cubin.data(), nullptr, nullptr, 0, nullptr, nullptr, 0) ==
             cudaSuccess)
@@ -344,15 +345,17 @@ vr_result_t device_arch(int* arch) {
 }  // namespace
 
 vr_result_t jit_tree_kernel(int dtype, int op, int stack, bool small, bool staged,
-                            const FoldProg* progs, int nProgs, const void** out, int minBlocks) {
+                            const FoldProg* progs, int nProgs, const void** out, int minBlocks,
+                            bool drawn) {
   int arch = 0;
   const vr_result_t e = device_arch(&arch);
   if (e != VR_SUCCESS) return e;
   small = small && !staged;
   if (staged) minBlocks = 0;
-  const std::string key = std::string(staged ? "t1/" : "t0/") + std::to_string(minBlocks) + "/" +
+  const int kind = staged ? (drawn ? 2 : 1) : 0;
+  const std::string key = "t" + std::to_string(kind) + "/" + std::to_string(minBlocks) + "/" +
                           cache_key(arch, dtype, op, stack, small, progs, nProgs);
-  return cached_kernel(key, dtype, op, kTreeAllReduce, stack, small, staged, progs, nProgs, 0,
+  return cached_kernel(key, dtype, op, kTreeAllReduce, stack, small, kind, progs, nProgs, 0,
                        minBlocks, arch, out);
 }
 
@@ -366,7 +369,7 @@ vr_result_t jit_ring_kernel(int dtype, int op, int R, bool small, bool staged,
   const std::string key = std::string(staged ? "r1/" : "r0/") + std::to_string(minBlocks) + "/" +
                           std::to_string(arch) + "/" + std::to_string(dtype) + "/" +
                           std::to_string(op) + "/" + std::to_string(R) + (small ? "/s" : "/g");
-  return cached_kernel(key, dtype, op, kRingAllReduce, 0, small, staged, nullptr, 0, R,
+  return cached_kernel(key, dtype, op, kRingAllReduce, 0, small, staged ? 1 : 0, nullptr, 0, R,
                        minBlocks, arch, out);
 }
 
@@ -376,8 +379,9 @@ void jit_counts(long long* compiled, long long* failed) {
   *failed = g_failed;
 }
 
-// Compile-only check of the double binary tree of (nNodes, localRanks): no
-// device is touched.  The compiler's log goes to `log` (truncated).
+// Compile-only check of the double binary tree of (nNodes, localRanks), all
+// three kernel kinds: no device is touched.  The compiler's log goes to
+// `log` (truncated).
 vr_result_t jit_compile_dtree(int nNodes, int L, int dtype, int op, int arch,
                               size_t* cubinBytes, char* log, size_t logBytes) {
   FoldProg p[2];
@@ -385,15 +389,19 @@ vr_result_t jit_compile_dtree(int nNodes, int L, int dtype, int op, int arch,
   if (e != VR_SUCCESS) return e;
   const int stack = p[0].depth > p[1].depth ? p[0].depth : p[1].depth;
   if (!nvrtc().ok || source_dir().empty()) return VR_ERR_UNSUPPORTED;
-  std::string cubin, name, text;
-  const bool ok = compile(arch, dtype, op, kTreeAllReduce, stack, false, 0, p, 2, 0, 0, &cubin,
-                          &name, &text);
-  if (log && logBytes) {
-    std::strncpy(log, text.c_str(), logBytes - 1);
-    log[logBytes - 1] = 0;
+  std::string text;
+  *cubinBytes = 0;
+  for (int kind = 0; kind < 3; ++kind) {
+    std::string cubin, name;
+    const bool ok = compile(arch, dtype, op, kTreeAllReduce, stack, false, kind, p, 2, 0, 0,
+                            &cubin, &name, &text);
+    if (log && logBytes) {
+      std::strncpy(log, text.c_str(), logBytes - 1);
+      log[logBytes - 1] = 0;
+    }
+    if (!ok) return VR_ERR_INTERNAL;
+    *cubinBytes += cubin.size();
   }
-  if (!ok) return VR_ERR_INTERNAL;
-  *cubinBytes = cubin.size();
   return VR_SUCCESS;
 }
 

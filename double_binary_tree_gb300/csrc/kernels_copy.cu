@@ -11,6 +11,9 @@ __device__ unsigned g_status_word = 0;
 // First address the bounds-checked build refused on this device since it
 // was last read (0 = none).
 __device__ unsigned long long g_bounds_word = 0;
+// Tile scheduler slots of the staged tree kernels (staged.cuh), 4 words
+// each, all zero when free.
+__device__ unsigned long long g_sched[kSchedSlots * 4];
 
 const void* kernel_ptr_allgather(bool vec) {
   return vec ? (const void*)allgather_kernel<true> : (const void*)allgather_kernel<false>;
@@ -49,6 +52,10 @@ cudaError_t status_word_address(unsigned** p) {
 
 cudaError_t bounds_word_address(unsigned long long** p) {
   return cudaGetSymbolAddress(reinterpret_cast<void**>(p), g_bounds_word);
+}
+
+cudaError_t sched_table_address(unsigned long long** p) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(p), g_sched);
 }
 
 cudaError_t read_and_clear_bounds(unsigned long long* value) {

@@ -29,11 +29,14 @@ const void* kernel_ptr_f16(int mode, int op, bool vec, int stack, bool /*small*/
 }
 
 // TMA-staged kernels (16-byte aligned buffers only).
-const void* staged_kernel_ptr_f16(int mode, int op, int stack) {
+const void* staged_kernel_ptr_f16(int mode, int op, int stack, bool drawn) {
 #define VR_PICK(OP)                                                                       \
   switch (mode) {                                                                         \
     case kRingAllReduce: return (const void*)staged_kernel<__half, OP, kRingAllReduce, 4>;  \
     case kTreeAllReduce:                                                                  \
+      if (drawn)                                                                          \
+        return stack <= 4 ? (const void*)staged_kernel<__half, OP, kTreeAllReduce, 4, true>     \
+                          : (const void*)staged_kernel<__half, OP, kTreeAllReduce, 8, true>;    \
       return stack <= 4 ? (const void*)staged_kernel<__half, OP, kTreeAllReduce, 4>          \
                         : (const void*)staged_kernel<__half, OP, kTreeAllReduce, 8>;         \
     case kReduceScatter: return (const void*)staged_kernel<__half, OP, kReduceScatter, 4>;  \

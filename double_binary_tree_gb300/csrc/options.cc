@@ -26,7 +26,8 @@ const Spec kSpecs[kOptCount] = {
     {"VR_STAGED_TILE_BYTES", 0},  {"VR_STAGED_MIN_STAGES", -1},
     {"VR_STAGED_STAGES", 0},      {"VR_AG_TILE", -1},
     {"VR_AG_STAGES", -1},         {"VR_AG_CTAS", -1},
-    {"VR_AG_ORDER", 0},           {"VR_DEBUG", 0},
+    {"VR_AG_ORDER", 0},           {"VR_SCHED", 1},
+    {"VR_DEBUG", 0},
 };
 
 std::atomic<long long> g_values[kOptCount];

@@ -96,6 +96,65 @@ __device__ __forceinline__ void raise_error(unsigned* status, volatile int* abor
   *abort = 1;
 }
 
+// ------------------------------------------------------------ tile scheduler
+// A staged tree AllReduce given a scheduler slot (KArgs::sched) does not cut
+// the message into one fixed run of tiles per CTA: its producers draw tiles
+// from a counter, so that CTAs on SMs that drain faster take more of them.
+// With few pipeline stages (many ranks, or few ranks with large tiles) the
+// SMs' rates differ by up to a fifth within one launch, and a fixed split
+// waits for the slowest.
+//
+// A slot is four words of global memory: the owning launch (its %gridid,
+// which is the same for every CTA of one launch and for every replay of one
+// instantiated graph node, and differs between concurrent launches), the next
+// tile, and the counts of CTAs that joined and left (32 bits each).  The host
+// gives each stream its own slot and each launch captured into a graph a
+// slot of its own, so that the launches sharing a slot run one after the
+// other; the owner word checks it.  A producer joins after the previous
+// kernel on the stream has finished (pdl_wait), and the last CTA to leave
+// clears the slot for the next launch.  A slot held by another launch is
+// waited for, bounded: a CTA that cannot join reports VR_ERR_TIMEOUT and
+// takes no tile; one that finds more joins than the grid has CTAs (a slot
+// left behind by an execution of this launch that did not complete) reports
+// VR_ERR_INTERNAL and takes none.
+constexpr long long kSchedChunkBytes = 64 << 10;  // traffic of the tiles of one draw
+
+__device__ __forceinline__ unsigned long long grid_id() {
+  unsigned long long g;
+  asm volatile("mov.u64 %0, %%gridid;" : "=l"(g));
+  return g | (1ull << 63);  // never 0, the free slot's owner
+}
+
+// Lane 0 of a producer warp: VR_SUCCESS once this CTA has joined the slot.
+__device__ __forceinline__ unsigned sched_join(unsigned long long* slot, unsigned ctas,
+                                               unsigned long long limit_ns) {
+  const unsigned long long gid = grid_id();
+  unsigned long long t0 = 0;
+  for (unsigned it = 0;; ++it) {
+    const unsigned long long prev = atomicCAS(slot, 0ull, gid);
+    if (prev == 0ull || prev == gid) break;
+    const unsigned long long now = global_ns();
+    if (it == 0) t0 = now;
+    else if (now - t0 > limit_ns) return VR_ERR_TIMEOUT;
+    __nanosleep(256);
+  }
+  __threadfence();  // the previous owner's clearing is seen before the counter is used
+  return atomicAdd(reinterpret_cast<unsigned*>(slot + 2), 1u) < ctas ? VR_SUCCESS
+                                                                     : VR_ERR_INTERNAL;
+}
+
+// Lane 0 of a producer warp that joined, after its last draw: the last CTA
+// to leave clears the counters, then frees the slot.
+__device__ __forceinline__ void sched_leave(unsigned long long* slot, unsigned ctas) {
+  __threadfence();
+  if (atomicAdd(reinterpret_cast<unsigned*>(slot + 2) + 1, 1u) == ctas - 1) {
+    atomicExch(slot + 1, 0ull);
+    atomicExch(slot + 2, 0ull);
+    __threadfence();
+    atomicExch(slot, 0ull);
+  }
+}
+
 // Tile i of a CTA's work: the byte offset of its slice inside each source
 // rank's buffer, the bytes the producer copies, and the units it covers.
 // AllReduce: every CTA owns a run [cub, cue) of whole tiles of the message
@@ -135,7 +194,9 @@ __device__ __forceinline__ TileGeom tile_geom(const KArgs& a, long long t, long 
   return g;
 }
 
-template <typename T, int OP, int MODE, int S>
+// DRAWN (trees only): the CTAs draw their tiles through the scheduler slot
+// KArgs::sched instead of taking fixed runs.
+template <typename T, int OP, int MODE, int S, bool DRAWN = false>
 __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
     staged_kernel(const __grid_constant__ KArgs a) {
   constexpr int U = Ty<T>::U;
@@ -150,9 +211,14 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
   const char** s_src = reinterpret_cast<const char**>(smem + 16 * kStagedMaxStages + 16);
   char** s_dst = reinterpret_cast<char**>(smem + 16 * kStagedMaxStages + 16 + 8 * kMaxRanks);
   FoldProg* s_prog = reinterpret_cast<FoldProg*>(s_dst + kMaxRanks);
-  static_assert(16 * kStagedMaxStages + 16 + 16 * kMaxRanks + kMaxProgs * sizeof(FoldProg) <=
+  // the tile each stage holds, when tiles are drawn at run time (-1: no more)
+  volatile long long* s_tile = reinterpret_cast<volatile long long*>(s_prog + kMaxProgs);
+  static_assert(16 * kStagedMaxStages + 16 + 16 * kMaxRanks + kMaxProgs * sizeof(FoldProg) +
+                        8 * kStagedMaxStages <=
                     kStagedHeader,
                 "shared-memory header overflows");
+  static_assert((16 * kStagedMaxStages + 16 + 16 * kMaxRanks + kMaxProgs * sizeof(FoldProg)) % 8 ==
+                0, "tile slots misaligned");
   const uint32_t data = smem_addr(smem + kStagedHeader);
   const unsigned char* stage0 = smem + kStagedHeader;
   const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kStagedMaxStages);
@@ -183,11 +249,17 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
   pdl_wait();  // the previous kernel on the stream is done
 
   // this CTA's work: tiles [tb, tb + n) of the call (ReduceScatter), or the
-  // units [cub, cue), n tiles (AllReduce)
+  // units [cub, cue), n tiles (AllReduce); with a scheduler slot, the tiles
+  // of the whole range that its producer draws
   long long tb = 0, n = 0, cub = 0, cue = 0;
+  constexpr bool dyn = MODE == kTreeAllReduce && DRAWN;
   if constexpr (MODE == kReduceScatter) {
     tb = udiv(a.tiles * blockIdx.x, gridDim.x);
     n = udiv(a.tiles * (blockIdx.x + 1), gridDim.x) - tb;
+  } else if (dyn) {
+    cub = a.unitLo;
+    cue = a.unitsAll;
+    n = a.tiles;
   } else {
     // whole tiles per CTA, on the tile grid of the message: measured 0.5-1.5 %
     // faster than equal runs of units (R = 4, 8 and 64), whose copies do not
@@ -204,7 +276,22 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
     // ------------------------------------------------------------ producer
     const long long stallAt = blockIdx.x == 0 ? a.injectStall : -1;
     long long issued = 0;
-    for (long long i = 0; i < n; ++i) {
+    // run-time tiles: draws of K tiles, the next draw made when a draw's
+    // first tile is issued (lane 0 holds its result)
+    bool joined = false;
+    int sent = -1;  // the stage that carried the end mark to the consumers
+    long long K = 1, cb = 0, left = 0;
+    unsigned long long nb = 0;
+    if (dyn) {
+      unsigned e = VR_SUCCESS;
+      if (lane == 0) e = sched_join(a.sched, gridDim.x, a.timeoutNs);
+      e = __shfl_sync(~0u, e, 0);
+      joined = e == VR_SUCCESS;
+      if (!joined && lane == 0) raise_error(a.status, abort, e);  // the consumers leave too
+      K = max(1LL, kSchedChunkBytes / (2LL * R * TB));
+      if (joined && lane == 0) nb = atomicAdd(a.sched + 1, (unsigned long long)K);
+    }
+    for (long long i = 0; dyn || i < n; ++i) {
       const int s = (int)(i % NS);
       const long long k = i / NS;
       if (k > 0) {
@@ -216,8 +303,30 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
         }
       }
       if (__shfl_sync(~0u, *abort, 0)) break;
-      const TileGeom g = tile_geom<MODE>(a, tb + i, cub, cue);
-      if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * s, (unsigned)R * g.bytes);
+      long long t = tb + i;
+      if (dyn) {
+        if (left == 0) {
+          cb = (long long)__shfl_sync(~0u, nb, 0);
+          left = K;
+          if (cb < a.tiles && lane == 0) nb = atomicAdd(a.sched + 1, (unsigned long long)K);
+        }
+        t = cb + (K - left);
+        --left;
+        if (t >= a.tiles) {  // none left: the consumers stop at this stage
+          if (lane == 0) {
+            s_tile[s] = -1;
+            mbar_arrive(full0 + 8 * s);
+          }
+          __syncwarp();
+          sent = s;
+          break;
+        }
+      }
+      const TileGeom g = tile_geom<MODE>(a, t, cub, cue);
+      if (lane == 0) {
+        if (dyn) s_tile[s] = t;
+        mbar_arrive_expect_tx(full0 + 8 * s, (unsigned)R * g.bytes);
+      }
       __syncwarp();
       issued = i + 1;
       if (i == stallAt) continue;  // test hook: this fill never lands
@@ -226,13 +335,16 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
           bulk_load(data + s * stageBytes + r * TB, s_src[r] + g.srcOff, g.bytes, full0 + 8 * s);
     }
     // Drain: every copy issued must have landed before the CTA may exit.
+    // (The stage that carried the end mark was waited for as empty, so its
+    // last copies have landed; its barrier has moved a phase past them.)
     for (int s = 0; s < NS && s < issued; ++s) {
       const long long last = s + ((issued - 1 - s) / NS) * NS;  // last tile index of stage s
-      if (last == stallAt) continue;
+      if (last == stallAt || s == sent) continue;
       const bool ok = __any_sync(
           ~0u, wait_phase(full0 + 8 * s, (unsigned)((last / NS) & 1), abort, false, a.timeoutNs));
       if (!ok && lane == 0) raise_error(a.status, abort, VR_ERR_TIMEOUT);
     }
+    if (joined && lane == 0) sched_leave(a.sched, gridDim.x);
     return;
   }
 
@@ -244,7 +356,7 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
   const int ct = threadIdx.x - kWarpSize;
   const int nct = kWarpSize * NC;
   Cursor cur{0, -1, 0, 0, 0, 0, 0};
-  for (long long i = 0; i < n; ++i) {
+  for (long long i = 0; dyn || i < n; ++i) {
     const int s = (int)(i % NS);
     const bool ok =
         __any_sync(~0u, wait_phase(full0 + 8 * s, (unsigned)((i / NS) & 1), abort, true, a.timeoutNs));
@@ -252,7 +364,12 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
       if (lane == 0 && !*abort) raise_error(a.status, abort, VR_ERR_TIMEOUT);
       break;
     }
-    const TileGeom g = tile_geom<MODE>(a, tb + i, cub, cue);
+    long long t = tb + i;
+    if (dyn) {
+      t = s_tile[s];
+      if (t < 0) break;
+    }
+    const TileGeom g = tile_geom<MODE>(a, t, cub, cue);
     const unsigned char* base = stage0 + (size_t)s * stageBytes;
     for (int lu = ct; lu < g.units; lu += nct) {
       if constexpr (MODE == kReduceScatter) {
@@ -296,7 +413,8 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
   // read from global memory, go to different consumer threads of the CTA
   // that owns it, so their loads are not waited for in turn.
   if constexpr (MODE != kReduceScatter) {
-    if (cue == a.unitsAll && a.unitsAll > a.unitsFull && ct < a.hi - a.unitsFull * U) {
+    if ((dyn ? blockIdx.x == 0 : cue == a.unitsAll) && a.unitsAll > a.unitsFull &&
+        ct < a.hi - a.unitsFull * U) {
       const long long e = a.unitsFull * U + ct;
       const GlobalSrc src{s_src, e * E};
       const typename Ty<T>::Bits o = fold_element<T, OP, MODE, S>(a, src, s_prog, e, cur);

@@ -83,6 +83,22 @@
  *                                   re-read from L2); by default
  *                                   destination-major when the R sources
  *                                   take at most a quarter of L2
+ *   VR_SCHED=0|1|2                  staged tree AllReduce: 0 every CTA
+ *                                   takes a fixed run of tiles; 1
+ *                                   (default) the CTAs draw tiles at run
+ *                                   time where that measured faster (4 or
+ *                                   more ranks, 8 excepted); 2 always drawn.
+ *                                   Drawing uses a scheduler slot in
+ *                                   device memory per stream, and one per
+ *                                   launch captured into a graph: launches
+ *                                   on one stream, and the replays of one
+ *                                   instantiated graph, run one after
+ *                                   another.  Two instances of one captured
+ *                                   graph running at the same time share
+ *                                   the captured launch's slot; the later
+ *                                   one's CTAs wait (bounded) and report
+ *                                   VR_ERR_TIMEOUT if it stays held.
+ *                                   The same bits either way.
  *   VR_DEBUG=GRAPH                  print every tree set, ring and channel
  *                                   partition a call plans to stderr, in
  *                                   the log formats of [Course13] "从 GRAPH
@@ -462,7 +478,8 @@ vr_result_t vr_jit_status(int* enabled, long long* compiled, long long* failed);
 
 /* Compiles, without loading or touching a device, the specialised kernels of
  * vr_build_dtree(nNodes, localRanks, 2)'s two trees for sm_<smArch>a (e.g.
- * 103) and returns the CUBIN size; the compiler log, if any, goes to `log`
+ * 103) -- register path, staged, staged drawing its tiles (VR_SCHED) -- and
+ * returns their total CUBIN size; the compiler log, if any, goes to `log`
  * (logBytes, NUL-terminated, may be NULL / 0).  Errors:
  * VR_ERR_INVALID_ARGUMENT for bad sizes, dtype, op or smArch < 90;
  * VR_ERR_UNSUPPORTED when NVRTC or the kernel sources are not found;
@@ -506,6 +523,18 @@ unsigned long long vr_launch_count(void);
  * VR_ERR_TIMEOUT; the stream and the context stay usable.  -1 cancels a
  * pending request.  Errors: VR_ERR_INVALID_ARGUMENT for tile < -1. */
 vr_result_t vr_debug_stall_next(long long tile);
+
+/* Test hook for the tile scheduler of the staged tree kernels (see
+ * VR_SCHED): reads (write = 0) or writes (write != 0) the four words of the
+ * scheduler slot that calls on `stream` use -- owner (0 when free), next
+ * tile, and the CTAs that joined (low 32 bits) and left (high 32 bits) --
+ * through a copy on `stream`, which is then synchronised.  A slot whose owner
+ * is set to a value no launch has makes the next call's CTAs wait for it
+ * (bounded) and report VR_ERR_TIMEOUT; writing four zeros frees it.
+ * `words` is host memory of 4 elements.  Errors: VR_ERR_INVALID_ARGUMENT
+ * (null words, or a stream being captured), VR_ERR_UNSUPPORTED (no slot
+ * left for a new stream), VR_ERR_CUDA. */
+vr_result_t vr_debug_sched_slot(void* stream, unsigned long long* words, int write);
 
 /* Sets one of the options listed at the top of this header for the rest of
  * the process (all threads, all devices); value -1 restores the built-in

@@ -532,6 +532,8 @@ def test_options_set_get_and_restore():
     vr.vr_set_option("VR_STAGED_TILE_BYTES", -1)      # the built-in default
     assert vr.vr_get_option("VR_STAGED_TILE_BYTES") == 0
     vr.vr_set_option("VR_STAGED_TILE_BYTES", old)
+    if "VR_SCHED" not in os.environ:
+        assert vr.vr_get_option("VR_SCHED") == 1          # tiles drawn where faster
     for bad in (("VR_NO_SUCH_OPTION", 1), ("VR_PDL", -2)):
         with pytest.raises(vr.VrError) as e:
             vr.vr_set_option(*bad)
