@@ -374,7 +374,7 @@ unsigned staged_tile_bytes(int R, int mode) {
   return R > 8 && R <= 16 ? 4096u : 2048u;
 }
 
-// The tile scheduler slot of a staged tree launch on `stream` (staged.cuh):
+// The tile scheduler slot of a staged AllReduce launch on `stream` (staged.cuh):
 // the stream's own slot, or a fresh one for a launch being captured into a
 // graph (each captured launch runs as its own graph node, whose replays CUDA
 // runs one after another); -1 when none is left or the stream's capture
@@ -404,18 +404,21 @@ int sched_slot(int device, void* stream) {
   return used++;
 }
 
-// Whether a staged tree of R ranks draws its tiles at run time (VR_SCHED=1).
-// Measured against fixed runs on one GB300: 1-4 % faster for 4-7 ranks
-// (32-256 MiB per rank), 12-16 % for 9-16 (4 KB tiles), 10-12 % for 17-64;
-// 9 % slower for 2 and 3 ranks, and 7-10 % slower for 8, the one geometry
-// with both 2 KB tiles and a deep pipeline (13 stages): the SMs' rates stay
-// even there, and each tile's drawn index costs its consumers a shared-memory
-// round trip on one unit of work per thread.
-bool sched_tiles(int R) {
+// Whether a staged AllReduce of R ranks draws its tiles at run time
+// (VR_SCHED=1).  Measured against fixed runs on one GB300 (16-256 MiB per
+// rank): trees 1-5 % faster for 4-7 ranks, 12-16 % for 9-16 (4 KB tiles),
+// 10-12 % for 17-64; rings 12-15 % faster for 16-33 ranks, 8 % for 48 and
+// 1 % for 64 (whose fold, a loop over 64 rotated ranks in 3 consumer warps,
+// bounds it).  Slower: 2-3 rank trees (9 %), 8 ranks (trees 7-13 %, rings
+// 22 %: the one geometry with both 2 KB tiles and a deep pipeline, 13
+// stages, where the SMs' rates stay even and each tile's drawn index costs
+// the consumers a shared-memory round trip on one unit of work per thread),
+// and 9-12 rank rings (0-2 %); 3-7 rank rings are within 2 % either way.
+bool sched_tiles(int mode, int R) {
   const long long o = option(kOptSched);
   if (o == 0) return false;
   if (o >= 2) return true;
-  return R >= 4 && R != 8;
+  return mode == kTreeAllReduce ? R >= 4 && R != 8 : R >= 16;
 }
 
 // Staged geometry: tiles of tileUnits 16-byte units per rank; as many stages
@@ -578,10 +581,10 @@ vr_result_t launch_allreduce_range(KArgs& a, int dtype, int mode, int op, int st
   // when they can be had (jit.cc), else the interpreting ones.
   // (The specialised register-path kernel measured slower than the
   // interpreting one at 64 ranks: above 32 only the staged one is used.)
-  // A staged tree draws its tiles through its stream's scheduler slot
+  // A staged AllReduce draws its tiles through its stream's scheduler slot
   // where that measured faster (staged.cuh).
   a.sched = nullptr;
-  if (staged && mode == kTreeAllReduce && sched_tiles(a.R)) {
+  if (staged && sched_tiles(mode, a.R)) {
     DeviceInfo di;
     int device = 0;
     const vr_result_t e = device_info(&di, &device);
@@ -600,7 +603,7 @@ vr_result_t launch_allreduce_range(KArgs& a, int dtype, int mode, int op, int st
   // it there, 0 turns it off).
   const long long jr = option(kOptJitRing);
   if (mode == kRingAllReduce && vec && a.R >= 3 && a.R <= 16 && jr != 0 &&
-      (!staged || jr == 1) && jit_enabled() &&
+      (!staged || (jr == 1 && !drawn)) && jit_enabled() &&
       jit_ring_kernel(dtype, op, a.R, use_small(dtype, mode, vec, stack, a.R, bytes), staged,
                       &special) != VR_SUCCESS)
     special = nullptr;

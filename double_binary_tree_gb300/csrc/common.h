@@ -77,7 +77,7 @@ struct KArgs {
   // the device word that records the first access outside them.
   unsigned long long srcBytes, dstBytes, scratchBytes;
   unsigned long long* boundsWhere;
-  // Staged tree AllReduce: this launch's tile scheduler slot (tiles drawn at
+  // Staged AllReduce: this launch's tile scheduler slot (tiles drawn at
   // run time), or null (every CTA takes a fixed run of tiles).
   unsigned long long* sched;
   // TMA-staged kernels (staged.cuh)

@@ -94,7 +94,7 @@ const void* kernel_ptr_allgather_tma_dest(int tile, int stages);
 int gather_tile_bytes();
 int gather_stages();
 int gather_ctas_per_sm();
-// `drawn` (trees): the variant whose CTAs draw tiles through KArgs::sched.
+// `drawn` (AllReduce): the variant whose CTAs draw tiles through KArgs::sched.
 const void* staged_kernel_ptr_f32(int mode, int op, int stack, bool drawn);
 const void* staged_kernel_ptr_f16(int mode, int op, int stack, bool drawn);
 const void* staged_kernel_ptr_bf16(int mode, int op, int stack, bool drawn);

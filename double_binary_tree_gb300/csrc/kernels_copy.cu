@@ -11,7 +11,7 @@ __device__ unsigned g_status_word = 0;
 // First address the bounds-checked build refused on this device since it
 // was last read (0 = none).
 __device__ unsigned long long g_bounds_word = 0;
-// Tile scheduler slots of the staged tree kernels (staged.cuh), 4 words
+// Tile scheduler slots of the staged AllReduce kernels (staged.cuh), 4 words
 // each, all zero when free.
 __device__ unsigned long long g_sched[kSchedSlots * 4];
 

@@ -32,7 +32,9 @@ const void* kernel_ptr_f16(int mode, int op, bool vec, int stack, bool /*small*/
 const void* staged_kernel_ptr_f16(int mode, int op, int stack, bool drawn) {
 #define VR_PICK(OP)                                                                       \
   switch (mode) {                                                                         \
-    case kRingAllReduce: return (const void*)staged_kernel<__half, OP, kRingAllReduce, 4>;  \
+    case kRingAllReduce:                                                                  \
+      return drawn ? (const void*)staged_kernel<__half, OP, kRingAllReduce, 4, true>           \
+                   : (const void*)staged_kernel<__half, OP, kRingAllReduce, 4>;                \
     case kTreeAllReduce:                                                                  \
       if (drawn)                                                                          \
         return stack <= 4 ? (const void*)staged_kernel<__half, OP, kTreeAllReduce, 4, true>     \

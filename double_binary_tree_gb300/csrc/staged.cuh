@@ -38,6 +38,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, unsigned byt
                "r"(bytes)
                : "memory");
 }
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, unsigned bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -97,9 +101,9 @@ __device__ __forceinline__ void raise_error(unsigned* status, volatile int* abor
 }
 
 // ------------------------------------------------------------ tile scheduler
-// A staged tree AllReduce given a scheduler slot (KArgs::sched) does not cut
-// the message into one fixed run of tiles per CTA: its producers draw tiles
-// from a counter, so that CTAs on SMs that drain faster take more of them.
+// A staged AllReduce given a scheduler slot (KArgs::sched) does not cut the
+// message into one fixed run of tiles per CTA: its producers draw tiles from
+// a counter, so that CTAs on SMs that drain faster take more of them.
 // With few pipeline stages (many ranks, or few ranks with large tiles) the
 // SMs' rates differ by up to a fifth within one launch, and a fixed split
 // waits for the slowest.
@@ -119,6 +123,14 @@ __device__ __forceinline__ void raise_error(unsigned* status, volatile int* abor
 // VR_ERR_INTERNAL and takes none.
 constexpr long long kSchedChunkBytes = 64 << 10;  // traffic of the tiles of one draw
 
+// A drawn ring tile's place in the ring schedule, found by the producer (one
+// search per tile) and handed to the consumers with the tile: the ring
+// block of the tile's first element, that block's loop, and the loop's block
+// sizes.  The consumers step forwards from it inside the tile.
+struct RingMark {
+  long long lo, loopEnd, q;
+  int j, m;
+};
 __device__ __forceinline__ unsigned long long grid_id() {
   unsigned long long g;
   asm volatile("mov.u64 %0, %%gridid;" : "=l"(g));
@@ -194,7 +206,7 @@ __device__ __forceinline__ TileGeom tile_geom(const KArgs& a, long long t, long 
   return g;
 }
 
-// DRAWN (trees only): the CTAs draw their tiles through the scheduler slot
+// DRAWN (AllReduce): the CTAs draw their tiles through the scheduler slot
 // KArgs::sched instead of taking fixed runs.
 template <typename T, int OP, int MODE, int S, bool DRAWN = false>
 __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
@@ -211,10 +223,13 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
   const char** s_src = reinterpret_cast<const char**>(smem + 16 * kStagedMaxStages + 16);
   char** s_dst = reinterpret_cast<char**>(smem + 16 * kStagedMaxStages + 16 + 8 * kMaxRanks);
   FoldProg* s_prog = reinterpret_cast<FoldProg*>(s_dst + kMaxRanks);
-  // the tile each stage holds, when tiles are drawn at run time (-1: no more)
+  // the tile each stage holds, when tiles are drawn at run time (-1: no more),
+  // and a drawn ring tile's place in the ring schedule
   volatile long long* s_tile = reinterpret_cast<volatile long long*>(s_prog + kMaxProgs);
+  RingMark* s_mark = reinterpret_cast<RingMark*>(
+      const_cast<long long*>(s_tile + kStagedMaxStages));
   static_assert(16 * kStagedMaxStages + 16 + 16 * kMaxRanks + kMaxProgs * sizeof(FoldProg) +
-                        8 * kStagedMaxStages <=
+                        (8 + sizeof(RingMark)) * kStagedMaxStages <=
                     kStagedHeader,
                 "shared-memory header overflows");
   static_assert((16 * kStagedMaxStages + 16 + 16 * kMaxRanks + kMaxProgs * sizeof(FoldProg)) % 8 ==
@@ -252,7 +267,7 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
   // units [cub, cue), n tiles (AllReduce); with a scheduler slot, the tiles
   // of the whole range that its producer draws
   long long tb = 0, n = 0, cub = 0, cue = 0;
-  constexpr bool dyn = MODE == kTreeAllReduce && DRAWN;
+  constexpr bool dyn = MODE != kReduceScatter && DRAWN;
   if constexpr (MODE == kReduceScatter) {
     tb = udiv(a.tiles * blockIdx.x, gridDim.x);
     n = udiv(a.tiles * (blockIdx.x + 1), gridDim.x) - tb;
@@ -282,6 +297,7 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
     int sent = -1;  // the stage that carried the end mark to the consumers
     long long K = 1, cb = 0, left = 0;
     unsigned long long nb = 0;
+    Cursor pcur{0, -1, 0, 0, 0, 0, 0};  // drawn ring: lane 0's place in the schedule
     if (dyn) {
       unsigned e = VR_SUCCESS;
       if (lane == 0) e = sched_join(a.sched, gridDim.x, a.timeoutNs);
@@ -323,9 +339,14 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
         }
       }
       const TileGeom g = tile_geom<MODE>(a, t, cub, cue);
+      // (a drawn ring tile: the copies are issued first and the tile's mark
+      // found while they fly; the producer's arrival, after the mark, ends
+      // the stage's phase)
+      constexpr bool mark = dyn && MODE == kRingAllReduce;
       if (lane == 0) {
         if (dyn) s_tile[s] = t;
-        mbar_arrive_expect_tx(full0 + 8 * s, (unsigned)R * g.bytes);
+        if (mark) mbar_expect_tx(full0 + 8 * s, (unsigned)R * g.bytes);
+        else mbar_arrive_expect_tx(full0 + 8 * s, (unsigned)R * g.bytes);
       }
       __syncwarp();
       issued = i + 1;
@@ -333,6 +354,13 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
       if (g.bytes)
         for (int r = lane; r < R; r += kWarpSize)
           bulk_load(data + s * stageBytes + r * TB, s_src[r] + g.srcOff, g.bytes, full0 + 8 * s);
+      if constexpr (mark) {
+        if (lane == 0) {
+          seek<U, MODE>(a, g.u0 * U, pcur);
+          s_mark[s] = RingMark{pcur.lo, pcur.loopEnd, pcur.q, pcur.j, pcur.m};
+          mbar_arrive(full0 + 8 * s);
+        }
+      }
     }
     // Drain: every copy issued must have landed before the CTA may exit.
     // (The stage that carried the end mark was waited for as empty, so its
@@ -368,6 +396,15 @@ __global__ void __launch_bounds__(kWarpSize * (kStagedMaxConsumers + 1), 1)
     if (dyn) {
       t = s_tile[s];
       if (t < 0) break;
+    }
+    if constexpr (dyn && MODE == kRingAllReduce) {
+      const RingMark mk = s_mark[s];
+      cur.lo = mk.lo;
+      cur.j = mk.j;
+      cur.m = mk.m;
+      cur.q = mk.q;
+      cur.loopEnd = mk.loopEnd;
+      cur.hi = mk.lo + mk.q + (mk.j < mk.m ? 1 : 0);
     }
     const TileGeom g = tile_geom<MODE>(a, t, cub, cue);
     const unsigned char* base = stage0 + (size_t)s * stageBytes;

@@ -83,11 +83,12 @@
  *                                   re-read from L2); by default
  *                                   destination-major when the R sources
  *                                   take at most a quarter of L2
- *   VR_SCHED=0|1|2                  staged tree AllReduce: 0 every CTA
- *                                   takes a fixed run of tiles; 1
- *                                   (default) the CTAs draw tiles at run
- *                                   time where that measured faster (4 or
- *                                   more ranks, 8 excepted); 2 always drawn.
+ *   VR_SCHED=0|1|2                  staged AllReduce: 0 every CTA takes a
+ *                                   fixed run of tiles; 1 (default) the
+ *                                   CTAs draw tiles at run time where that
+ *                                   measured faster (trees of 4 or more
+ *                                   ranks, 8 excepted; rings of 16 or
+ *                                   more); 2 always drawn.
  *                                   Drawing uses a scheduler slot in
  *                                   device memory per stream, and one per
  *                                   launch captured into a graph: launches
@@ -524,7 +525,7 @@ unsigned long long vr_launch_count(void);
  * pending request.  Errors: VR_ERR_INVALID_ARGUMENT for tile < -1. */
 vr_result_t vr_debug_stall_next(long long tile);
 
-/* Test hook for the tile scheduler of the staged tree kernels (see
+/* Test hook for the tile scheduler of the staged AllReduce kernels (see
  * VR_SCHED): reads (write = 0) or writes (write != 0) the four words of the
  * scheduler slot that calls on `stream` use -- owner (0 when free), next
  * tile, and the CTAs that joined (low 32 bits) and left (high 32 bits) --

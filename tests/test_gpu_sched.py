@@ -1,7 +1,7 @@
-"""Run-time tile scheduling of the staged tree kernels (VR_SCHED).
+"""Run-time tile scheduling of the staged AllReduce kernels (VR_SCHED).
 
-A staged tree AllReduce may let its CTAs draw tiles from a counter in a
-scheduler slot instead of taking fixed runs.  Which CTA folds a tile never
+A staged AllReduce (tree or ring) may let its CTAs draw tiles from a counter
+in a scheduler slot instead of taking fixed runs.  Which CTA folds a tile never
 changes the tile's fold, so the results must be the oracle's bit for bit
 whichever way the tiles are shared out; the slot must be free again after
 every call; launches on two streams at once, and the replays of a captured
@@ -30,19 +30,19 @@ import double_binary_tree_gb300 as vr  # noqa: E402
 
 F32, F16, BF16 = vr.VR_FLOAT32, vr.VR_FLOAT16, vr.VR_BFLOAT16
 SUM, MAX = vr.VR_SUM, vr.VR_MAX
-TREE = vr.VR_ALGO_TREE
+RING, TREE = vr.VR_ALGO_RING, vr.VR_ALGO_TREE
 NCH, CB = 12, 512 * 1024
 FREE = (0, 0, 0, 0)
 HELD = 0xC000000000003039  # an owner no launch has (grid ids stay far below 2^62)
 
 
-def expected(inputs, dtype, op, L=1, nch=NCH, cb=CB):
+def expected(inputs, dtype, op, L=1, nch=NCH, cb=CB, algo=TREE):
     raws = [workloads.raw_numpy(t) for t in inputs]
-    return oracle.allreduce(raws, dtype, op, TREE, nch, cb, local_ranks=L)[0]
+    return oracle.allreduce(raws, dtype, op, algo, nch, cb, local_ranks=L)[0]
 
 
-def run(src, dst, R, count, dtype, op, L=1, stream=None, nch=NCH, cb=CB):
-    vr.vr_allreduce_ex(src, dst, R, count, dtype, op, TREE, nch, cb, L, stream)
+def run(src, dst, R, count, dtype, op, L=1, stream=None, nch=NCH, cb=CB, algo=TREE):
+    vr.vr_allreduce_ex(src, dst, R, count, dtype, op, algo, nch, cb, L, stream)
 
 
 def same_everywhere(dst):
@@ -68,18 +68,19 @@ FULL = [
 ]
 
 
+@pytest.mark.parametrize("algo", [TREE, RING])
 @pytest.mark.parametrize("R,count,dtype,op,L,dist", FULL)
-def test_drawn_tiles_are_the_oracle_and_the_fixed_split(R, count, dtype, op, L, dist):
+def test_drawn_tiles_are_the_oracle_and_the_fixed_split(R, count, dtype, op, L, dist, algo):
     inp = workloads.generate(R, count, dtype, dist, 700 + R)
     src = [t.cuda() for t in inp]
     dst = [torch.empty_like(s) for s in src]
     stream = torch.cuda.current_stream()
-    want = expected(inp, dtype, op, L)
+    want = expected(inp, dtype, op, L, algo=algo)
     for sched in (2, 0):
         with options(vr, VR_SCHED=sched):
             for d in dst:
                 d.zero_()
-            run(src, dst, R, count, dtype, op, L)
+            run(src, dst, R, count, dtype, op, L, algo=algo)
             assert vr.vr_stream_status(stream) == vr.VR_SUCCESS
             assert_exact(dst, want)
     assert vr.vr_debug_sched_slot(stream) == FREE
@@ -90,17 +91,34 @@ def test_drawn_tiles_are_the_oracle_and_the_fixed_split(R, count, dtype, op, L, 
 SMALL = [(3, 1000), (4, 4093), (7, 65536 + 5), (16, 3 * 4096 + 1), (33, 777), (64, 8192 + 3)]
 
 
+@pytest.mark.parametrize("algo", [TREE, RING])
 @pytest.mark.parametrize("R,count", SMALL)
 @pytest.mark.parametrize("dtype", [F32, BF16])
-def test_drawn_tiles_small_and_ragged(R, count, dtype):
+def test_drawn_tiles_small_and_ragged(R, count, dtype, algo):
     inp = workloads.generate(R, count, dtype, "normal", 800 + R)
     src = [t.cuda() for t in inp]
     dst = [torch.empty_like(s) for s in src]
     stream = torch.cuda.current_stream()
     with options(vr, VR_KERNEL_PATH="staged", VR_SCHED=2):
-        run(src, dst, R, count, dtype, SUM, nch=2, cb=4096)
+        run(src, dst, R, count, dtype, SUM, nch=2, cb=4096, algo=algo)
         assert vr.vr_stream_status(stream) == vr.VR_SUCCESS
-    assert_exact(dst, expected(inp, dtype, SUM, nch=2, cb=4096))
+    assert_exact(dst, expected(inp, dtype, SUM, nch=2, cb=4096, algo=algo))
+    assert vr.vr_debug_sched_slot(stream) == FREE
+
+
+@pytest.mark.parametrize("R,count,cb", [(16, (4 << 20) + 7, 4096), (5, (8 << 20) + 3, 1040)])
+def test_drawn_ring_tiles_across_many_blocks(R, count, cb):
+    """Ring blocks much smaller than a tile (small chunks): every drawn tile
+    crosses ring blocks and loops, and the consumers step through them from
+    the producer's mark."""
+    inp = workloads.generate(R, count, F32, "normal", 850 + R)
+    src = [t.cuda() for t in inp]
+    dst = [torch.empty_like(s) for s in src]
+    stream = torch.cuda.current_stream()
+    with options(vr, VR_KERNEL_PATH="staged", VR_SCHED=2):
+        run(src, dst, R, count, F32, SUM, nch=3, cb=cb, algo=RING)
+        assert vr.vr_stream_status(stream) == vr.VR_SUCCESS
+    assert_exact(dst, expected(inp, F32, SUM, nch=3, cb=cb, algo=RING))
     assert vr.vr_debug_sched_slot(stream) == FREE
 
 
