@@ -339,13 +339,37 @@ constexpr size_t kSmallStagedMinBytes = 32u << 20;  // per rank, 2-7 ranks
 // ranks and, with its fold specialised at run time (jit.cc), for the tree of
 // 8-64 ranks (the interpreting staged tree is 2-3x slower than the register
 // path); with 2-7 ranks it wins from 32 MiB per rank with the geometry above.
+// Whether a staged AllReduce of R ranks draws its tiles at run time
+// (VR_SCHED=1).  Measured against fixed runs on one GB300 (16-256 MiB per
+// rank): trees 1-5 % faster for 4-7 ranks, 12-16 % for 9-16 (4 KB tiles),
+// 10-12 % for 17-64; rings 12-15 % faster for 16-33 ranks, 8 % for 48 and
+// 1 % for 64 (whose fold, a loop over 64 rotated ranks in 3 consumer warps,
+// bounds it).  Slower: 2-3 rank trees (9 %), 8 ranks (trees 7-13 %, rings
+// 22 %: the one geometry with both 2 KB tiles and a deep pipeline, 13
+// stages, where the SMs' rates stay even and each tile's drawn index costs
+// the consumers a shared-memory round trip on one unit of work per thread),
+// and 9-12 rank rings (0-2 %); 3-7 rank rings are within 2 % either way.
+bool sched_tiles(int mode, int R) {
+  const long long o = option(kOptSched);
+  if (o == 0) return false;
+  if (o >= 2) return true;
+  return mode == kTreeAllReduce ? R >= 4 && R != 8 : R >= 16;
+}
+
 bool use_staged(int mode, int R, size_t bytesPerRank) {
   const size_t minBytes = (size_t)option(kOptStagedMinBytes);
+  // Trees that draw their tiles beat the register path earlier: above 8
+  // ranks from half the threshold (R = 12 / 16 bf16 at 8 MiB per rank: 0 /
+  // 5 % faster, at 12 MiB 9 / 12 %), and 5-7 ranks from 24 MiB (2-6 %
+  // faster there, 0-2 % slower at 16 MiB; 4 ranks stay 2-14 % slower below
+  // 32 MiB).
+  const bool drawnTree = mode == kTreeAllReduce && sched_tiles(mode, R);
   if (R < 8) {
-    if (small_geometry(mode, R).tile == 0 ||
-        bytesPerRank < std::max(minBytes, kSmallStagedMinBytes))
+    const size_t small =
+        drawnTree && R >= 5 ? kSmallStagedMinBytes * 3 / 4 : kSmallStagedMinBytes;
+    if (small_geometry(mode, R).tile == 0 || bytesPerRank < std::max(minBytes, small))
       return false;
-  } else if (bytesPerRank < minBytes) {
+  } else if (bytesPerRank < (drawnTree ? minBytes / 2 : minBytes)) {
     return false;
   }
   if (mode == kRingAllReduce) return true;
@@ -404,22 +428,6 @@ int sched_slot(int device, void* stream) {
   return used++;
 }
 
-// Whether a staged AllReduce of R ranks draws its tiles at run time
-// (VR_SCHED=1).  Measured against fixed runs on one GB300 (16-256 MiB per
-// rank): trees 1-5 % faster for 4-7 ranks, 12-16 % for 9-16 (4 KB tiles),
-// 10-12 % for 17-64; rings 12-15 % faster for 16-33 ranks, 8 % for 48 and
-// 1 % for 64 (whose fold, a loop over 64 rotated ranks in 3 consumer warps,
-// bounds it).  Slower: 2-3 rank trees (9 %), 8 ranks (trees 7-13 %, rings
-// 22 %: the one geometry with both 2 KB tiles and a deep pipeline, 13
-// stages, where the SMs' rates stay even and each tile's drawn index costs
-// the consumers a shared-memory round trip on one unit of work per thread),
-// and 9-12 rank rings (0-2 %); 3-7 rank rings are within 2 % either way.
-bool sched_tiles(int mode, int R) {
-  const long long o = option(kOptSched);
-  if (o == 0) return false;
-  if (o >= 2) return true;
-  return mode == kTreeAllReduce ? R >= 4 && R != 8 : R >= 16;
-}
 
 // Staged geometry: tiles of tileUnits 16-byte units per rank; as many stages
 // (at most 16) as fit in the opt-in shared memory; up to 7 consumer warps.

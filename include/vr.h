@@ -67,7 +67,10 @@
  *                                   touching memory)
  *   VR_STAGED_MIN_BYTES=n           staged kernel from n bytes per rank
  *                                   (default 16 MiB; 2-7 ranks: from the
- *                                   larger of n and 32 MiB)
+ *                                   larger of n and 32 MiB; trees that draw
+ *                                   their tiles (VR_SCHED): above 8 ranks
+ *                                   from n / 2, 5-7 ranks from the larger
+ *                                   of n and 24 MiB)
  *   VR_STAGED_TILE_BYTES, VR_STAGED_STAGES, VR_STAGED_MIN_STAGES
  *                                   staged geometry: bytes per rank per
  *                                   tile, most stages, fewest stages
@@ -238,8 +241,9 @@ vr_result_t vr_ring_block(size_t count, vr_dtype_t dtype, int R, int nChannels,
  * loop and the chunk of a tree channel.
  * In place: sendbufs[r] == recvbufs[r] is allowed.
  * Buffers: any alignment.  16-byte aligned buffers run 16-byte units: from
- * 16 MiB per rank the ring and the tree with 8..64 ranks, and from 32 MiB
- * per rank those with 2..7 ranks (but the ring of 6), run on a kernel that
+ * 16 MiB per rank the ring and the tree with 8..64 ranks (the tree with
+ * 9..64 ranks from 8 MiB), and from 32 MiB per rank those with 2..7 ranks
+ * (the tree with 5..7 from 24 MiB; not the ring of 6), run on a kernel that
  * stages each tile of all R ranks in shared memory with bulk asynchronous
  * copies (the tree's fold specialised at run time, see vr_jit_status),
  * everything else on a kernel that loads the ranks' units into registers

@@ -57,9 +57,12 @@ def assert_exact(dst, want):
 
 
 # Staged-kernel sizes: 32 MiB per rank for 4-7 ranks (their staged
-# threshold), 16 MiB above.
+# threshold), 16 MiB above; trees that draw their tiles start at 24 MiB
+# (5-7 ranks) and 8 MiB (9 and more).
 FULL = [
     (4, 8 << 20, F32, SUM, 1, "normal"),
+    (6, 6 << 20, F32, SUM, 1, "normal"),      # 24 MiB: staged only when drawn
+    (12, 4 << 20, BF16, SUM, 1, "normal"),    # 8 MiB: staged only when drawn
     (5, 16 << 20, BF16, SUM, 1, "normal"),
     (7, 8 << 20, F32, MAX, 1, "normal"),
     (16, 8 << 20, F16, SUM, 1, "uniform"),
