@@ -333,12 +333,6 @@ SmallGeometry small_geometry(int mode, int R) {
 }
 constexpr size_t kSmallStagedMinBytes = 32u << 20;  // per rank, 2-7 ranks
 
-// Which kernel family serves an aligned AllReduce.  Below 16 MiB per rank
-// the staged kernel's pipeline does not fill.  Measured on GB300: from 16 MiB
-// per rank the staged kernel beats the register path for the ring of 8-64
-// ranks and, with its fold specialised at run time (jit.cc), for the tree of
-// 8-64 ranks (the interpreting staged tree is 2-3x slower than the register
-// path); with 2-7 ranks it wins from 32 MiB per rank with the geometry above.
 // Whether a staged AllReduce of R ranks draws its tiles at run time
 // (VR_SCHED=1).  Measured against fixed runs on one GB300 (16-256 MiB per
 // rank): trees 1-5 % faster for 4-7 ranks, 12-16 % for 9-16 (4 KB tiles),
@@ -356,6 +350,12 @@ bool sched_tiles(int mode, int R) {
   return mode == kTreeAllReduce ? R >= 4 && R != 8 : R >= 16;
 }
 
+// Which kernel family serves an aligned AllReduce.  Below 16 MiB per rank
+// the staged kernel's pipeline does not fill.  Measured on GB300: from 16 MiB
+// per rank the staged kernel beats the register path for the ring of 8-64
+// ranks and, with its fold specialised at run time (jit.cc), for the tree of
+// 8-64 ranks (the interpreting staged tree is 2-3x slower than the register
+// path); with 2-7 ranks it wins from 32 MiB per rank with the geometry above.
 bool use_staged(int mode, int R, size_t bytesPerRank) {
   const size_t minBytes = (size_t)option(kOptStagedMinBytes);
   // Trees that draw their tiles beat the register path earlier: above 8
@@ -427,7 +427,6 @@ int sched_slot(int device, void* stream) {
   g_streamSlots.emplace(key, used);
   return used++;
 }
-
 
 // Staged geometry: tiles of tileUnits 16-byte units per rank; as many stages
 // (at most 16) as fit in the opt-in shared memory; up to 7 consumer warps.
