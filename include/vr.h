@@ -102,7 +102,9 @@
  *                                   the captured launch's slot; the later
  *                                   one's CTAs wait (bounded) and report
  *                                   VR_ERR_TIMEOUT if it stays held.
- *                                   The same bits either way.
+ *                                   Slots per device: 1024 streams and
+ *                                   3072 captured launches; past them,
+ *                                   fixed runs.  The same bits either way.
  *   VR_DEBUG=GRAPH                  print every tree set, ring and channel
  *                                   partition a call plans to stderr, in
  *                                   the log formats of [Course13] "从 GRAPH
