@@ -101,7 +101,10 @@
  *                                   graph running at the same time share
  *                                   the captured launch's slot; the later
  *                                   one's CTAs wait (bounded) and report
- *                                   VR_ERR_TIMEOUT if it stays held.
+ *                                   VR_ERR_TIMEOUT if it stays held (a
+ *                                   slot so left held fails later drawing
+ *                                   calls on it the same way until
+ *                                   vr_debug_sched_slot frees it).
  *                                   Slots per device: 1024 streams and
  *                                   3072 captured launches; past them,
  *                                   fixed runs.  The same bits either way.
