@@ -50,6 +50,16 @@ def test_small_parity_cases_pass_under_bounds_checks():
     assert " passed" in r.stdout and "skipped" not in r.stdout.splitlines()[-1], r.stdout[-500:]
 
 
+def test_drawn_tiles_pass_under_bounds_checks():
+    """The staged kernels that draw their tiles (trees and rings, small and
+    ragged messages, ring blocks far smaller than a tile) under the checks."""
+    args = [sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", "-m", "gpu",
+            os.path.join("tests", "test_gpu_sched.py"), "-k", "small_and_ragged or many_blocks"]
+    r = subprocess.run(args, cwd=ROOT, env=ENV, capture_output=True, text=True, timeout=1500)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+    assert " passed" in r.stdout and "skipped" not in r.stdout.splitlines()[-1], r.stdout[-500:]
+
+
 SHRINK = r"""
 import numpy as np, torch, double_binary_tree_gb300 as vr, oracle, workloads
 assert vr.vr_debug_bounds_checked()
