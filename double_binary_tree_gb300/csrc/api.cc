@@ -333,21 +333,24 @@ SmallGeometry small_geometry(int mode, int R) {
 }
 constexpr size_t kSmallStagedMinBytes = 32u << 20;  // per rank, 2-7 ranks
 
-// Whether a staged AllReduce of R ranks draws its tiles at run time
-// (VR_SCHED=1).  Measured against fixed runs on one GB300 (16-256 MiB per
-// rank): trees 1-5 % faster for 4-7 ranks, 12-16 % for 9-16 (4 KB tiles),
-// 10-12 % for 17-64; rings 12-15 % faster for 16-33 ranks, 8 % for 48 and
-// 1 % for 64 (whose fold, a loop over 64 rotated ranks in 3 consumer warps,
-// bounds it).  Slower: 2-3 rank trees (9 %), 8 ranks (trees 7-13 %, rings
-// 22 %: the one geometry with both 2 KB tiles and a deep pipeline, 13
-// stages, where the SMs' rates stay even and each tile's drawn index costs
-// the consumers a shared-memory round trip on one unit of work per thread),
-// and 9-12 rank rings (0-2 %); 3-7 rank rings are within 2 % either way.
-bool sched_tiles(int mode, int R) {
+// Whether a staged AllReduce of R ranks of `dtype` draws its tiles at run
+// time (VR_SCHED=1).  Measured against fixed runs on one GB300 (16-256 MiB
+// per rank): trees 1-5 % faster for 4-7 ranks, 12-16 % for 9-16 (4 KB
+// tiles), 10-12 % for 17-64; rings 12-15 % faster for 16-33 ranks, 8 % for
+// 48 and 1 % for 64 (whose fold, a loop over 64 rotated ranks in 3 consumer
+// warps, bounds it), and for 9-15 ranks 13-19 % in fp32 but within 2 % in
+// fp16 (each 16-byte unit twice the elements to widen and add: the
+// consumers, not the SMs' copy rates, bound those).  Slower: 2-3 rank trees
+// (9 %), 8 ranks (trees 7-13 %, rings 22-24 %: the one geometry with both
+// 2 KB tiles and a deep pipeline, 13 stages, where the SMs' rates stay even
+// and each tile's drawn index costs the consumers a shared-memory round trip
+// on one unit of work per thread); 3-7 rank rings are within 2 % either way.
+bool sched_tiles(int mode, int R, int dtype) {
   const long long o = option(kOptSched);
   if (o == 0) return false;
   if (o >= 2) return true;
-  return mode == kTreeAllReduce ? R >= 4 && R != 8 : R >= 16;
+  if (mode == kTreeAllReduce) return R >= 4 && R != 8;
+  return R >= 16 || (R >= 9 && dtype == VR_FLOAT32);
 }
 
 // Which kernel family serves an aligned AllReduce.  Below 16 MiB per rank
@@ -363,7 +366,8 @@ bool use_staged(int mode, int R, size_t bytesPerRank) {
   // 5 % faster, at 12 MiB 9 / 12 %), and 5-7 ranks from 24 MiB (2-6 %
   // faster there, 0-2 % slower at 16 MiB; 4 ranks stay 2-14 % slower below
   // 32 MiB).
-  const bool drawnTree = mode == kTreeAllReduce && sched_tiles(mode, R);
+  // (the trees' drawing rule does not depend on the element type)
+  const bool drawnTree = mode == kTreeAllReduce && sched_tiles(mode, R, VR_FLOAT32);
   if (R < 8) {
     const size_t small =
         drawnTree && R >= 5 ? kSmallStagedMinBytes * 3 / 4 : kSmallStagedMinBytes;
@@ -591,7 +595,7 @@ vr_result_t launch_allreduce_range(KArgs& a, int dtype, int mode, int op, int st
   // A staged AllReduce draws its tiles through its stream's scheduler slot
   // where that measured faster (staged.cuh).
   a.sched = nullptr;
-  if (staged && sched_tiles(mode, a.R)) {
+  if (staged && sched_tiles(mode, a.R, dtype)) {
     DeviceInfo di;
     int device = 0;
     const vr_result_t e = device_info(&di, &device);

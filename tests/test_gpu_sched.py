@@ -63,6 +63,7 @@ FULL = [
     (4, 8 << 20, F32, SUM, 1, "normal"),
     (6, 6 << 20, F32, SUM, 1, "normal"),      # 24 MiB: staged only when drawn
     (12, 4 << 20, BF16, SUM, 1, "normal"),    # 8 MiB: staged only when drawn
+    (12, 4 << 20, F32, MAX, 1, "normal"),     # 16 MiB: fp32 rings of 9-15 ranks draw
     (5, 16 << 20, BF16, SUM, 1, "normal"),
     (7, 8 << 20, F32, MAX, 1, "normal"),
     (16, 8 << 20, F16, SUM, 1, "uniform"),
