@@ -323,7 +323,12 @@ struct SmallGeometry {
   unsigned tile;
   int stages;
 };
-SmallGeometry small_geometry(int mode, int R) {
+// `drawn`: the geometry of a launch that draws its tiles, where it differs --
+// the 4-rank ring: 12 KB x 3 (0.965 of the copy bandwidth at 64 MiB per rank
+// against 0.92 with 8 KB x 4 drawn and 0.93 with fixed runs; 12 KB x 3 with
+// fixed runs 0.86).
+SmallGeometry small_geometry(int mode, int R, bool drawn = false) {
+  if (drawn && mode == kRingAllReduce && R == 4) return {12288, 3};
   static const SmallGeometry ring[8] = {{0, 0},    {0, 0},    {0, 0},    {14336, 3},
                                         {8192, 4}, {6144, 3}, {0, 0},    {4096, 4}};
   static const SmallGeometry tree[8] = {{0, 0},    {0, 0},    {14336, 4}, {8192, 4},
@@ -340,17 +345,19 @@ constexpr size_t kSmallStagedMinBytes = 32u << 20;  // per rank, 2-7 ranks
 // 48 and 1 % for 64 (whose fold, a loop over 64 rotated ranks in 3 consumer
 // warps, bounds it), and for 9-15 ranks 13-19 % in fp32 but within 2 % in
 // fp16 (each 16-byte unit twice the elements to widen and add: the
-// consumers, not the SMs' copy rates, bound those).  Slower: 2-3 rank trees
-// (9 %), 8 ranks (trees 7-13 %, rings 22-24 %: the one geometry with both
-// 2 KB tiles and a deep pipeline, 13 stages, where the SMs' rates stay even
-// and each tile's drawn index costs the consumers a shared-memory round trip
-// on one unit of work per thread); 3-7 rank rings are within 2 % either way.
+// consumers, not the SMs' copy rates, bound those); the 4-rank fp32 ring,
+// with larger tiles (small_geometry), 4-5 % at 32-256 MiB per rank.
+// Slower: 2-3 rank trees (9 %), 8 ranks (trees 7-13 %, rings 22-24 %: the
+// one geometry with both 2 KB tiles and a deep pipeline, 13 stages, where the
+// SMs' rates stay even and each tile's drawn index costs the consumers a
+// shared-memory round trip on one unit of work per thread); 3, 5 and 7 rank
+// rings are within 2 % either way with their fixed-run geometry.
 bool sched_tiles(int mode, int R, int dtype) {
   const long long o = option(kOptSched);
   if (o == 0) return false;
   if (o >= 2) return true;
   if (mode == kTreeAllReduce) return R >= 4 && R != 8;
-  return R >= 16 || (R >= 9 && dtype == VR_FLOAT32);
+  return R >= 16 || ((R == 4 || R >= 9) && dtype == VR_FLOAT32);
 }
 
 // Which kernel family serves an aligned AllReduce.  Below 16 MiB per rank
@@ -396,9 +403,9 @@ bool use_staged_rs(int R, int dtype, size_t sendBytesPerRank) {
 // Per-rank tile bytes of the staged kernel (bulk copies below 2 KB lose
 // throughput; 4 KB measured best for 9..16 ranks; ReduceScatter: 64 KB stages
 // up to 16 KB per rank).
-unsigned staged_tile_bytes(int R, int mode) {
+unsigned staged_tile_bytes(int R, int mode, bool drawn) {
   if (mode == kReduceScatter) return std::min(16384u, (65536u / (unsigned)R) & ~15u);
-  if (R < 8 && small_geometry(mode, R).tile) return small_geometry(mode, R).tile;
+  if (R < 8 && small_geometry(mode, R, drawn).tile) return small_geometry(mode, R, drawn).tile;
   return R > 8 && R <= 16 ? 4096u : 2048u;
 }
 
@@ -469,7 +476,7 @@ vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
   // three smaller ones: measured 2.5% (tree) to 20% (ring) faster at 64.
   int minStages = (int)option_or(kOptStagedMinStages, a.R > 32 ? 2 : 3);
   if (!tb) {
-    tb = staged_tile_bytes(a.R, mode);
+    tb = staged_tile_bytes(a.R, mode, a.sched != nullptr);
     if (a.R > 32 && mode != kReduceScatter)  // the largest 512-byte multiple that fits
       tb = std::max(512u, ((unsigned)(room / (minStages * a.R))) & ~511u);
     while (tb > 512 && (long long)a.R * tb * minStages > room) tb -= 512;
@@ -483,8 +490,9 @@ vr_result_t launch_staged(const void* fn, KArgs& a, int mode, void* stream) {
   const int fit = room / (int)a.stageBytes;
   a.stages = std::min(kStagedMaxStages, fit);
   int cap = (int)option(kOptStagedStages);
-  if (!cap && a.R < 8 && mode != kReduceScatter && (unsigned)tb == small_geometry(mode, a.R).tile)
-    cap = small_geometry(mode, a.R).stages;  // the few-rank geometry's short pipeline
+  const SmallGeometry sg = small_geometry(mode, a.R, a.sched != nullptr);
+  if (!cap && a.R < 8 && mode != kReduceScatter && (unsigned)tb == sg.tile)
+    cap = sg.stages;  // the few-rank geometry's short pipeline
   if (cap) a.stages = std::min(a.stages, cap);
   if (a.stages < 2) return VR_ERR_INTERNAL;
   a.consumers = std::max(1, std::min(kStagedMaxConsumers, a.tileUnits / 32));

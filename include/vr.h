@@ -91,7 +91,8 @@
  *                                   CTAs draw tiles at run time where that
  *                                   measured faster (trees of 4 or more
  *                                   ranks, 8 excepted; rings of 16 or
- *                                   more, and fp32 rings of 9 or more);
+ *                                   more, and fp32 rings of 4 and of 9
+ *                                   or more);
  *                                   2 always drawn.
  *                                   Drawing uses a scheduler slot in
  *                                   device memory per stream, and one per
