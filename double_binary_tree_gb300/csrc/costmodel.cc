@@ -17,7 +17,7 @@ std::mutex g_modelMu;
 // The alpha-beta cost model: built-in constants fitted on GB300 with
 // vr_fit_cost_model to the measured times of 4 ranks, 8 B .. 256 MiB per rank
 // (bench.py --sweep); replaceable through vr_set_cost_model.
-const vr_cost_model_t kBuiltinModel = {{0.344687, 0.474346}, {8.93019e-7, 6.13249e-7}};
+const vr_cost_model_t kBuiltinModel = {{0.343939, 0.473172}, {8.66964e-7, 6.13639e-7}};
 vr_cost_model_t g_model = kBuiltinModel;
 
 // Exact depth (edges from the root to the deepest leaf) of one tree.
