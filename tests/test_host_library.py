@@ -31,6 +31,21 @@ def test_exports_every_declared_symbol():
     assert declared == set(vr.EXPORTED)
 
 
+def test_every_option_is_documented_and_settable():
+    """The option table of the library (options.cc) and the header's option
+    list name the same switches, and each can be read through the API."""
+    src = open(os.path.join(ROOT, "double_binary_tree_gb300", "csrc", "options.cc"),
+               encoding="utf-8").read()
+    table = src[src.index("kSpecs[kOptCount] = {"):]
+    table = table[:table.index("};")]
+    names = re.findall(r'"(VR_[A-Z_]+)"', table)
+    assert len(names) == len(set(names)) >= 16
+    header = open(os.path.join(ROOT, "include", "vr.h"), encoding="utf-8").read()
+    for name in names:
+        assert name in header, name
+        vr.vr_get_option(name)
+
+
 @pytest.mark.parametrize("nch", [1, 2, 12, 24, 64])
 def test_ring_matches_oracle(nch):
     for R in range(1, 65):
